@@ -1,0 +1,410 @@
+"""Benchmark: KDA forward-recompute + backward tokens/s on GB300.
+
+One step = one ``kda_chunk_bwd`` call with ``states = NULL`` (the call
+recomputes the chunk forward it needs, then runs the whole backward) over the
+bf16 workload B=8, T=4096, H=HV=32, K=V=128, chunk 64 (seeded synthetic
+inputs; see kda_inputs.py). Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+* ``value``: device-timed tokens/s (inputs resident in HBM; K steps between
+  CUDA events, barrier + synchronize on both sides, max over ranks). The
+  per-step working set (~10 GB) is far larger than the 129 MB L2, so no flush
+  is needed between steps.
+* ``e2e``: the same metric through the C ABI from pinned host buffers: every
+  step copies the inputs host->device, runs the call, and copies every
+  gradient back.
+* ``roofline``: the dominant kernel's algorithmic bytes (or FLOPs) per launch
+  over its average launch time, measured with CUDA events that the library
+  records between its own launches on the call's stream.
+* ``cpu_baseline``: the fp64 oracle on the host cores on a bounded sample of
+  the same workload (whole sequences x heads), scaled to tokens/s.
+* ``--impl reference``: the fp64 oracle timed as the reference arm.
+
+Multi-GPU (torchrun): every rank runs the full workload on its own GPU (weak
+scaling, independent batches, no data-path collective); ``value`` is the sum
+of tokens over ranks divided by the max over ranks of the timed span.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_inputs  # noqa: E402
+
+WORKLOAD = "bf16_b8_t4096_h32_k128"
+METRIC = "KDA fwd-recompute+bwd tokens/s on 1 GB300 and % of roofline vs CPU oracle"
+UNIT = "tokens/s"
+
+# ----------------------------------------------------------------------------
+# Algorithmic cost model (per launch) of each kernel, from the problem sizes.
+# Bytes count what the step must read/write at its dtype, plus the fp32 chunk
+# state written once and read once; FLOPs count each dense product once.
+# ----------------------------------------------------------------------------
+
+
+def step_cost(B, T, H, HV, K, V, in_bytes=2, C=64):
+    th = B * T * HV  # token-heads
+    tk = B * T * H
+    nck = B * ((T + C - 1) // C) * HV
+    io_in = tk * K * in_bytes * 2 + th * V * in_bytes * 2 + th * K * 4 + th * in_bytes
+    io_out = tk * K * in_bytes * 2 + th * V * in_bytes + th * K * 4 + th * in_bytes
+    states = 2 * nck * K * V * 4
+    flops = nck * (16 * C * K * V + 9 * C * C * K + 5 * C * C * V + C ** 3)
+    return dict(bytes=io_in + io_out + states, flops=flops, io_in=io_in, io_out=io_out, states=states, nck=nck)
+
+
+def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
+    """(bound, algorithmic bytes, algorithmic flops) of one launch of kernel ``name``."""
+    s = step_cost(B, T, H, HV, K, V, in_bytes, C)
+    nck = s["nck"]
+    th = B * T * HV
+    tk = B * T * H
+    st = nck * K * V * 4  # one pass over the fp32 chunk states
+    if name == "simt_intra":
+        b = tk * K * in_bytes * 2 + th * (V * in_bytes + K * 4 + in_bytes)
+        f = nck * (4 * C * C * K + 2 * C * C * (K + V) + C ** 3 // 3)
+        return "alu", b, f
+    if name == "simt_state_fwd":
+        return "alu", st + tk * K * in_bytes, nck * 4 * C * K * V
+    if name == "simt_ds_rev":
+        return "alu", th * V * in_bytes + tk * K * in_bytes * 2, nck * (6 * C * K * V + 2 * C * C * V)
+    if name == "simt_grads_a":
+        return "alu", 2 * st + th * V * in_bytes, nck * 6 * C * K * V
+    if name == "simt_grads_b":
+        b = s["io_out"] + tk * K * in_bytes * 2 + th * (2 * V * in_bytes + in_bytes)
+        f = nck * (6 * C * C * V + 10 * C * C * K + 4 * C ** 3)
+        return "alu", b, f
+    if name == "gva_reduce":
+        return "hbm", th * K * 4 * 2 + tk * K * in_bytes * 2, 0
+    return "hbm", s["bytes"], s["flops"]
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def alu_peak_tflops(sm_mhz):
+    """FP32 FFMA peak: 152 SMs x 128 FP32 lanes x 2 FLOP x clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        mhz, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [m for m, p in zip(mhz, power) if p > 0.3 * max(power)] or mhz
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(mhz), "power_w_max": max(power)}
+
+
+# ----------------------------------------------------------------------------
+# distributed helpers
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, device) -> float:
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate(tokens_per_rank: int, elapsed_s: float, world: int, device) -> tuple:
+    """Whole-job tokens/s: every rank processed ``tokens_per_rank``; time is the max over ranks."""
+    t = max_over_ranks(elapsed_s, device)
+    return tokens_per_rank * world / t, t
+
+
+# ----------------------------------------------------------------------------
+# the CPU oracle leg
+# ----------------------------------------------------------------------------
+
+def oracle_sample(inp, n_seqs, n_heads):
+    """Time the fp64 oracle on ``n_seqs`` whole sequences x ``n_heads`` key heads (all host cores)."""
+    import oracle
+
+    H = inp.q.shape[2]
+    HV = inp.v.shape[2]
+    G = HV // H
+    T = inp.T
+    sl = lambda x, hs: x[:n_seqs, :, hs].contiguous()
+    hs, vs = slice(0, n_heads), slice(0, n_heads * G)
+    args = (sl(inp.q, hs), sl(inp.k, hs), sl(inp.v, vs), sl(inp.g, vs), sl(inp.beta, vs), inp.scale,
+            None if inp.h0 is None else inp.h0[:n_seqs, vs].contiguous(), sl(inp.do, vs),
+            None if inp.dht is None else inp.dht[:n_seqs, vs].contiguous())
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    used = min(cores, n_seqs * n_heads)
+    t0 = time.perf_counter()
+    oracle.run(*args, nthreads=used)
+    dt = time.perf_counter() - t0
+    # tokens/s of the full-width problem: token-heads processed / heads / time
+    token_heads = n_seqs * T * n_heads
+    return token_heads / H / dt, used, dt, f"{n_seqs} sequence(s) x {n_heads} of {H} key heads x {T} tokens"
+
+
+def reference_arm(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    inp = kda_inputs.workload(WORKLOAD)
+    n_seqs, n_heads = 1, 16
+    vals = []
+    for _ in range(args.warmup):
+        oracle_sample(inp, n_seqs, n_heads)
+    used = 0
+    sample = ""
+    for _ in range(args.steps):
+        v, used, dt, sample = oracle_sample(inp, n_seqs, n_heads)
+        vals.append(v)
+    value = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": 8, "seq_len": 4096, "heads": 32, "head_dim": 128,
+                       "chunk": 64},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def gpu_arm(args):
+    import chunked_gated_delta_10_gb300 as kda
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    kda.build()
+    lib = kda.load()
+
+    inp = kda_inputs.workload(WORKLOAD)
+    B, T, H, K = inp.q.shape
+    HV, V = inp.v.shape[2], inp.v.shape[3]
+    tokens = B * T
+    host = dict(q=inp.q, k=inp.k, v=inp.v, g=inp.g, beta=inp.beta, do=inp.do)
+    x = {n: t.to(device).contiguous() for n, t in host.items()}
+    dims = kda.make_dims(x["q"], x["v"], inp.scale)
+    wsb = kda.workspace_bytes(dims, kda.PASS_BWD)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+    out = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+               dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]), dh0=None)
+    stream = torch.cuda.current_stream(device)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+
+    def step(inputs, outs):
+        rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]), P(inputs["g"]),
+                               P(inputs["beta"]), None, None, None, None, P(inputs["do"]), None, None,
+                               P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]), None,
+                               P(ws), wsb, sptr)
+        if rc != 0:
+            raise kda.KdaError(rc, "kda_chunk_bwd")
+
+    for _ in range(args.warmup):
+        step(x, out)
+    torch.cuda.synchronize(device)
+    launches = int(lib.kda_last_launch_count())
+    names = [lib.kda_launch_name(i).decode() for i in range(launches)]
+
+    # -- device-timed region, with per-launch events recorded by the library --
+    nev = launches + 1
+    ev_sets = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    clocks = ClockSampler(device.index)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    time.sleep(0.3)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(args.steps):
+        handles = (ctypes.c_void_p * nev)(*[e.cuda_event for e in ev_sets[i]])
+        for e in ev_sets[i]:
+            e.record(stream)  # materialise the event objects (re-recorded by the library below)
+        lib.kda_set_profile_events(handles, nev)
+        step(x, out)
+    lib.kda_set_profile_events(None, 0)
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clk = clocks.stop()
+    elapsed = start.elapsed_time(stop) / 1e3
+    value, tmax = aggregate(tokens * args.steps, elapsed, world, device)
+
+    per = {n: [] for n in names}
+    for evs in ev_sets:
+        for i, n in enumerate(names):
+            per[n].append(evs[i].elapsed_time(evs[i + 1]) / 1e3)
+    tot = {n: sum(v) for n, v in per.items()}
+    dom = max(tot, key=tot.get)
+    avg = tot[dom] / len(per[dom])
+    peaks, peak_src = load_peaks()
+    bound, abytes, aflops = kernel_cost(dom, B, T, H, HV, K, V)
+    if bound == "hbm":
+        ach, pk, unit = abytes / avg / 1e9, peaks["hbm_gbs"], "GB/s"
+    elif bound == "tensor":
+        ach, pk, unit = aflops / avg / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
+    else:
+        ach, pk, unit = aflops / avg / 1e12, alu_peak_tflops(clk.get("sm_mhz") or peaks["sm_max_mhz"]), "TFLOP/s"
+    roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
+                "traffic": None, "peak_source": peak_src if bound != "alu" else "152 SMs x 128 FFMA lanes x SM clock",
+                "avg_launch_ms": avg * 1e3, "share": tot[dom] / sum(tot.values()),
+                "kernels_ms": {n: 1e3 * tot[n] / len(per[n]) for n in names}}
+    sc = step_cost(B, T, H, HV, K, V)
+    step_s = elapsed / args.steps
+    path = {"bytes_alg": sc["bytes"], "flops_alg": sc["flops"],
+            "hbm_frac": sc["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
+            "tensor_frac": sc["flops"] / step_s / 1e12 / peaks["bf16_tflops_sustained"]}
+
+    # -- end to end through the C ABI from pinned host buffers --
+    hin = {n: t.pin_memory() for n, t in host.items()}
+    hout = {n: torch.empty(out[n].shape, dtype=out[n].dtype, pin_memory=True) for n in ("dq", "dk", "dv", "dg", "dbeta")}
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n in hin:
+            x[n].copy_(hin[n], non_blocking=True)
+        step(x, out)
+        for n in hout:
+            hout[n].copy_(out[n], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_val, _ = aggregate(tokens * e2e_steps, e0.elapsed_time(e1) / 1e3, world, device)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
+                       "head_dim": K, "chunk": 64, "parallelism": f"dp{world}" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (about 10 GB touched per step), no flush"},
+            "roofline": roofline, "path": path, "clocks": clk, "gpu_launches": launches * args.steps,
+            "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps}}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, used, dt, sample = oracle_sample(inp, 1, 16)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
+                                "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,265 @@
+// C-ABI layer of the KDA library: argument validation, workspace carving and
+// launch sequencing. Declared in include/kda.h. Nothing here allocates device
+// memory or synchronises (except kda_device_status, which is documented to).
+#include <string.h>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Validate dims; fills the device-side problem description (pointers unset).
+kda_status check_dims(const kda_dims* d, Prob* p) {
+    if (!d) return KDA_ERR_INVALID_ARG;
+    if (d->B < 1 || d->T < 0 || d->H < 1 || d->HV < 1 || d->HV % d->H != 0) return KDA_ERR_INVALID_ARG;
+    if (d->chunk != kC) return KDA_ERR_UNSUPPORTED;
+    if (!((d->K == 64 || d->K == 128) && (d->V == 64 || d->V == 128))) return KDA_ERR_UNSUPPORTED;
+    if (d->dtype != KDA_DTYPE_BF16 && d->dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (d->num_seqs < 1 || d->num_chunks < 0) return KDA_ERR_INVALID_ARG;
+    if (d->HV > 65535 || d->num_seqs > 2147483647 || d->num_chunks > 2147483647) return KDA_ERR_UNSUPPORTED;
+    memset(p, 0, sizeof(*p));
+    p->B = d->B;
+    p->T = d->T;
+    p->H = d->H;
+    p->HV = d->HV;
+    p->K = d->K;
+    p->V = d->V;
+    p->N = d->num_seqs;
+    p->NT = d->num_chunks;
+    p->NTs = (d->T + kC - 1) / kC;
+    p->scale = d->scale;
+    return KDA_OK;
+}
+
+struct Layout {
+    size_t status, gam, w, u, vn, inv, aqk, sin, dso, dvn, dqt, dkh, dw, dgc, dqp, dkp, total;
+};
+
+Layout layout(const Prob& p, int pass) {
+    Layout L;
+    memset(&L, 0, sizeof(L));
+    const size_t R = (size_t)p.B * p.T, HV = p.HV, K = p.K, V = p.V, NT = (size_t)p.NT, f = sizeof(float);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    L.status = take(kAlign);
+    L.gam = take(R * HV * K * f);
+    L.w = take(R * HV * K * f);
+    L.u = take(R * HV * V * f);
+    L.vn = take(R * HV * V * f);
+    L.inv = take(NT * HV * kC * kC * f);
+    L.aqk = take(NT * HV * kC * kC * f);
+    if (pass == KDA_PASS_BWD) {
+        L.sin = take(NT * HV * K * V * f);
+        L.dso = take(NT * HV * K * V * f);
+        L.dvn = take(R * HV * V * f);
+        L.dqt = take(R * HV * K * f);
+        L.dkh = take(R * HV * K * f);
+        L.dw = take(R * HV * K * f);
+        L.dgc = take(NT * HV * K * f);
+        if (p.HV != p.H) {
+            L.dqp = take(R * HV * K * f);
+            L.dkp = take(R * HV * K * f);
+        }
+    }
+    L.total = off;
+    return L;
+}
+
+Ws carve(void* base, const Layout& L) {
+    char* b = (char*)base;
+    Ws w;
+    memset(&w, 0, sizeof(w));
+    auto at = [&](size_t off) { return (float*)(b + off); };
+    w.status = (int*)(b + L.status);
+    w.gam = at(L.gam);
+    w.w = at(L.w);
+    w.u = at(L.u);
+    w.vn = at(L.vn);
+    w.inv = at(L.inv);
+    w.aqk = at(L.aqk);
+    if (L.sin) {
+        w.sin = at(L.sin);
+        w.dso = at(L.dso);
+        w.dvn = at(L.dvn);
+        w.dqt = at(L.dqt);
+        w.dkh = at(L.dkh);
+        w.dw = at(L.dw);
+        w.dgc = at(L.dgc);
+        if (L.dqp) {
+            w.dqp = at(L.dqp);
+            w.dkp = at(L.dkp);
+        }
+    }
+    return w;
+}
+
+// Shared checks of the forward and backward inputs.
+kda_status check_common(const kda_dims* dims, Prob* p, const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, const float* h0, const int64_t* cu, const int32_t* cidx,
+                        const int64_t* coff, void* ws, size_t ws_bytes, int pass) {
+    kda_status s = check_dims(dims, p);
+    if (s != KDA_OK) return s;
+    const bool packed = cu != nullptr;
+    if (packed != (cidx != nullptr) || packed != (coff != nullptr)) return KDA_ERR_INVALID_ARG;
+    if (packed) {
+        if (dims->B != 1) return KDA_ERR_INVALID_ARG;
+    } else {
+        if (dims->num_seqs != dims->B || dims->num_chunks != (int64_t)dims->B * p->NTs) return KDA_ERR_INVALID_ARG;
+    }
+    const size_t rows = (size_t)dims->B * dims->T;
+    if (rows > 0 && (!q || !k || !v || !g || !beta)) return KDA_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, beta, h0, cu, cidx, coff};
+    for (const void* x : ptrs)
+        if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
+    if (!ws || !aligned16(ws) || ws_bytes < layout(*p, pass).total) return KDA_ERR_WORKSPACE;
+    p->cu = cu;
+    p->cidx = cidx;
+    p->coff = coff;
+    return KDA_OK;
+}
+
+constexpr int kMaxLaunches = 64;
+void* const* g_prof_events = nullptr;
+int g_prof_n = 0;
+thread_local const char* t_names[kMaxLaunches];
+thread_local int t_count = 0;
+
+}  // namespace
+
+void begin_launches(cudaStream_t st) {
+    t_count = 0;
+    if (g_prof_n > 0) cudaEventRecord((cudaEvent_t)g_prof_events[0], st);
+}
+
+void note_launch(const char* name, cudaStream_t st) {
+    if (t_count < kMaxLaunches) t_names[t_count] = name;
+    ++t_count;
+    if (t_count < g_prof_n) cudaEventRecord((cudaEvent_t)g_prof_events[t_count], st);
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_set_profile_events(void* const* events, int32_t n_events) {
+    if (n_events < 0 || (n_events > 0 && !events)) return KDA_ERR_INVALID_ARG;
+    g_prof_events = n_events > 0 ? events : nullptr;
+    g_prof_n = n_events;
+    return KDA_OK;
+}
+
+extern "C" int32_t kda_last_launch_count(void) { return t_count; }
+
+extern "C" const char* kda_launch_name(int32_t i) {
+    return (i >= 0 && i < t_count && i < kMaxLaunches) ? t_names[i] : nullptr;
+}
+
+extern "C" const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid size, pointer, alignment or cu_seqlens";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: valid but unsupported configuration";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: a CUDA call or kernel launch failed";
+        case KDA_ERR_DEVICE_TIMEOUT: return "KDA_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+    }
+    return "unknown kda_status";
+}
+
+extern "C" kda_status kda_prepare_chunks(const int64_t* cu, int32_t num_seqs, int32_t chunk, int32_t* chunk_idx,
+                                         int64_t* chunk_off, int64_t* num_chunks) {
+    if (!cu || !num_chunks || num_seqs < 1 || chunk != kC || cu[0] != 0) return KDA_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int32_t n = 0; n < num_seqs; ++n) {
+        if (cu[n + 1] < cu[n]) return KDA_ERR_INVALID_ARG;
+        const int64_t nt = (cu[n + 1] - cu[n] + kC - 1) / kC;
+        if (chunk_off) chunk_off[n] = total;
+        if (chunk_idx)
+            for (int64_t i = 0; i < nt; ++i) {
+                chunk_idx[2 * (total + i)] = n;
+                chunk_idx[2 * (total + i) + 1] = (int32_t)i;
+            }
+        total += nt;
+    }
+    if (chunk_off) chunk_off[num_seqs] = total;
+    *num_chunks = total;
+    return KDA_OK;
+}
+
+extern "C" size_t kda_workspace_bytes(const kda_dims* dims, int32_t pass) {
+    Prob p;
+    if (check_dims(dims, &p) != KDA_OK || (pass != KDA_PASS_FWD && pass != KDA_PASS_BWD)) return 0;
+    return layout(p, pass).total;
+}
+
+extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                    const float* g, const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                    const int32_t* chunk_idx, const int64_t* chunk_off, void* o, float* ht,
+                                    float* states, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    Prob p;
+    kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, ws, ws_bytes,
+                                KDA_PASS_FWD);
+    if (s != KDA_OK) return s;
+    if ((size_t)dims->B * dims->T > 0 && !o) return KDA_ERR_INVALID_ARG;
+    for (const void* x : {(const void*)o, (const void*)ht, (const void*)states})
+        if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
+    const Layout L = layout(p, KDA_PASS_FWD);
+    Ws w = carve(ws, L);
+    cudaStream_t st = (cudaStream_t)stream;
+    IO io;
+    memset(&io, 0, sizeof(io));
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.g = g; io.h0 = h0;
+    io.o = o; io.ht = ht; io.states_out = states;
+    if (cudaMemsetAsync(w.status, 0, kAlign, st) != cudaSuccess) return KDA_ERR_CUDA;
+    begin_launches(st);
+    if (simt_fwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                    const float* g, const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                    const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
+                                    const float* dht, const float* states, void* dq, void* dk, void* dv, float* dg,
+                                    void* dbeta, float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    Prob p;
+    kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, ws, ws_bytes,
+                                KDA_PASS_BWD);
+    if (s != KDA_OK) return s;
+    if (dh0 && !h0) return KDA_ERR_INVALID_ARG;
+    if ((size_t)dims->B * dims->T > 0 && (!d_o || !dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+    for (const void* x : {(const void*)d_o, (const void*)dht, (const void*)states, (const void*)dq,
+                          (const void*)dk, (const void*)dv, (const void*)dg, (const void*)dbeta, (const void*)dh0})
+        if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
+    if (states) return KDA_ERR_UNSUPPORTED;
+    const Layout L = layout(p, KDA_PASS_BWD);
+    Ws w = carve(ws, L);
+    cudaStream_t st = (cudaStream_t)stream;
+    IO io;
+    memset(&io, 0, sizeof(io));
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht;
+    io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0;
+    if (cudaMemsetAsync(w.status, 0, kAlign, st) != cudaSuccess) return KDA_ERR_CUDA;
+    begin_launches(st);
+    if (simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+extern "C" kda_status kda_device_status(const void* ws, kda_stream_t stream) {
+    if (!ws) return KDA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    return word == 0 ? KDA_OK : KDA_ERR_DEVICE_TIMEOUT;
+}

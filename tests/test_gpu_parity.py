@@ -1,0 +1,191 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the fp64
+oracle on the same seeded inputs.
+
+Tolerances (per-tensor relative L2, oracle rounded to the output dtype):
+5e-3 for bf16 inputs (bf16 tensor-core operands, fp32 accumulation) and 1e-4
+for fp32 inputs. Small cases are compared in full; the full-size workloads are
+compared on whole independent units (one sequence x one key head and its value
+heads), which the oracle computes exactly, at the sizes and launch
+configuration the benchmark times.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs
+import oracle
+from tests.util import TOL, rel_l2, round_like, to64
+
+pytestmark = pytest.mark.gpu
+
+GRADS = ("dq", "dk", "dv", "dg", "dbeta", "dh0")
+
+
+@pytest.fixture(scope="session")
+def kda():
+    import chunked_gated_delta_10_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    m.build()
+    m.load()
+    return m
+
+
+def _cuda(inp):
+    c = lambda t: None if t is None else t.cuda().contiguous()
+    return dict(q=c(inp.q), k=c(inp.k), v=c(inp.v), g=c(inp.g), beta=c(inp.beta), h0=c(inp.h0), do=c(inp.do),
+                dht=c(inp.dht))
+
+
+def gpu_bwd(kda, inp, states=None):
+    x = _cuda(inp)
+    out = kda.chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], scale=inp.scale, h0=x["h0"],
+                        dht=x["dht"], cu_seqlens=inp.cu_seqlens, states=states)
+    torch.cuda.synchronize()
+    return out
+
+
+def gpu_fwd(kda, inp):
+    x = _cuda(inp)
+    o, ht, st = kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], scale=inp.scale, h0=x["h0"],
+                              cu_seqlens=inp.cu_seqlens)
+    torch.cuda.synchronize()
+    return o, ht, st
+
+
+def _tol(inp):
+    return TOL[inp.spec.dtype]
+
+
+def _check(name, got, ref64, out_dtype, tol, errs):
+    e = rel_l2(to64(got), round_like(ref64, out_dtype))
+    errs[name] = e
+    assert e <= tol, (name, e, tol)
+
+
+def compare_full(inp, out, ref):
+    dt, tol, errs = inp.torch_dtype, _tol(inp), {}
+    for key in ("dq", "dk", "dv", "dbeta"):
+        _check(key, out[key], ref[key], dt, tol, errs)
+    _check("dg", out["dg"], ref["dg"], torch.float32, tol, errs)
+    if inp.h0 is not None:
+        _check("dh0", out["dh0"], ref["dh0"], torch.float32, tol, errs)
+    return errs
+
+
+def compare_unit(inp, out, n, h):
+    """Compare one (sequence n, key head h) unit against the oracle."""
+    ref = oracle.run_unit(inp, n, h)
+    b, e = inp.seq_bounds[n]
+    H, HV = inp.q.shape[2], inp.v.shape[2]
+    G = HV // H
+    rows = lambda t, hs: t.reshape(-1, *t.shape[2:])[b:e, hs].unsqueeze(0)
+    sl = dict(dq=rows(out["dq"], slice(h, h + 1)), dk=rows(out["dk"], slice(h, h + 1)),
+              dv=rows(out["dv"], slice(h * G, h * G + G)), dg=rows(out["dg"], slice(h * G, h * G + G)),
+              dbeta=rows(out["dbeta"], slice(h * G, h * G + G)))
+    if inp.h0 is not None:
+        sl["dh0"] = out["dh0"][n:n + 1, h * G:h * G + G]
+    return compare_full(inp, sl, ref)
+
+
+# ---------------------------------------------------------------- small cases
+
+SMALL = {
+    "t1": dict(B=1, T=1, H=1, HV=1, K=64, V=64),
+    "t63": dict(B=2, T=63, H=2, HV=2, K=64, V=64),
+    "t64": dict(B=1, T=64, H=1, HV=2, K=128, V=128),
+    "t65": dict(B=1, T=65, H=2, HV=2, K=64, V=128),
+    "t200_gva": dict(B=2, T=200, H=2, HV=4, K=128, V=64),
+    "varlen_empty": dict(B=1, T=0, H=2, HV=2, K=64, V=64, seq_lens=[5, 0, 70, 129, 1]),
+    "no_state": dict(B=1, T=150, H=1, HV=1, K=128, V=128, h0=False, dht=False),
+}
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_cases_full(kda, name, dtype):
+    inp = kda_inputs.small(seed=31, dtype=dtype, **SMALL[name])
+    out = gpu_bwd(kda, inp)
+    compare_full(inp, out, oracle.run_inputs(inp))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("name", ["t65", "t200_gva", "varlen_empty"])
+def test_forward_outputs_and_states(kda, name, dtype):
+    inp = kda_inputs.small(seed=32, dtype=dtype, **SMALL[name])
+    o, ht, st = gpu_fwd(kda, inp)
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    tol = _tol(inp)
+    assert rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)) <= tol
+    assert rel_l2(to64(ht), ref["ht"]) <= tol
+    assert rel_l2(to64(st), ref["s_in"]) <= tol
+
+
+# ------------------------------------------------------- the five workloads
+
+@functools.lru_cache(maxsize=1)
+def _workload(name):
+    return kda_inputs.workload(name)
+
+
+def test_workload_fp32_b1_t256_full(kda):
+    inp = _workload("fp32_b1_t256_h2_k64")
+    out = gpu_bwd(kda, inp)
+    errs = compare_full(inp, out, oracle.run_inputs(inp))
+    print("fp32_b1_t256_h2_k64", errs)
+
+
+def test_workload_bf16_b1_t2048_full(kda):
+    inp = _workload("bf16_b1_t2048_h16_k128")
+    out = gpu_bwd(kda, inp)
+    errs = compare_full(inp, out, oracle.run_inputs(inp))
+    print("bf16_b1_t2048_h16_k128", errs)
+
+
+def test_workload_bf16_b8_t4096_sampled(kda):
+    inp = _workload("bf16_b8_t4096_h32_k128")
+    out = gpu_bwd(kda, inp)
+    for n, h in [(0, 0), (7, 31), (3, 17)]:
+        print("bf16_b8_t4096_h32_k128", n, h, compare_unit(inp, out, n, h))
+
+
+def test_workload_bf16_varlen_sampled(kda):
+    inp = _workload("bf16_varlen16_h32_k128")
+    out = gpu_bwd(kda, inp)
+    lens = [e - b for b, e in inp.seq_bounds]
+    picks = [int(np.argmin(lens)), int(np.argmax(lens)), 5]
+    for n, h in zip(picks, [3, 30, 11]):
+        print("bf16_varlen16_h32_k128", n, lens[n], h, compare_unit(inp, out, n, h))
+
+
+@pytest.mark.slow
+def test_workload_bf16_t65536_gva_sampled(kda):
+    inp = _workload("bf16_b1_t65536_h16_hv32_k128")
+    out = gpu_bwd(kda, inp)
+    print("bf16_b1_t65536_h16_hv32_k128", compare_unit(inp, out, 0, 9))
+
+
+# ------------------------------------------------------------ invariances
+
+def test_rerun_is_bitwise_identical(kda):
+    inp = kda_inputs.small(seed=33, B=1, T=0, H=2, HV=4, K=128, V=128, dtype="bf16", seq_lens=[300, 17, 64])
+    a = gpu_bwd(kda, inp)
+    b = gpu_bwd(kda, inp)
+    for key in GRADS:
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_packed_equals_separate_sequences_bitwise(kda):
+    lens = [100, 1, 64, 257]
+    inp = kda_inputs.small(seed=34, B=1, T=0, H=2, HV=2, K=128, V=128, dtype="bf16", seq_lens=lens)
+    packed = gpu_bwd(kda, inp)
+    for n, (b, e) in enumerate(inp.seq_bounds):
+        sl = lambda t: t[:, b:e].contiguous()
+        one = kda_inputs.Inputs(inp.spec, sl(inp.q), sl(inp.k), sl(inp.v), sl(inp.g), sl(inp.beta),
+                                inp.h0[n:n + 1].contiguous(), sl(inp.do), inp.dht[n:n + 1].contiguous(), None,
+                                inp.scale)
+        single = gpu_bwd(kda, one)
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            assert torch.equal(single[key][0], packed[key][0, b:e]), (n, key)
+        assert torch.equal(single["dh0"][0], packed["dh0"][n]), n
