@@ -311,12 +311,14 @@ def gpu_arm(args):
     clocks.start()
     time.sleep(0.3)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for evs in ev_sets:
+        for e in evs:
+            e.record(stream)  # create the event objects before the timed region
+    handle_sets = [(ctypes.c_void_p * nev)(*[e.cuda_event for e in evs]) for evs in ev_sets]
+    torch.cuda.synchronize(device)
     start.record(stream)
     for i in range(args.steps):
-        handles = (ctypes.c_void_p * nev)(*[e.cuda_event for e in ev_sets[i]])
-        for e in ev_sets[i]:
-            e.record(stream)  # materialise the event objects (re-recorded by the library below)
-        lib.kda_set_profile_events(handles, nev)
+        lib.kda_set_profile_events(handle_sets[i], nev)
         step(x, out)
     lib.kda_set_profile_events(None, 0)
     stop.record(stream)

@@ -32,7 +32,10 @@ STATUS = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "K
 class KdaError(RuntimeError):
     def __init__(self, code, where):
         self.code = code
-        super().__init__(f"{where}: {STATUS.get(code, code)} ({load().kda_status_string(code).decode()})")
+        msg = f"{where}: {STATUS.get(code, code)} ({load().kda_status_string(code).decode()})"
+        if code == 4:
+            msg += f" [{load().kda_last_cuda_error().decode()}]"
+        super().__init__(msg)
 
 
 class Dims(ctypes.Structure):
@@ -67,6 +70,14 @@ def load():
             lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(Dims)] + [_P] * 19 + [ctypes.c_size_t, _P]
             lib.kda_device_status.restype = ctypes.c_int
             lib.kda_device_status.argtypes = [_P, _P]
+            lib.kda_set_profile_events.restype = ctypes.c_int
+            lib.kda_set_profile_events.argtypes = [_P, ctypes.c_int32]
+            lib.kda_last_launch_count.restype = ctypes.c_int32
+            lib.kda_last_launch_count.argtypes = []
+            lib.kda_last_cuda_error.restype = ctypes.c_char_p
+            lib.kda_last_cuda_error.argtypes = []
+            lib.kda_launch_name.restype = ctypes.c_char_p
+            lib.kda_launch_name.argtypes = [ctypes.c_int32]
             _lib = lib
     return _lib
 

@@ -135,6 +135,12 @@ void* const* g_prof_events = nullptr;
 int g_prof_n = 0;
 thread_local const char* t_names[kMaxLaunches];
 thread_local int t_count = 0;
+thread_local const char* t_cuda_err = "no error";
+
+kda_status cuda_fail(cudaError_t e) {
+    t_cuda_err = cudaGetErrorString(e);
+    return KDA_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -161,6 +167,8 @@ extern "C" kda_status kda_set_profile_events(void* const* events, int32_t n_even
 }
 
 extern "C" int32_t kda_last_launch_count(void) { return t_count; }
+
+extern "C" const char* kda_last_cuda_error(void) { return t_cuda_err; }
 
 extern "C" const char* kda_launch_name(int32_t i) {
     return (i >= 0 && i < t_count && i < kMaxLaunches) ? t_names[i] : nullptr;
@@ -222,9 +230,11 @@ extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const v
     memset(&io, 0, sizeof(io));
     io.q = q; io.k = k; io.v = v; io.beta = beta; io.g = g; io.h0 = h0;
     io.o = o; io.ht = ht; io.states_out = states;
-    if (cudaMemsetAsync(w.status, 0, kAlign, st) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(w.status, 0, kAlign, st);
+    if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);
-    if (simt_fwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st) != cudaSuccess) return KDA_ERR_CUDA;
+    e = simt_fwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st);
+    if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
 }
 
@@ -250,16 +260,20 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
     memset(&io, 0, sizeof(io));
     io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht;
     io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0;
-    if (cudaMemsetAsync(w.status, 0, kAlign, st) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t e = cudaMemsetAsync(w.status, 0, kAlign, st);
+    if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);
-    if (simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st) != cudaSuccess) return KDA_ERR_CUDA;
+    e = simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st);
+    if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
 }
 
 extern "C" kda_status kda_device_status(const void* ws, kda_stream_t stream) {
     if (!ws) return KDA_ERR_INVALID_ARG;
-    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
     int word = 0;
-    if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    e = cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e);
     return word == 0 ? KDA_OK : KDA_ERR_DEVICE_TIMEOUT;
 }

@@ -163,6 +163,10 @@ kda_status kda_set_profile_events(void* const* events, int32_t n_events);
 /* Number of kernel launches the last kda_chunk_fwd / kda_chunk_bwd call made
  * on this host thread, and the name of the i-th (static string, NULL if out of range). */
 int32_t kda_last_launch_count(void);
+
+/* Text of the CUDA error behind the last KDA_ERR_CUDA returned on this host
+ * thread (static string; "no error" if none). */
+const char* kda_last_cuda_error(void);
 const char* kda_launch_name(int32_t i);
 
 #ifdef __cplusplus
