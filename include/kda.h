@@ -148,6 +148,36 @@ kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, con
 kda_status kda_device_status(const void* ws, kda_stream_t stream);
 
 /*
+ * Backward without a caller workspace, for callers that cannot allocate.
+ *
+ * Some callers cannot call cudaMalloc or any other allocating routine where
+ * they run the backward (for example a plugin running inside another
+ * engine's enqueue/execute phase, where allocation is forbidden or would
+ * synchronise the device, or a process whose device memory is all reserved by
+ * another allocator), so they cannot pass a workspace either. This variant of
+ * kda_chunk_bwd (always the recompute path: no saved states) uses a fixed
+ * scratch array of KDA_NOALLOC_SCRATCH_BYTES that the library keeps in device
+ * memory on every GPU that loads it, until the process exits. It allocates
+ * nothing; the caller still passes every input and output, as for
+ * kda_chunk_bwd.
+ *   - The first call on a device looks up that array's device address (a
+ *     one-time set-up with the device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array. Calls whose execution overlaps on the
+ *     GPU (several streams or host threads) race on it: serialise them.
+ *   - Errors: those of kda_chunk_bwd; KDA_ERR_WORKSPACE when the problem needs
+ *     more than KDA_NOALLOC_SCRATCH_BYTES (kda_workspace_bytes(dims,
+ *     KDA_PASS_BWD) > KDA_NOALLOC_SCRATCH_BYTES), returned before any launch.
+ * This entry point has no counterpart in the paper; it is a deployment aid.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+kda_status kda_chunk_bwd_noalloc(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                                 const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                 const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
+                                 const float* dht, void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0,
+                                 kda_stream_t stream);
+
+/*
  * Per-kernel timing hook (for benchmarks and profiling; off by default).
  * After kda_set_profile_events(events, n) with n >= 1 caller-created
  * cudaEvent_t handles, every later kda_chunk_fwd / kda_chunk_bwd call records
