@@ -87,8 +87,24 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
         b = s["io_out"] + tk * K * in_bytes * 2 + th * (2 * V * in_bytes + in_bytes)
         f = nck * (6 * C * C * V + 10 * C * C * K + 4 * C ** 3)
         return "alu", b, f
-    if name == "gva_reduce":
+    if name in ("gva_reduce", "tc_gva_reduce"):
         return "hbm", th * K * 4 * 2 + tk * K * in_bytes * 2, 0
+    # Tensor-core path (bf16 K = V = 128): per chunk-head I/O of each kernel at
+    # its dtypes (bf16 tiles CxK = 16 KB, CxC = 8 KB, KxV = 32 KB), read once
+    # and written once; FLOPs of its dense products counted once.
+    tcd, tcc, tdd = C * K * 2, C * C * 2, K * V * 2
+    per_in = C * (2 * K * in_bytes + V * in_bytes + K * 4 + in_bytes)  # q, k, v, g, beta of one chunk-head
+    if name == "tc_intra":
+        b = nck * (per_in + 4 * tcd + 2 * tcc + K * 4)
+        f = nck * (2 * 2 * C * C * K + 2 * 2 * C * C * (K + V) // 2 + C ** 3 // 3)
+        return "hbm", b, f
+    if name == "tc_state_fwd":
+        return "hbm", nck * (3 * tcd + K * 4 + tdd + tcd), nck * 4 * C * K * V
+    if name == "tc_ds_rev":
+        return "hbm", nck * (3 * tcd + tcc + C * V * in_bytes + K * 4 + tdd + tcd), nck * (6 * C * K * V + 2 * C * C * V)
+    if name == "tc_grads":
+        b = nck * (per_in + C * V * in_bytes + 2 * tcd + 2 * tdd + tcc + K * 4) + s["io_out"]
+        return "hbm", b, s["flops"]
     return "hbm", s["bytes"], s["flops"]
 
 

@@ -4,6 +4,7 @@
 #include <string.h>
 
 #include "../../include/kda.h"
+#include "../../include/kda_selftest.h"
 #include "kda_common.cuh"
 #include "kda_internal.h"
 
@@ -41,9 +42,17 @@ kda_status check_dims(const kda_dims* d, Prob* p) {
 
 struct Layout {
     size_t status, gam, w, u, vn, inv, aqk, sin, dso, dvn, dqt, dkh, dw, dgc, dqp, dkp, total;
+    // tensor-core path regions
+    bool tc;
+    size_t t_w, t_u, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc;
 };
 
-Layout layout(const Prob& p, int pass) {
+// The backward of bf16 inputs with K = V = 128 runs on the tensor-core path.
+bool use_tc(const kda_dims* d, int pass) {
+    return pass == KDA_PASS_BWD && d->dtype == KDA_DTYPE_BF16 && d->K == 128 && d->V == 128;
+}
+
+Layout layout(const Prob& p, int pass, bool tc) {
     Layout L;
     memset(&L, 0, sizeof(L));
     const size_t R = (size_t)p.B * p.T, HV = p.HV, K = p.K, V = p.V, NT = (size_t)p.NT, f = sizeof(float);
@@ -54,6 +63,27 @@ Layout layout(const Prob& p, int pass) {
         return at;
     };
     L.status = take(kAlign);
+    L.tc = tc;
+    if (tc) {
+        const size_t CH = NT * HV, TCD = (size_t)kC * 128 * 2, TCC = (size_t)kC * kC * 2, TDD = 128 * 128 * 2;
+        L.t_w = take(CH * TCD);
+        L.t_u = take(CH * TCD);
+        L.t_kh = take(CH * TCD);
+        L.t_qs = take(CH * TCD);
+        L.t_vn = take(CH * TCD);
+        L.t_dvn = take(CH * TCD);
+        L.t_aqk = take(CH * TCC);
+        L.t_inv = take(CH * TCC);
+        L.t_sin = take(CH * TDD);
+        L.t_dso = take(CH * TDD);
+        L.t_egc = take(CH * 128 * f);
+        if (p.HV != p.H) {
+            L.dqp = take(R * HV * K * f);
+            L.dkp = take(R * HV * K * f);
+        }
+        L.total = off;
+        return L;
+    }
     L.gam = take(R * HV * K * f);
     L.w = take(R * HV * K * f);
     L.u = take(R * HV * V * f);
@@ -105,6 +135,30 @@ Ws carve(void* base, const Layout& L) {
     return w;
 }
 
+TcWs carve_tc(void* base, const Layout& L) {
+    char* b = (char*)base;
+    TcWs w;
+    memset(&w, 0, sizeof(w));
+    auto at = [&](size_t off) { return (uint8_t*)(b + off); };
+    w.status = (int*)(b + L.status);
+    w.w = at(L.t_w);
+    w.u = at(L.t_u);
+    w.kh = at(L.t_kh);
+    w.qs = at(L.t_qs);
+    w.vn = at(L.t_vn);
+    w.dvn = at(L.t_dvn);
+    w.aqk = at(L.t_aqk);
+    w.inv = at(L.t_inv);
+    w.sin = at(L.t_sin);
+    w.dso = at(L.t_dso);
+    w.egc = (float*)at(L.t_egc);
+    if (L.dqp) {
+        w.dqp = (float*)at(L.dqp);
+        w.dkp = (float*)at(L.dkp);
+    }
+    return w;
+}
+
 // Shared checks of the forward and backward inputs.
 kda_status check_common(const kda_dims* dims, Prob* p, const void* q, const void* k, const void* v, const float* g,
                         const void* beta, const float* h0, const int64_t* cu, const int32_t* cidx,
@@ -123,7 +177,7 @@ kda_status check_common(const kda_dims* dims, Prob* p, const void* q, const void
     const void* ptrs[] = {q, k, v, g, beta, h0, cu, cidx, coff};
     for (const void* x : ptrs)
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
-    if (!ws || !aligned16(ws) || ws_bytes < layout(*p, pass).total) return KDA_ERR_WORKSPACE;
+    if (!ws || !aligned16(ws) || ws_bytes < layout(*p, pass, use_tc(dims, pass)).total) return KDA_ERR_WORKSPACE;
     p->cu = cu;
     p->cidx = cidx;
     p->coff = coff;
@@ -209,7 +263,7 @@ extern "C" kda_status kda_prepare_chunks(const int64_t* cu, int32_t num_seqs, in
 extern "C" size_t kda_workspace_bytes(const kda_dims* dims, int32_t pass) {
     Prob p;
     if (check_dims(dims, &p) != KDA_OK || (pass != KDA_PASS_FWD && pass != KDA_PASS_BWD)) return 0;
-    return layout(p, pass).total;
+    return layout(p, pass, use_tc(dims, pass)).total;
 }
 
 extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const void* k, const void* v,
@@ -223,7 +277,7 @@ extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const v
     if ((size_t)dims->B * dims->T > 0 && !o) return KDA_ERR_INVALID_ARG;
     for (const void* x : {(const void*)o, (const void*)ht, (const void*)states})
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
-    const Layout L = layout(p, KDA_PASS_FWD);
+    const Layout L = layout(p, KDA_PASS_FWD, false);
     Ws w = carve(ws, L);
     cudaStream_t st = (cudaStream_t)stream;
     IO io;
@@ -253,19 +307,67 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
                           (const void*)dk, (const void*)dv, (const void*)dg, (const void*)dbeta, (const void*)dh0})
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
     if (states) return KDA_ERR_UNSUPPORTED;
-    const Layout L = layout(p, KDA_PASS_BWD);
-    Ws w = carve(ws, L);
+    const Layout L = layout(p, KDA_PASS_BWD, use_tc(dims, KDA_PASS_BWD));
     cudaStream_t st = (cudaStream_t)stream;
     IO io;
     memset(&io, 0, sizeof(io));
     io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht;
     io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0;
-    cudaError_t e = cudaMemsetAsync(w.status, 0, kAlign, st);
+    cudaError_t e = cudaMemsetAsync((char*)ws + L.status, 0, kAlign, st);
     if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);
-    e = simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st);
+    if (L.tc)
+        e = tc_bwd(p, io, carve_tc(ws, L), st, 4);
+    else
+        e = simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, carve(ws, L), st);
     if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
+}
+
+extern "C" kda_status kda_debug_bwd_stages(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                           const float* g, const void* beta, const float* h0,
+                                           const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                                           const int64_t* chunk_off, const void* d_o, const float* dht, float* dh0,
+                                           int32_t stages, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    Prob p;
+    kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, ws, ws_bytes,
+                                KDA_PASS_BWD);
+    if (s != KDA_OK) return s;
+    if (!use_tc(dims, KDA_PASS_BWD)) return KDA_ERR_UNSUPPORTED;
+    if (stages < 1 || stages > 4 || !d_o || (dh0 && !h0)) return KDA_ERR_INVALID_ARG;
+    const Layout L = layout(p, KDA_PASS_BWD, true);
+    cudaStream_t st = (cudaStream_t)stream;
+    IO io;
+    memset(&io, 0, sizeof(io));
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht; io.dh0 = dh0;
+    cudaError_t e = cudaMemsetAsync((char*)ws + L.status, 0, kAlign, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    begin_launches(st);
+    e = tc_bwd(p, io, carve_tc(ws, L), st, stages);
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+extern "C" kda_status kda_debug_ws_region(const kda_dims* dims, int32_t pass, const char* name, size_t* offset,
+                                          size_t* bytes) {
+    Prob p;
+    if (!name || !offset || !bytes || check_dims(dims, &p) != KDA_OK) return KDA_ERR_INVALID_ARG;
+    const Layout L = layout(p, pass, use_tc(dims, pass));
+    const struct {
+        const char* n;
+        size_t off;
+    } tab[] = {{"w", L.t_w}, {"u", L.t_u}, {"kh", L.t_kh}, {"qs", L.t_qs}, {"vn", L.t_vn}, {"dvn", L.t_dvn},
+               {"aqk", L.t_aqk}, {"inv", L.t_inv}, {"sin", L.t_sin}, {"dso", L.t_dso}, {"egc", L.t_egc}};
+    if (!L.tc) return KDA_ERR_UNSUPPORTED;
+    for (size_t i = 0; i < sizeof(tab) / sizeof(tab[0]); ++i)
+        if (strcmp(tab[i].n, name) == 0) {
+            *offset = tab[i].off;
+            size_t end = L.total;
+            for (size_t j = 0; j < sizeof(tab) / sizeof(tab[0]); ++j)
+                if (tab[j].off > tab[i].off && tab[j].off < end) end = tab[j].off;
+            *bytes = end - tab[i].off;
+            return KDA_OK;
+        }
+    return KDA_ERR_INVALID_ARG;
 }
 
 extern "C" kda_status kda_device_status(const void* ws, kda_stream_t stream) {

@@ -38,4 +38,24 @@ void note_launch(const char* name, cudaStream_t st);
 cudaError_t simt_fwd(const Prob& p, bool bf16, const IO& io, const Ws& ws, cudaStream_t st);
 cudaError_t simt_bwd(const Prob& p, bool bf16, const IO& io, const Ws& ws, cudaStream_t st);
 
+// Workspace of the tensor-core path (bf16, K = V = 128). Per chunk-head
+// ch = chunk * HV + hv, bf16 tiles in the operand layout of tc_util.cuh:
+//   w, u, kh (K^), qs (scale Q~), vn (delta), dvn (d_delta): 64 x 128 (16 KB)
+//   aqk, inv: 64 x 64 (8 KB);  sin, dso: 128 x 128 (32 KB)
+//   egc: 128 fp32 (e^Gamma_C per key channel)
+// dqp, dkp: fp32 [R, HV, K] per-value-head dq/dk before the group sum.
+struct TcWs {
+    uint8_t *w, *u, *kh, *qs, *vn, *dvn, *aqk, *inv, *sin, *dso;
+    float *egc, *dqp, *dkp;
+    int* status;
+};
+
+// The tensor-core path handles bf16 inputs with K = V = 128.
+bool tc_path_ok(const Prob& p, bool bf16);
+// Runs the first `stages` stages of the tensor-core backward (1: intra,
+// 2: + state pass, 3: + reverse pass, 4: + gradients).
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages);
+// The per-chunk gradient stage (and the grouped-value-head reduction).
+cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
+
 }  // namespace kda

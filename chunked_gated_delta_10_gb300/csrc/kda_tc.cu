@@ -1,0 +1,583 @@
+// Tensor-core (tcgen05) kernels of the chunked KDA backward for bf16 inputs
+// with K = V = 128 and chunks of 64 tokens.
+//
+// Stages (the same steps as the fp32 kernels in kda_simt.cu, regrouped so
+// that every dense product is a tcgen05.mma with bf16 operands and an fp32
+// accumulator in TMEM):
+//
+//   tc_intra      per (chunk, value head): gate cumsum in log2 units, the
+//                 decayed factors Kr = k e^(G-Gref), Qr = q e^(G-Gref),
+//                 Kc = k e^(Gref-G) (Gref = middle row of the chunk), one
+//                 MMA [Kr; Qr] Kc^T giving Akk and Aqk together, the inverse
+//                 INV = (I + Akk)^-1 by blocked forward substitution in fp32,
+//                 then w^T = (beta K~)^T INV^T and u^T = (beta V)^T INV^T.
+//                 Writes w, u, K^, scale*Q~, Aqk, INV and e^(Gamma_C).
+//   tc_state_fwd  per (sequence, value head, 64-column half of V): the chunk
+//                 loop delta^T = u^T - S^T w^T, S <- e^(Gamma_C) S + K^^T delta
+//                 with S in registers (fp32) and a bf16 copy in shared memory;
+//                 writes S_in and delta of every chunk.
+//   tc_ds_rev     per (sequence, value head, V half), chunks in reverse:
+//                 dDelta^T = dO^T Aqk + dS^T K^^T,
+//                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
+//                 dDelta and dh0.
+//
+// Intermediates live in the workspace as bf16 tiles in exactly the
+// shared-memory operand layout of tc_util.cuh (row-major, 64-column blocks,
+// 128-byte swizzle), so each consumer fetches a tile with one bulk copy.
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "tc_util.cuh"
+#include "tma_host.h"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+using bf16 = __nv_bfloat16;
+
+constexpr int D = 128;                 // K = V on this path
+constexpr int TCD = kC * D * 2;        // bytes of a 64 x 128 bf16 tile
+constexpr int TCC = kC * kC * 2;       // 64 x 64
+constexpr int TDD = D * D * 2;         // 128 x 128
+constexpr int HALF = 64;               // V columns per state-pass CTA
+
+// ---------------------------------------------------------------------------
+// (I + L)^-1 for a strictly lower triangular 64 x 64 L (fp32, shared), by
+// blocked forward substitution: 16 x 16 diagonal blocks first, then the
+// 2 x 2 block formula [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]] at
+// 32 and 64. Out and scratch X (1024 floats) are shared; 128 threads.
+// ---------------------------------------------------------------------------
+__device__ void tri_inverse64(const float* L, float* Out, float* X) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < kC * kC; i += blockDim.x) Out[i] = 0.f;
+    __syncthreads();
+    if (lane < 16) {
+        const int b = warp * 16, j = lane;
+        float x[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < rr; ++m) s = fmaf(L[(b + rr) * kC + b + m], x[m], s);
+            x[rr] = rr == j ? 1.f : (rr > j ? -s : 0.f);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) Out[(b + rr) * kC + b + j] = x[rr];
+    }
+    __syncthreads();
+    // 16 -> 32: blocks (1,0) and (3,2)
+    {
+        const int pr = tid >> 6, base = 32 * pr;
+        for (int u = 0; u < 4; ++u) {
+            const int e = (tid & 63) * 4 + u, a = e >> 4, c = e & 15;
+            float s = 0.f;
+            for (int m = c; m < 16; ++m) s = fmaf(L[(base + 16 + a) * kC + base + m], Out[(base + m) * kC + base + c], s);
+            X[pr * 256 + a * 16 + c] = s;
+        }
+        __syncthreads();
+        for (int u = 0; u < 4; ++u) {
+            const int e = (tid & 63) * 4 + u, a = e >> 4, c = e & 15;
+            float s = 0.f;
+            for (int m = 0; m <= a; ++m)
+                s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
+            Out[(base + 16 + a) * kC + base + c] = -s;
+        }
+        __syncthreads();
+    }
+    // 32 -> 64: block rows 32..63, columns 0..31
+    for (int u = 0; u < 8; ++u) {
+        const int e = tid * 8 + u, a = e >> 5, c = e & 31;
+        float s = 0.f;
+        for (int m = c; m < 32; ++m) s = fmaf(L[(32 + a) * kC + m], Out[m * kC + c], s);
+        X[a * 32 + c] = s;
+    }
+    __syncthreads();
+    for (int u = 0; u < 8; ++u) {
+        const int e = tid * 8 + u, a = e >> 5, c = e & 31;
+        float s = 0.f;
+        for (int m = 0; m <= a; ++m) s = fmaf(Out[(32 + a) * kC + 32 + m], X[m * 32 + c], s);
+        Out[(32 + a) * kC + c] = -s;
+    }
+    __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// tc_intra
+// ---------------------------------------------------------------------------
+constexpr int kIntraSmem = 1024 + 32768 + 3 * TCD + TCC + 4096 + 256 + 64;
+
+__global__ void __launch_bounds__(128, 2) k_tc_intra(Prob p, const bf16* __restrict__ q, const bf16* __restrict__ k,
+                                                      const bf16* __restrict__ v, const float* __restrict__ g,
+                                                      const bf16* __restrict__ beta, TcWs ws) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    uint8_t* tKQ = sm;               // [Kr; Qr] 128 x 128; after the first MMA: Akk, INV fp32
+    uint8_t* tKc = sm + 32768;       // 64 x 128
+    uint8_t* tXk = tKc + TCD;        // beta K~, 64 x 128
+    uint8_t* tXv = tXk + TCD;        // beta V, 64 x 128
+    uint8_t* tINV = tXv + TCD;       // 64 x 64
+    float* X = reinterpret_cast<float*>(tINV + TCC);
+    float* sb = X + 1024;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sb + 64);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+    float* Akk = reinterpret_cast<float*>(tKQ);
+    float* Fi = Akk + kC * kC;
+
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int HV = p.HV, H = p.H, hv = blockIdx.y, h = hv / (HV / H);
+    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
+    int64_t r0;
+    int c;
+    chunk_rows(p, gc, r0, c);
+
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    if (tid < kC) sb[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
+
+    // Gamma2 (log2 units) of channel d = tid for all 64 rows.
+    const int d = tid;
+    float G2[kC];
+    {
+        float acc = 0.f;
+#pragma unroll
+        for (int r = 0; r < kC; ++r) {
+            const float gv = r < c ? g[((r0 + r) * HV + hv) * D + d] : 0.f;
+            acc += gv;
+            G2[r] = acc * kLog2e;
+        }
+    }
+    const int rmid = (c - 1) >> 1;
+    float ref = 0.f, gC = 0.f;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+        if (r == rmid) ref = G2[r];
+        if (r == c - 1) gC = G2[r];
+    }
+    ws.egc[ch * D + d] = exp2f(gC);
+    __syncthreads();
+    uint8_t* gKh = ws.kh + ch * TCD;
+    uint8_t* gQs = ws.qs + ch * TCD;
+#pragma unroll
+    for (int r = 0; r < kC; ++r) {
+        float kv = 0.f, qv = 0.f, vv = 0.f;
+        if (r < c) {
+            kv = __bfloat162float(k[((r0 + r) * H + h) * D + d]);
+            qv = __bfloat162float(q[((r0 + r) * H + h) * D + d]);
+            vv = __bfloat162float(v[((r0 + r) * HV + hv) * D + d]);
+        }
+        const float b = sb[r], gm = G2[r];
+        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm), eh = exp2f(gC - gm);
+        st_tile(tKQ, r, d, 128, kv * ep);
+        st_tile(tKQ, kC + r, d, 128, qv * ep);
+        st_tile(tKc, r, d, kC, kv * em);
+        st_tile(tXk, r, d, kC, b * kv * E);
+        st_tile(tXv, r, d, kC, b * vv);
+        st_tile(gKh, r, d, kC, kv * eh);
+        st_tile(gQs, r, d, kC, p.scale * qv * E);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (tid == 0) {
+        const uint32_t id = idesc_bf16(128, 64, false, false);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem, desc_kmajor(smem_u32(tKQ), 128, ks), desc_kmajor(smem_u32(tKc), kC, ks), id, ks > 0);
+        mma_commit(bar);
+    }
+    if (wait_all(bar, 0, ws.status, 11, fail)) {
+        tc_fence_after();
+        float row[kC];
+        tmem_ld32(tmem + lane_base, row);
+        tmem_ld32(tmem + lane_base + 32, row + 32);
+        tmem_ld_wait();
+        if (tid < kC) {  // Akk row r = tid (strictly lower, beta_r scaled)
+            const int r = tid;
+            for (int j = 0; j < kC; ++j) Akk[r * kC + j] = j < r ? sb[r] * row[j] : 0.f;
+        } else {  // Aqk row r = tid - 64 (lower incl. diagonal, scaled)
+            const int r = tid - kC;
+            uint8_t* gA = ws.aqk + ch * TCC;
+            for (int c0 = 0; c0 < kC; c0 += 8) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = (c0 + u <= r) ? p.scale * row[c0 + u] : 0.f;
+                uint4 vv;
+                vv.x = pack2(x[0], x[1]);
+                vv.y = pack2(x[2], x[3]);
+                vv.z = pack2(x[4], x[5]);
+                vv.w = pack2(x[6], x[7]);
+                *reinterpret_cast<uint4*>(gA + tile_off(r, c0, kC)) = vv;
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (*(volatile int*)fail == 0) {
+        tri_inverse64(Akk, Fi, X);
+        uint8_t* gI = ws.inv + ch * TCC;
+        if (tid < kC) {
+            const int r = tid;
+            for (int c0 = 0; c0 < kC; c0 += 8) {
+                st_tile_row8(tINV, r, c0, kC, Fi + r * kC + c0);
+                *reinterpret_cast<uint4*>(gI + tile_off(r, c0, kC)) =
+                    *reinterpret_cast<const uint4*>(tINV + tile_off(r, c0, kC));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            const uint32_t id = idesc_bf16(128, 64, true, false);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(tXk), kC, ks), desc_kmajor(smem_u32(tINV), kC, ks), id,
+                         ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(tXv), kC, ks), desc_kmajor(smem_u32(tINV), kC, ks), id,
+                         ks > 0);
+            mma_commit(bar);
+        }
+        if (wait_all(bar, 1, ws.status, 12, fail)) {
+            tc_fence_after();
+            uint8_t* gW = ws.w + ch * TCD;
+            uint8_t* gU = ws.u + ch * TCD;
+            float col[32];
+            for (int half = 0; half < 2; ++half) {
+                tmem_ld32(tmem + lane_base + 64 + 32 * half, col);
+                tmem_ld_wait();
+                for (int j = 0; j < 32; ++j) st_tile(gW, 32 * half + j, d, kC, col[j]);
+                tmem_ld32(tmem + lane_base + 128 + 32 * half, col);
+                tmem_ld_wait();
+                for (int j = 0; j < 32; ++j) st_tile(gU, 32 * half + j, d, kC, col[j]);
+            }
+            tc_fence_before();
+        }
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// tc_state_fwd: one CTA per (sequence, value head, V half); 128 threads,
+// thread t owns state row t (64 fp32 columns). Double-buffered chunk inputs.
+// ---------------------------------------------------------------------------
+struct FwdBuf {
+    static constexpr int W = 0, KH = TCD, U = 2 * TCD, EGC = 2 * TCD + TCD / 2, BYTES = 2 * TCD + TCD / 2 + 1024;
+};
+constexpr int kFwdSmem = 1024 + 2 * FwdBuf::BYTES + D * HALF * 2 + kC * HALF * 2 + 64;
+
+__global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
+                                                          TcWs ws) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    uint8_t* buf0 = sm;
+    uint8_t* tS = sm + 2 * FwdBuf::BYTES;   // bf16 S, 128 rows x 64 cols
+    uint8_t* tDl = tS + D * HALF * 2;       // bf16 delta, 64 rows x 64 cols
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tDl + kC * HALF * 2);  // full[2], mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HV = p.HV, n = blockIdx.x, hv = blockIdx.y, z = blockIdx.z, v0 = z * HALF;
+    int64_t bos, eos, c0;
+    seq_range(p, n, bos, eos, c0);
+    const int nts = (int)((eos - bos + kC - 1) / kC);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 128);
+    float S[HALF];
+    {
+        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + tid) * D + v0 : nullptr;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) S[j] = src ? src[j] : 0.f;
+    }
+    auto issue = [&](int it) {
+        const int64_t ch = (c0 + it) * HV + hv;
+        uint8_t* b = buf0 + (it & 1) * FwdBuf::BYTES;
+        uint64_t* full = &bars[it & 1];
+        mbar_expect_tx(full, 2 * TCD + TCD / 2 + 512);
+        bulk_load(b + FwdBuf::W, ws.w + ch * TCD, TCD, full);
+        bulk_load(b + FwdBuf::KH, ws.kh + ch * TCD, TCD, full);
+        bulk_load(b + FwdBuf::U, ws.u + ch * TCD + z * (TCD / 2), TCD / 2, full);
+        bulk_load(b + FwdBuf::EGC, ws.egc + ch * D, 512, full);
+    };
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (tid == 0) {
+        if (nts > 0) issue(0);
+        if (nts > 1) issue(1);
+    }
+    uint32_t mph = 0;
+    for (int it = 0; it < nts; ++it) {
+        const int64_t ch = (c0 + it) * HV + hv;
+        uint8_t* b = buf0 + (it & 1) * FwdBuf::BYTES;
+        if (!wait_all(&bars[it & 1], (it >> 1) & 1, ws.status, 21, fail)) break;
+        // bf16 copy of S (row tid) for the MMAs, and the S_in checkpoint
+#pragma unroll
+        for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tS, tid, c8, D, S + c8);
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 64, true, false);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem, desc_mnmajor(smem_u32(tS), D, ks), desc_kmajor(smem_u32(b + FwdBuf::W), kC, ks), id,
+                         ks > 0);
+            mma_commit(&bars[2]);
+            bulk_store(ws.sin + ch * TDD + z * (TDD / 2), tS, TDD / 2);
+            bulk_commit();
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 22, fail)) break;
+        mph ^= 1;
+        tc_fence_after();
+        {  // delta^T rows: M = 64 layout, row v = 16 * warp + lane for lane < 16
+            float acc[kC];
+            tmem_ld32(tmem + lane_base, acc);
+            tmem_ld32(tmem + lane_base + 32, acc + 32);
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int vv = 16 * warp + lane;
+                const uint8_t* tU = b + FwdBuf::U;
+#pragma unroll
+                for (int r = 0; r < kC; ++r) st_tile(tDl, r, vv, kC, ld_tile(tU, r, vv, kC) - acc[r]);
+            }
+        }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 64, true, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + FwdBuf::KH), kC, ks), desc_mnmajor(smem_u32(tDl), kC, ks),
+                         id, ks > 0);
+            mma_commit(&bars[2]);
+            bulk_store(ws.vn + ch * TCD + z * (TCD / 2), tDl, TCD / 2);
+            bulk_commit();
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 23, fail)) break;
+        mph ^= 1;
+        tc_fence_after();
+        {
+            const float e = reinterpret_cast<const float*>(b + FwdBuf::EGC)[tid];
+            float acc[HALF];
+            tmem_ld32(tmem + lane_base + 64, acc);
+            tmem_ld32(tmem + lane_base + 96, acc + 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < HALF; ++j) S[j] = fmaf(e, S[j], acc[j]);
+        }
+        tc_fence_before();
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        if (tid == 0 && it + 2 < nts) issue(it + 2);
+    }
+    if (ht && *(volatile int*)fail == 0) {
+        float* dst = ht + (((int64_t)n * HV + hv) * D + tid) * D + v0;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) dst[j] = S[j];
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------
+// tc_ds_rev: one CTA per (sequence, value head, V half), chunks in reverse;
+// thread t owns dS row t (64 fp32 columns). Single-buffered chunk inputs.
+// ---------------------------------------------------------------------------
+struct RevBuf {
+    static constexpr int KH = 0, W = TCD, QS = 2 * TCD, AQK = 3 * TCD, DO = 3 * TCD + TCC, EGC = 3 * TCD + TCC + 8192,
+                         BYTES = 3 * TCD + TCC + 8192 + 1024;
+};
+constexpr int kRevSmem = 1024 + RevBuf::BYTES + D * HALF * 2 + kC * HALF * 2 + 64;
+
+__global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
+                                                       TcWs ws, const __grid_constant__ CUtensorMap tm_do) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    uint8_t* b = sm;
+    uint8_t* tS = sm + RevBuf::BYTES;        // bf16 dS, 128 x 64
+    uint8_t* tDd = tS + D * HALF * 2;        // bf16 dDelta, 64 x 64
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tDd + kC * HALF * 2);  // full, mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HV = p.HV, n = blockIdx.x, hv = blockIdx.y, z = blockIdx.z, v0 = z * HALF;
+    int64_t bos, eos, c0;
+    seq_range(p, n, bos, eos, c0);
+    const int nts = (int)((eos - bos + kC - 1) / kC);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 128);
+    float S[HALF];
+    {
+        const float* src = dht ? dht + (((int64_t)n * HV + hv) * D + tid) * D + v0 : nullptr;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) S[j] = src ? src[j] : 0.f;
+    }
+    auto issue = [&](int it) {
+        const int64_t ch = (c0 + it) * HV + hv;
+        mbar_expect_tx(&bars[0], 3 * TCD + TCC + 8192 + 512);
+        bulk_load(b + RevBuf::KH, ws.kh + ch * TCD, TCD, &bars[0]);
+        bulk_load(b + RevBuf::W, ws.w + ch * TCD, TCD, &bars[0]);
+        bulk_load(b + RevBuf::QS, ws.qs + ch * TCD, TCD, &bars[0]);
+        bulk_load(b + RevBuf::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
+        bulk_load(b + RevBuf::EGC, ws.egc + ch * D, 512, &bars[0]);
+        tma_load_3d(b + RevBuf::DO, &tm_do, v0, hv, (int)(bos + (int64_t)it * kC), &bars[0]);
+    };
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (tid == 0 && nts > 0) issue(nts - 1);
+    uint32_t fph = 0, mph = 0;
+    for (int it = nts - 1; it >= 0; --it) {
+        const int64_t ch = (c0 + it) * HV + hv;
+        if (!wait_all(&bars[0], fph, ws.status, 31, fail)) break;
+        fph ^= 1;
+#pragma unroll
+        for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tS, tid, c8, D, S + c8);
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // dDelta^T = dO^T Aqk + dS^T K^^T (M = 64)
+            const uint32_t ida = idesc_bf16(64, 64, true, true), idb = idesc_bf16(64, 64, true, false);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem, desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks),
+                         desc_mnmajor(smem_u32(b + RevBuf::AQK), kC, ks), ida, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem, desc_mnmajor(smem_u32(tS), D, ks), desc_kmajor(smem_u32(b + RevBuf::KH), kC, ks), idb,
+                         1);
+            // dS_acc = Q~s^T dO (M = 128)
+            const uint32_t idc = idesc_bf16(128, 64, true, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + RevBuf::QS), kC, ks),
+                         desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks), idc, ks > 0);
+            mma_commit(&bars[1]);
+            bulk_store(ws.dso + ch * TDD + z * (TDD / 2), tS, TDD / 2);
+            bulk_commit();
+        }
+        if (!wait_all(&bars[1], mph, ws.status, 32, fail)) break;
+        mph ^= 1;
+        tc_fence_after();
+        {
+            float acc[kC];
+            tmem_ld32(tmem + lane_base, acc);
+            tmem_ld32(tmem + lane_base + 32, acc + 32);
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int vv = 16 * warp + lane;
+#pragma unroll
+                for (int r = 0; r < kC; ++r) st_tile(tDd, r, vv, kC, acc[r]);
+            }
+        }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            const uint32_t id = idesc_neg_a(idesc_bf16(128, 64, true, true));
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + RevBuf::W), kC, ks), desc_mnmajor(smem_u32(tDd), kC, ks),
+                         id, 1);
+            mma_commit(&bars[1]);
+            bulk_store(ws.dvn + ch * TCD + z * (TCD / 2), tDd, TCD / 2);
+            bulk_commit();
+        }
+        if (!wait_all(&bars[1], mph, ws.status, 33, fail)) break;
+        mph ^= 1;
+        tc_fence_after();
+        {
+            const float e = reinterpret_cast<const float*>(b + RevBuf::EGC)[tid];
+            float acc[HALF];
+            tmem_ld32(tmem + lane_base + 64, acc);
+            tmem_ld32(tmem + lane_base + 96, acc + 32);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < HALF; ++j) S[j] = fmaf(e, S[j], acc[j]);
+        }
+        tc_fence_before();
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
+        if (tid == 0 && it > 0) issue(it - 1);
+    }
+    if (dh0 && *(volatile int*)fail == 0) {
+        float* dst = dh0 + (((int64_t)n * HV + hv) * D + tid) * D + v0;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) dst[j] = S[j];
+    }
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+template <typename F>
+cudaError_t set_smem(F* f, int bytes) {
+    return cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+}  // namespace
+
+bool tc_path_ok(const Prob& p, bool bf16) { return bf16 && p.K == D && p.V == D; }
+
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages) {
+    cudaError_t e;
+    if ((e = set_smem(k_tc_intra, kIntraSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_ds_rev, kRevSmem)) != cudaSuccess) return e;
+    const int64_t rows = (int64_t)p.B * p.T;
+    CUtensorMap tm_do;
+    memset(&tm_do, 0, sizeof(tm_do));
+    if (rows > 0 && !make_tmap_bf16_3d(&tm_do, io.d_o, D, (uint64_t)p.HV, (uint64_t)rows, (uint64_t)D * 2,
+                                       (uint64_t)p.HV * D * 2, 64, 1, kC))
+        return cudaErrorInvalidValue;
+    const bf16 *q = (const bf16*)io.q, *k = (const bf16*)io.k, *v = (const bf16*)io.v, *beta = (const bf16*)io.beta;
+    if (p.NT > 0 && stages >= 1) {
+        k_tc_intra<<<dim3((unsigned)p.NT, p.HV), 128, kIntraSmem, st>>>(p, q, k, v, io.g, beta, ws);
+        note_launch("tc_intra", st);
+    }
+    if (stages >= 2) {
+        k_tc_state_fwd<<<dim3(p.N, p.HV, 2), 128, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
+        note_launch("tc_state_fwd", st);
+    }
+    if (stages >= 3) {
+        k_tc_ds_rev<<<dim3(p.N, p.HV, 2), 128, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
+        note_launch("tc_ds_rev", st);
+    }
+    if (stages >= 4) {
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return tc_grads(p, io, ws, st);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

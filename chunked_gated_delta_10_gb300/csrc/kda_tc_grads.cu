@@ -1,0 +1,440 @@
+// Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
+// K = V = 128, chunks of 64), and the grouped-value-head reduction.
+//
+// One CTA per (chunk, value head), 128 threads. Inputs: q, k, v, dO (TMA),
+// and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
+// (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
+// Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
+// Gamma, Gref = middle row), the kernel evaluates, in five dependent MMA
+// phases (fp32 accumulators in TMEM, columns noted):
+//
+//  A  dQ~^T = S_in dO^T [0,64)     dK^^T = dS_out delta^T [64,128)
+//     dw = -d_delta S_in^T [128,256) (M=64)   dAqk = dO delta^T [256,320)
+//  B  PR^T = V d_delta^T + K~ dw^T [128,192)  Mkk = Kr Kc^T [192,256)
+//     dQr^T = Kc^T dN^T [256,320)   dXv = INV^T d_delta [320,448)
+//     dXk^T = dw^T INV [448,512)
+//  C  T = dINV INV^T [128,192)     with dINV = (P + R) diag(beta)
+//  D  dAkk = -INV^T T [320,384)
+//  E  dKr^T = Kc^T dM^T [128,192)  dKc^T = Qr^T dN + Kr^T dM [192,256)
+//
+// where dN = scale tril0(dAqk) and dM = diag(beta) tril-1(dAkk). The
+// epilogues give dv = beta dXv and dbeta = sum_j INV[j,r] PR[j,r] +
+// sum_j dAkk[r,j] Mkk[r,j] per chunk row (row-per-thread layout), and per key
+// channel (channel-per-thread layout) dq, dk and dGamma, whose reverse
+// in-chunk cumsum is dg (the Gamma_C terms e^Gamma_C <S_in, dS_out> and
+// sum_r dK^ K^ land on the last valid row first). These are the formulas of
+// FLA's chunk_bwd.py page (kernel wy_dqkg_fused: dq, dk, dw, dA = -A^T dA A^T,
+// dg = q dq - k dk + [last] dgk + kg dkgb beta; the triangle backward of
+// chunk_kda_bwd_intra) and the FlashKDA K2 page (dvcorr = INV^T dU, dL).
+#include <string.h>
+
+#include "kda_common.cuh"
+#include "kda_internal.h"
+#include "tc_util.cuh"
+#include "tma_host.h"
+
+namespace kda {
+namespace {
+
+using namespace tc;
+using bf16 = __nv_bfloat16;
+
+constexpr int D = 128;
+constexpr int TCD = kC * D * 2, TCC = kC * kC * 2, TDD = D * D * 2;
+
+// Shared-memory map (offsets from a 1024-aligned base).
+struct GS {
+    static constexpr int Q = 0, K = TCD, V = 2 * TCD, DO = 3 * TCD, DL = 4 * TCD, DDL = 5 * TCD;
+    static constexpr int SIN = 6 * TCD, DSO = SIN + TDD;
+    // after phase A the S_in / dS_out area holds the decayed factor tiles
+    static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
+    static constexpr int DW = DSO + TDD;
+    static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, DINV = DM + TCC, TT = DINV + TCC;
+    static constexpr int EGC = TT + TCC, BETA = EGC + 512, DB = BETA + 256, BARS = DB + 256, END = BARS + 64;
+};
+constexpr int kGradsSmem = 1024 + GS::END;
+
+__device__ __forceinline__ float bfr(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+struct GradMaps {
+    CUtensorMap q, k, v, d_o;
+};
+
+__global__ void __launch_bounds__(128, 1)
+    k_tc_grads(Prob p, const float* __restrict__ g, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
+               bf16* __restrict__ dk_out, bf16* __restrict__ dv_out, float* __restrict__ dg_out,
+               bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    float* sbeta = reinterpret_cast<float*>(sm + GS::BETA);
+    float* sdb = reinterpret_cast<float*>(sm + GS::DB);
+    const float* segc = reinterpret_cast<const float*>(sm + GS::EGC);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);  // [0] loads, [1] mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+    auto S = [&](int off) { return smem_u32(sm + off); };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HV = p.HV, H = p.H, G = HV / H, hv = blockIdx.y, h = hv / G;
+    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
+    int64_t r0;
+    int c;
+    chunk_rows(p, gc, r0, c);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    if (tid < kC) {
+        sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
+        sdb[tid] = 0.f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lb = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+    if (tid == 0) {
+        mbar_expect_tx(&bars[0], 6 * TCD + 2 * TDD + TCC + 512);
+        const int row = (int)r0;
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + GS::Q + b * (TCD / 2), &maps.q, 64 * b, h, row, &bars[0]);
+            tma_load_3d(sm + GS::K + b * (TCD / 2), &maps.k, 64 * b, h, row, &bars[0]);
+            tma_load_3d(sm + GS::V + b * (TCD / 2), &maps.v, 64 * b, hv, row, &bars[0]);
+            tma_load_3d(sm + GS::DO + b * (TCD / 2), &maps.d_o, 64 * b, hv, row, &bars[0]);
+        }
+        bulk_load(sm + GS::DL, ws.vn + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + GS::DDL, ws.dvn + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + GS::SIN, ws.sin + ch * TDD, TDD, &bars[0]);
+        bulk_load(sm + GS::DSO, ws.dso + ch * TDD, TDD, &bars[0]);
+        bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
+        bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
+    }
+
+    // Gamma2 (log2 units) of channel d = tid; reference and last valid rows.
+    const int d = tid;
+    const int rmid = (c - 1) >> 1;
+    float ref = 0.f, gC = 0.f;
+    {
+        float acc = 0.f;
+#pragma unroll 8
+        for (int r = 0; r < kC; ++r) {
+            if (r < c) acc += g[((r0 + r) * HV + hv) * D + d];
+            const float gm = acc * kLog2e;
+            if (r == rmid) ref = gm;
+            if (r == c - 1) gC = gm;
+        }
+    }
+
+    float rowdot = 0.f;
+    if (!wait_all(&bars[0], 0, ws.status, 41, fail)) goto cleanup;
+    if (tid == 0) {  // phase A
+        tc_fence_after();
+        const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
+                       i64 = idesc_bf16(64, 64, false, false);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks), idesc_neg_a(i64n),
+                     ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
+        mma_commit(&bars[1]);
+    }
+    for (int c8 = 0; c8 < D; c8 += 8) {  // <S_in[d,:], dS_out[d,:]>
+        const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
+        const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
+            rowdot = fmaf(fa.x, fb.x, rowdot);
+            rowdot = fmaf(fa.y, fb.y, rowdot);
+        }
+    }
+    if (!wait_all(&bars[1], 0, ws.status, 42, fail)) goto cleanup;
+    tc_fence_after();
+    {  // epilogue A: dw rows and dN rows (row r = 16 warp + lane for lane < 16)
+        const int r = 16 * warp + lane;
+        const bool rv = lane < 16;
+        float x[32];
+        for (int cb = 0; cb < 4; ++cb) {
+            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
+            tmem_ld_wait();
+            if (rv)
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, r, 32 * cb + 8 * u, kC, x + 8 * u);
+        }
+        for (int cb = 0; cb < 2; ++cb) {
+            tmem_ld32(tmem + lb + 256 + 32 * cb, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = (32 * cb + u <= r && r < c) ? p.scale * x[u] : 0.f;
+            if (rv)
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DN, r, 32 * cb + 8 * u, kC, x + 8 * u);
+        }
+    }
+    tc_fence_before();
+    {  // decayed factor tiles of channel d (rows >= c are zero)
+        float acc = 0.f;
+#pragma unroll 4
+        for (int r = 0; r < kC; ++r) {
+            float kv = 0.f, qv = 0.f;
+            if (r < c) {
+                acc += g[((r0 + r) * HV + hv) * D + d];
+                kv = ld_tile(sm + GS::K, r, d, kC);
+                qv = ld_tile(sm + GS::Q, r, d, kC);
+            }
+            const float gm = acc * kLog2e;
+            const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm);
+            st_tile(sm + GS::KR, r, d, kC, kv * ep);
+            st_tile(sm + GS::KC, r, d, kC, kv * em);
+            st_tile(sm + GS::QR, r, d, kC, qv * ep);
+            st_tile(sm + GS::KT, r, d, kC, kv * E);
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // phase B
+        tc_fence_after();
+        const uint32_t i64 = idesc_bf16(64, 64, false, false);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks), i64, ks > 0);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 128, desc_kmajor(S(GS::KT), kC, ks), desc_kmajor(S(GS::DW), kC, ks), i64, 1);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), kC, ks), desc_kmajor(S(GS::KC), kC, ks), i64, ks > 0);
+        const uint32_t imk = idesc_bf16(128, 64, true, false);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 256, desc_mnmajor(S(GS::KC), kC, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
+        const uint32_t ixv = idesc_bf16(64, 128, true, true);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv, ks > 0);
+        const uint32_t ixk = idesc_bf16(128, 64, true, true);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk, ks > 0);
+        mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 1, ws.status, 43, fail)) goto cleanup;
+    tc_fence_after();
+    {  // epilogue B: dbeta (INV part), dINV columns, dv rows
+        const int r = 16 * warp + lane;
+        const bool rv = lane < 16;
+        float x[32];
+        float db = 0.f;
+        const float br = rv ? sbeta[r] : 0.f;
+        for (int cb = 0; cb < 2; ++cb) {
+            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
+            tmem_ld_wait();
+            if (rv)
+                for (int u = 0; u < 32; ++u) {
+                    const int j = 32 * cb + u;
+                    db = fmaf(ld_tile(sm + GS::INV, j, r, kC), x[u], db);
+                    st_tile(sm + GS::DINV, j, r, kC, br * x[u]);
+                }
+        }
+        if (rv) sdb[r] = db;
+        bf16* dvrow = dv_out + ((r0 + r) * HV + hv) * D;
+        for (int cb = 0; cb < 4; ++cb) {
+            tmem_ld32(tmem + lb + 320 + 32 * cb, x);
+            tmem_ld_wait();
+            if (rv && r < c)
+                for (int u = 0; u < 32; u += 8) {
+                    uint4 vv;
+                    vv.x = pack2(br * x[u], br * x[u + 1]);
+                    vv.y = pack2(br * x[u + 2], br * x[u + 3]);
+                    vv.z = pack2(br * x[u + 4], br * x[u + 5]);
+                    vv.w = pack2(br * x[u + 6], br * x[u + 7]);
+                    *reinterpret_cast<uint4*>(dvrow + 32 * cb + u) = vv;
+                }
+        }
+    }
+    tc_fence_before();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // phase C: T = dINV INV^T
+        tc_fence_after();
+        const uint32_t i64 = idesc_bf16(64, 64, false, false);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 128, desc_kmajor(S(GS::DINV), kC, ks), desc_kmajor(S(GS::INV), kC, ks), i64, ks > 0);
+        mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 0, ws.status, 44, fail)) goto cleanup;
+    tc_fence_after();
+    {
+        const int r = 16 * warp + lane;
+        float x[32];
+        for (int cb = 0; cb < 2; ++cb) {
+            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
+            tmem_ld_wait();
+            if (lane < 16)
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::TT, r, 32 * cb + 8 * u, kC, x + 8 * u);
+        }
+    }
+    tc_fence_before();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // phase D: dAkk = -INV^T T
+        tc_fence_after();
+        const uint32_t id = idesc_neg_a(idesc_bf16(64, 64, true, true));
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), id, ks > 0);
+        mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 1, ws.status, 45, fail)) goto cleanup;
+    tc_fence_after();
+    {  // epilogue D: dbeta (Akk part), dM rows
+        const int r = 16 * warp + lane;
+        const bool rv = lane < 16;
+        const float br = rv ? sbeta[r] : 0.f;
+        float db = rv ? sdb[r] : 0.f;
+        float a[32], m[32];
+        for (int cb = 0; cb < 2; ++cb) {
+            tmem_ld32(tmem + lb + 320 + 32 * cb, a);
+            tmem_ld32(tmem + lb + 192 + 32 * cb, m);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int j = 32 * cb + u;
+                const bool in = j < r && r < c;
+                db = in ? fmaf(a[u], m[u], db) : db;
+                a[u] = in ? br * a[u] : 0.f;
+            }
+            if (rv)
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DM, r, 32 * cb + 8 * u, kC, a + 8 * u);
+        }
+        if (rv && r < c) db_out[(r0 + r) * HV + hv] = __float2bfloat16_rn(db);
+    }
+    tc_fence_before();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {  // phase E
+        tc_fence_after();
+        const uint32_t ik = idesc_bf16(128, 64, true, false), im = idesc_bf16(128, 64, true, true);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 128, desc_mnmajor(S(GS::KC), kC, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 192, desc_mnmajor(S(GS::QR), kC, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), kC, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+        mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 0, ws.status, 46, fail)) goto cleanup;
+    tc_fence_after();
+    {  // final epilogue, channel d = tid: dq, dk, dGamma -> dg
+        float dG[kC];
+        float acc = 0.f, dGC = 0.f;
+        const float sc = p.scale;
+#pragma unroll
+        for (int rb = 0; rb < 4; ++rb) {
+            float aQt[16], aKh[16], aKr[16], aKc[16], aQr[16], aXk[16];
+            tmem_ld16(tmem + lb + 0 + 16 * rb, aQt);
+            tmem_ld16(tmem + lb + 64 + 16 * rb, aKh);
+            tmem_ld16(tmem + lb + 128 + 16 * rb, aKr);
+            tmem_ld16(tmem + lb + 192 + 16 * rb, aKc);
+            tmem_ld16(tmem + lb + 256 + 16 * rb, aQr);
+            tmem_ld16(tmem + lb + 448 + 16 * rb, aXk);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * rb + i;
+                float kv = 0.f, qv = 0.f;
+                if (r < c) {
+                    acc += g[((r0 + r) * HV + hv) * D + d];
+                    kv = ld_tile(sm + GS::K, r, d, kC);
+                    qv = ld_tile(sm + GS::Q, r, d, kC);
+                }
+                const float gm = acc * kLog2e;
+                const float E = exp2f(gm), ep = exp2f(gm - ref), em = exp2f(ref - gm), eh = exp2f(gC - gm);
+                const float b = sbeta[r];
+                const float dQt = sc * aQt[i], bX = b * aXk[i];
+                const float dqv = dQt * E + aQr[i] * ep;
+                const float dkv = aKh[i] * eh + bX * E + aKr[i] * ep + aKc[i] * em;
+                const float khk = aKh[i] * kv * eh;
+                // The factor values of the dGamma pair terms are the bf16 values the MMAs used, so that each
+                // in-chunk pair's contributions to its two rows cancel in the chunk sum as they do exactly.
+                const float kt_b = bfr(kv * E), qr_b = bfr(qv * ep), kr_b = bfr(kv * ep), kc_b = bfr(kv * em);
+                const float dgv = dQt * qv * E - khk + bX * kt_b + aQr[i] * qr_b + aKr[i] * kr_b - aKc[i] * kc_b;
+                dG[r] = r < c ? dgv : 0.f;
+                if (r < c) {
+                    dGC += khk;
+                    if (G == 1) {
+                        const int64_t o = ((r0 + r) * H + h) * D + d;
+                        dq_out[o] = __float2bfloat16_rn(dqv);
+                        dk_out[o] = __float2bfloat16_rn(dkv);
+                    } else {
+                        const int64_t o = ((r0 + r) * HV + hv) * D + d;
+                        ws.dqp[o] = dqv;
+                        ws.dkp[o] = dkv;
+                    }
+                }
+            }
+        }
+        dGC += segc[d] * rowdot;
+#pragma unroll
+        for (int r = 0; r < kC; ++r)
+            if (r == c - 1) dG[r] += dGC;
+        float run = 0.f;
+#pragma unroll
+        for (int r = kC - 1; r >= 0; --r) {
+            run += dG[r];
+            if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = run;
+        }
+    }
+cleanup:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// dq, dk of key head h = sum over its G value heads in ascending order.
+__global__ void k_tc_gva_reduce(int64_t rows, int H, int G, const float* __restrict__ dqp,
+                                const float* __restrict__ dkp, bf16* __restrict__ dq, bf16* __restrict__ dk) {
+    const int64_t total = rows * H * D;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int dd = (int)(i % D);
+        const int64_t rh = i / D;
+        const int hh = (int)(rh % H);
+        const int64_t r = rh / H;
+        const int64_t base = (r * H * G + (int64_t)hh * G) * D + dd;
+        float aq = 0.f, ak = 0.f;
+        for (int j = 0; j < G; ++j) {
+            aq += dqp[base + (int64_t)j * D];
+            ak += dkp[base + (int64_t)j * D];
+        }
+        dq[i] = __float2bfloat16_rn(aq);
+        dk[i] = __float2bfloat16_rn(ak);
+    }
+}
+
+}  // namespace
+
+cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t rows = (int64_t)p.B * p.T;
+    if (p.NT == 0 || rows == 0) return cudaSuccess;
+    GradMaps m;
+    memset(&m, 0, sizeof(m));
+    const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
+    if (!make_tmap_bf16_3d(&m.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+        !make_tmap_bf16_3d(&m.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+        !make_tmap_bf16_3d(&m.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
+        !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC))
+        return cudaErrorInvalidValue;
+    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 128, kGradsSmem, st>>>(
+        p, io.g, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
+    note_launch("tc_grads", st);
+    if (p.HV != p.H) {
+        k_tc_gva_reduce<<<1024, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq, (bf16*)io.dk);
+        note_launch("tc_gva_reduce", st);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -92,6 +92,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// As tmem_ld32 with 16 consecutive columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 // ---------------------------------------------------------------------- MMA
 // Shared-memory matrix descriptor, 128-byte swizzle (sm_100 format).
@@ -163,6 +174,52 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 __device__ __forceinline__ uint32_t tile_off(int r, int c, int R) {
     const uint32_t off = (uint32_t)((c >> 6) * R * 128 + r * 128 + (c & 63) * 2);
     return off ^ (((off >> 7) & 7u) << 4);
+}
+
+
+// ------------------------------------------------- tiles, bulk copies, waits
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+__device__ __forceinline__ void st_tile(uint8_t* tile, int r, int c, int R, float x) {
+    *reinterpret_cast<__nv_bfloat16*>(tile + tile_off(r, c, R)) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ float ld_tile(const uint8_t* tile, int r, int c, int R) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + tile_off(r, c, R)));
+}
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// Row r, columns c0 .. c0+7 of a tile with R rows, as one 16-byte store.
+__device__ __forceinline__ void st_tile_row8(uint8_t* tile, int r, int c0, int R, const float* x) {
+    uint4 v;
+    v.x = pack2(x[0], x[1]);
+    v.y = pack2(x[2], x[3]);
+    v.z = pack2(x[4], x[5]);
+    v.w = pack2(x[6], x[7]);
+    *reinterpret_cast<uint4*>(tile + tile_off(r, c0, R)) = v;
+}
+
+// Bulk copy shared -> global (16-byte aligned, size % 16 == 0) and its group ops.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Negated-A variant of the __nv_bfloat16 instruction descriptor.
+__host__ __device__ constexpr uint32_t idesc_neg_a(uint32_t id) { return id | (1u << 13); }
+
+// Uniform bounded wait: every thread waits on (bar, parity); if any gives up,
+// *fail becomes nonzero for all after the barrier.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* status, int code, int* fail) {
+    if (!mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
+    __syncthreads();
+    return *(volatile int*)fail == 0;
 }
 
 }  // namespace tc

@@ -32,6 +32,28 @@ extern "C" {
 kda_status kda_selftest_umma(int32_t M, int32_t N, int32_t Kd, int32_t mode, const void* A, const void* B,
                              float* raw, int* status, kda_stream_t stream);
 
+/*
+ * Stage-by-stage check of the tensor-core backward (bf16, K = V = 128 only):
+ * runs its first `stages` kernels (1: intra-chunk, 2: + forward state pass,
+ * 3: + reverse state-gradient pass, 4: + gradients, whose outputs are not
+ * returned here) on `ws`, leaving their intermediates in the workspace.
+ * Arguments as kda_chunk_bwd (dh0 nullable; needs h0). Errors:
+ * KDA_ERR_UNSUPPORTED off the tensor-core path, else as kda_chunk_bwd.
+ */
+kda_status kda_debug_bwd_stages(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
+                                const float* dht, float* dh0, int32_t stages, void* ws, size_t ws_bytes,
+                                kda_stream_t stream);
+
+/*
+ * Byte offset and size, inside the backward (pass = KDA_PASS_BWD) workspace,
+ * of a tensor-core intermediate: "w", "u", "kh", "qs", "aqk", "inv", "egc",
+ * "sin", "dso", "vn", "dvn" (bf16 tiles per chunk and value head, see the
+ * library's tile layout; "egc" is fp32). KDA_ERR_UNSUPPORTED off that path.
+ */
+kda_status kda_debug_ws_region(const kda_dims* dims, int32_t pass, const char* name, size_t* offset, size_t* bytes);
+
 #ifdef __cplusplus
 }
 #endif
