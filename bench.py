@@ -289,7 +289,12 @@ def gpu_arm(args):
     kda.build()
     lib = kda.load()
 
-    inp = kda_inputs.workload(WORKLOAD)
+    spec = kda_inputs.WORKLOADS[WORKLOAD]
+    if args.batch:
+        import dataclasses
+
+        spec = dataclasses.replace(spec, B=args.batch)
+    inp = kda_inputs.make(spec)
     B, T, H, K = inp.q.shape
     HV, V = inp.v.shape[2], inp.v.shape[3]
     tokens = B * T
@@ -392,7 +397,8 @@ def gpu_arm(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
+            "config": {"workload": WORKLOAD if not args.batch else f"{WORKLOAD} with B={args.batch}",
+                       "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
                        "head_dim": K, "chunk": 64, "parallelism": f"dp{world}" if world > 1 else "single",
                        "l2": "inputs larger than L2 (about 10 GB touched per step), no flush"},
             "roofline": roofline, "path": path, "clocks": clk, "gpu_launches": launches * args.steps,
@@ -417,6 +423,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size (smaller cases for profiling; not the benchmark workload)")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

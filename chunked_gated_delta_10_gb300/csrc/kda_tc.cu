@@ -50,10 +50,10 @@ constexpr int HALF = 64;               // V columns per state-pass CTA
 // 32 and 64. Out and scratch X (1024 floats) are shared; 128 threads.
 // ---------------------------------------------------------------------------
 __device__ void tri_inverse64(const float* L, float* Out, float* X) {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < kC * kC; i += blockDim.x) Out[i] = 0.f;
+    const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < kC * kC; i += nth) Out[i] = 0.f;
     __syncthreads();
-    if (lane < 16) {
+    if (warp < 4 && lane < 16) {
         const int b = warp * 16, j = lane;
         float x[16];
 #pragma unroll
@@ -67,35 +67,31 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
         for (int rr = 0; rr < 16; ++rr) Out[(b + rr) * kC + b + j] = x[rr];
     }
     __syncthreads();
-    // 16 -> 32: blocks (1,0) and (3,2)
-    {
-        const int pr = tid >> 6, base = 32 * pr;
-        for (int u = 0; u < 4; ++u) {
-            const int e = (tid & 63) * 4 + u, a = e >> 4, c = e & 15;
-            float s = 0.f;
-            for (int m = c; m < 16; ++m) s = fmaf(L[(base + 16 + a) * kC + base + m], Out[(base + m) * kC + base + c], s);
-            X[pr * 256 + a * 16 + c] = s;
-        }
-        __syncthreads();
-        for (int u = 0; u < 4; ++u) {
-            const int e = (tid & 63) * 4 + u, a = e >> 4, c = e & 15;
-            float s = 0.f;
-            for (int m = 0; m <= a; ++m)
-                s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
-            Out[(base + 16 + a) * kC + base + c] = -s;
-        }
-        __syncthreads();
-    }
-    // 32 -> 64: block rows 32..63, columns 0..31
-    for (int u = 0; u < 8; ++u) {
-        const int e = tid * 8 + u, a = e >> 5, c = e & 31;
+    // 16 -> 32: blocks (1,0) and (3,2); 512 entries
+    for (int e = tid; e < 512; e += nth) {
+        const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
         float s = 0.f;
-        for (int m = c; m < 32; ++m) s = fmaf(L[(32 + a) * kC + m], Out[m * kC + c], s);
-        X[a * 32 + c] = s;
+        for (int m = c; m < 16; ++m) s = fmaf(L[(base + 16 + a) * kC + base + m], Out[(base + m) * kC + base + c], s);
+        X[e] = s;
     }
     __syncthreads();
-    for (int u = 0; u < 8; ++u) {
-        const int e = tid * 8 + u, a = e >> 5, c = e & 31;
+    for (int e = tid; e < 512; e += nth) {
+        const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
+        float s = 0.f;
+        for (int m = 0; m <= a; ++m) s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
+        Out[(base + 16 + a) * kC + base + c] = -s;
+    }
+    __syncthreads();
+    // 32 -> 64: block rows 32..63, columns 0..31; 1024 entries
+    for (int e = tid; e < 1024; e += nth) {
+        const int a = e >> 5, c = e & 31;
+        float s = 0.f;
+        for (int m = c; m < 32; ++m) s = fmaf(L[(32 + a) * kC + m], Out[m * kC + c], s);
+        X[e] = s;
+    }
+    __syncthreads();
+    for (int e = tid; e < 1024; e += nth) {
+        const int a = e >> 5, c = e & 31;
         float s = 0.f;
         for (int m = 0; m <= a; ++m) s = fmaf(Out[(32 + a) * kC + 32 + m], X[m * 32 + c], s);
         Out[(32 + a) * kC + c] = -s;
@@ -104,164 +100,182 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 }
 
 // ---------------------------------------------------------------------------
-// tc_intra
+// tc_intra: 256 threads (two per key channel: rows 0..31 and 32..63); inputs
+// staged by TMA and transformed in place (q -> scale Q~, k -> K^, v -> beta V).
+// 112 KB of shared memory, two CTAs per SM.
 // ---------------------------------------------------------------------------
-constexpr int kIntraSmem = 1024 + 32768 + 3 * TCD + TCC + 4096 + 256 + 64;
+struct IS {
+    static constexpr int Q = 0, K = TCD, V = 2 * TCD, KQ = 3 * TCD, KC = 5 * TCD, XK = 6 * TCD, MISC = 7 * TCD;
+    // aliases: after the first MMA, KQ holds Akk / INV in fp32; after the last, W and U staging.
+    // after the first MMA, KC holds the bf16 INV tile and the inversion scratch.
+    static constexpr int AKK = KQ, FI = KQ + 16384, TINV = KC, XS = KC + TCC, WST = KQ, UST = KQ + TCD;
+    static constexpr int END = MISC + 256 + 64;
+};
+constexpr int kIntraSmem = IS::END;
 
-__global__ void __launch_bounds__(128, 2) k_tc_intra(Prob p, const bf16* __restrict__ q, const bf16* __restrict__ k,
-                                                      const bf16* __restrict__ v, const float* __restrict__ g,
-                                                      const bf16* __restrict__ beta, TcWs ws) {
-    extern __shared__ uint8_t smraw[];
-    uint8_t* sm = align1024(smraw);
-    uint8_t* tKQ = sm;               // [Kr; Qr] 128 x 128; after the first MMA: Akk, INV fp32
-    uint8_t* tKc = sm + 32768;       // 64 x 128
-    uint8_t* tXk = tKc + TCD;        // beta K~, 64 x 128
-    uint8_t* tXv = tXk + TCD;        // beta V, 64 x 128
-    uint8_t* tINV = tXv + TCD;       // 64 x 64
-    float* X = reinterpret_cast<float*>(tINV + TCC);
-    float* sb = X + 1024;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sb + 64);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
+struct IntraMaps {
+    CUtensorMap q, k, v;
+};
+
+__global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __restrict__ g,
+                                                      const bf16* __restrict__ beta, TcWs ws,
+                                                      const __grid_constant__ IntraMaps maps) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    float* sb = reinterpret_cast<float*>(sm + IS::MISC);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + IS::MISC + 256);  // [0] loads, [1] mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
     int* fail = reinterpret_cast<int*>(tslot + 1);
-    float* Akk = reinterpret_cast<float*>(tKQ);
-    float* Fi = Akk + kC * kC;
+    float* Akk = reinterpret_cast<float*>(sm + IS::AKK);
+    float* Fi = reinterpret_cast<float*>(sm + IS::FI);
+    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // phase-0 scratch (3 x 128 floats)
 
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = tid & 127, half = tid >> 7;
     const int HV = p.HV, H = p.H, hv = blockIdx.y, h = hv / (HV / H);
     const int64_t gc = blockIdx.x, ch = gc * HV + hv;
     int64_t r0;
     int c;
     chunk_rows(p, gc, r0, c);
-
     if (tid == 0) {
-        mbar_init(bar, 1);
+        *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
+        if (*fail) *(volatile int*)ws.status = 10;
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         fence_mbar_init();
-        *fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     if (tid < kC) sb[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
-
-    // Gamma2 (log2 units) of channel d = tid for all 64 rows.
-    const int d = tid;
-    float G2[kC];
-    {
-        float acc = 0.f;
-#pragma unroll
-        for (int r = 0; r < kC; ++r) {
-            const float gv = r < c ? g[((r0 + r) * HV + hv) * D + d] : 0.f;
-            acc += gv;
-            G2[r] = acc * kLog2e;
-        }
-    }
-    const int rmid = (c - 1) >> 1;
-    float ref = 0.f, gC = 0.f;
-#pragma unroll
-    for (int r = 0; r < kC; ++r) {
-        if (r == rmid) ref = G2[r];
-        if (r == c - 1) gC = G2[r];
-    }
-    ws.egc[ch * D + d] = exp2f(gC);
+    tc_fence_before();
     __syncthreads();
-    uint8_t* gKh = ws.kh + ch * TCD;
-    uint8_t* gQs = ws.qs + ch * TCD;
-#pragma unroll
-    for (int r = 0; r < kC; ++r) {
-        float kv = 0.f, qv = 0.f, vv = 0.f;
-        if (r < c) {
-            kv = __bfloat162float(k[((r0 + r) * H + h) * D + d]);
-            qv = __bfloat162float(q[((r0 + r) * H + h) * D + d]);
-            vv = __bfloat162float(v[((r0 + r) * HV + hv) * D + d]);
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (tid == 0 && *fail == 0) {
+        mbar_expect_tx(&bars[0], 3 * TCD);
+        for (int b = 0; b < 2; ++b) {
+            tma_load_3d(sm + IS::Q + b * (TCD / 2), &maps.q, 64 * b, h, (int)r0, &bars[0]);
+            tma_load_3d(sm + IS::K + b * (TCD / 2), &maps.k, 64 * b, h, (int)r0, &bars[0]);
+            tma_load_3d(sm + IS::V + b * (TCD / 2), &maps.v, 64 * b, hv, (int)r0, &bars[0]);
         }
-        const float b = sb[r], gm = G2[r];
+    }
+    float G2[32];
+    chunk_cumsum_log2(g, r0, c, HV, hv, d, half, tmp, G2);
+    // reference row (middle of the chunk, always in rows 0..31) and last valid row
+    const int rmid = (c - 1) >> 1;
+    if (half == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i == rmid) tmp[128 + d] = G2[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (32 * half + i == c - 1) tmp[256 + d] = G2[i];
+    __syncthreads();
+    const float ref = tmp[128 + d], gC = tmp[256 + d];
+    if (half == 0) ws.egc[ch * D + d] = exp2f(gC);
+    if (!wait_all(&bars[0], 0, ws.status, 11, fail)) goto cleanup;
+    // decayed factors; in place: q -> scale Q~, k -> K^, v -> beta V
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * half + i;
+        const bool in = r < c;
+        const float kv = in ? ld_tile(sm + IS::K, r, d, kC) : 0.f;
+        const float qv = in ? ld_tile(sm + IS::Q, r, d, kC) : 0.f;
+        const float vv = in ? ld_tile(sm + IS::V, r, d, kC) : 0.f;
+        const float b = sb[r], gm = G2[i];
         const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm), eh = exp2f(gC - gm);
-        st_tile(tKQ, r, d, 128, kv * ep);
-        st_tile(tKQ, kC + r, d, 128, qv * ep);
-        st_tile(tKc, r, d, kC, kv * em);
-        st_tile(tXk, r, d, kC, b * kv * E);
-        st_tile(tXv, r, d, kC, b * vv);
-        st_tile(gKh, r, d, kC, kv * eh);
-        st_tile(gQs, r, d, kC, p.scale * qv * E);
+        st_tile(sm + IS::KQ, r, d, 128, kv * ep);
+        st_tile(sm + IS::KQ, kC + r, d, 128, qv * ep);
+        st_tile(sm + IS::KC, r, d, kC, kv * em);
+        st_tile(sm + IS::XK, r, d, kC, b * kv * E);
+        st_tile(sm + IS::V, r, d, kC, b * vv);
+        st_tile(sm + IS::K, r, d, kC, kv * eh);
+        st_tile(sm + IS::Q, r, d, kC, p.scale * qv * E);
     }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     if (tid == 0) {
         const uint32_t id = idesc_bf16(128, 64, false, false);
         for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, desc_kmajor(smem_u32(tKQ), 128, ks), desc_kmajor(smem_u32(tKc), kC, ks), id, ks > 0);
-        mma_commit(bar);
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + IS::KQ), 128, ks), desc_kmajor(smem_u32(sm + IS::KC), kC, ks), id,
+                     ks > 0);
+        mma_commit(&bars[1]);
+        bulk_store(ws.kh + ch * TCD, sm + IS::K, TCD);
+        bulk_store(ws.qs + ch * TCD, sm + IS::Q, TCD);
+        bulk_commit();
     }
-    if (wait_all(bar, 0, ws.status, 11, fail)) {
-        tc_fence_after();
-        float row[kC];
-        tmem_ld32(tmem + lane_base, row);
-        tmem_ld32(tmem + lane_base + 32, row + 32);
+    if (!wait_all(&bars[1], 0, ws.status, 12, fail)) goto cleanup;
+    tc_fence_after();
+    {  // Akk (rows 0..63) and Aqk (rows 64..127): lane row 32 * (warp % 4) + lane, 32 columns per warp half
+        const int R = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+        float row[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0, row);
         tmem_ld_wait();
-        if (tid < kC) {  // Akk row r = tid (strictly lower, beta_r scaled)
-            const int r = tid;
-            for (int j = 0; j < kC; ++j) Akk[r * kC + j] = j < r ? sb[r] * row[j] : 0.f;
-        } else {  // Aqk row r = tid - 64 (lower incl. diagonal, scaled)
-            const int r = tid - kC;
+        if (R < kC) {
+            const int r = R;
+            for (int j = 0; j < 32; ++j) Akk[r * kC + c0 + j] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
+        } else {
+            const int r = R - kC;
             uint8_t* gA = ws.aqk + ch * TCC;
-            for (int c0 = 0; c0 < kC; c0 += 8) {
+            for (int u = 0; u < 32; u += 8) {
                 float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = (c0 + u <= r) ? p.scale * row[c0 + u] : 0.f;
+                for (int t = 0; t < 8; ++t) x[t] = (c0 + u + t <= r) ? p.scale * row[u + t] : 0.f;
                 uint4 vv;
                 vv.x = pack2(x[0], x[1]);
                 vv.y = pack2(x[2], x[3]);
                 vv.z = pack2(x[4], x[5]);
                 vv.w = pack2(x[6], x[7]);
-                *reinterpret_cast<uint4*>(gA + tile_off(r, c0, kC)) = vv;
+                *reinterpret_cast<uint4*>(gA + tile_off(r, c0 + u, kC)) = vv;
             }
         }
-        tc_fence_before();
     }
+    tc_fence_before();
     __syncthreads();
-    if (*(volatile int*)fail == 0) {
-        tri_inverse64(Akk, Fi, X);
-        uint8_t* gI = ws.inv + ch * TCC;
-        if (tid < kC) {
-            const int r = tid;
-            for (int c0 = 0; c0 < kC; c0 += 8) {
-                st_tile_row8(tINV, r, c0, kC, Fi + r * kC + c0);
-                *reinterpret_cast<uint4*>(gI + tile_off(r, c0, kC)) =
-                    *reinterpret_cast<const uint4*>(tINV + tile_off(r, c0, kC));
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-        if (tid == 0) {
-            const uint32_t id = idesc_bf16(128, 64, true, false);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(tXk), kC, ks), desc_kmajor(smem_u32(tINV), kC, ks), id,
-                         ks > 0);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(tXv), kC, ks), desc_kmajor(smem_u32(tINV), kC, ks), id,
-                         ks > 0);
-            mma_commit(bar);
-        }
-        if (wait_all(bar, 1, ws.status, 12, fail)) {
-            tc_fence_after();
-            uint8_t* gW = ws.w + ch * TCD;
-            uint8_t* gU = ws.u + ch * TCD;
-            float col[32];
-            for (int half = 0; half < 2; ++half) {
-                tmem_ld32(tmem + lane_base + 64 + 32 * half, col);
-                tmem_ld_wait();
-                for (int j = 0; j < 32; ++j) st_tile(gW, 32 * half + j, d, kC, col[j]);
-                tmem_ld32(tmem + lane_base + 128 + 32 * half, col);
-                tmem_ld_wait();
-                for (int j = 0; j < 32; ++j) st_tile(gU, 32 * half + j, d, kC, col[j]);
-            }
-            tc_fence_before();
-        }
+    tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
+    for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
+        const int r = e >> 3, c0 = (e & 7) * 8;
+        st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
     }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, true, false);
+        const uint32_t ti = smem_u32(sm + IS::TINV);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 64, desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), desc_kmajor(ti, kC, ks), id, ks > 0);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + IS::V), kC, ks), desc_kmajor(ti, kC, ks), id, ks > 0);
+        mma_commit(&bars[1]);
+        bulk_store(ws.inv + ch * TCC, sm + IS::TINV, TCC);
+        bulk_commit();
+    }
+    if (!wait_all(&bars[1], 1, ws.status, 13, fail)) goto cleanup;
+    tc_fence_after();
+    {  // w^T, u^T: lane = channel 32 * (warp % 4) + lane, 32 chunk rows per warp half
+        const int dd = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+        float col[32];
+        tmem_ld32(tmem + lb + 64 + c0, col);
+        tmem_ld_wait();
+        for (int j = 0; j < 32; ++j) st_tile(sm + IS::WST, c0 + j, dd, kC, col[j]);
+        tmem_ld32(tmem + lb + 128 + c0, col);
+        tmem_ld_wait();
+        for (int j = 0; j < 32; ++j) st_tile(sm + IS::UST, c0 + j, dd, kC, col[j]);
+    }
+    tc_fence_before();
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
+        bulk_store(ws.u + ch * TCD, sm + IS::UST, TCD);
+        bulk_commit();
+    }
+cleanup:
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
@@ -562,7 +576,14 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         return cudaErrorInvalidValue;
     const bf16 *q = (const bf16*)io.q, *k = (const bf16*)io.k, *v = (const bf16*)io.v, *beta = (const bf16*)io.beta;
     if (p.NT > 0 && stages >= 1) {
-        k_tc_intra<<<dim3((unsigned)p.NT, p.HV), 128, kIntraSmem, st>>>(p, q, k, v, io.g, beta, ws);
+        IntraMaps im;
+        memset(&im, 0, sizeof(im));
+        const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
+        if (!make_tmap_bf16_3d(&im.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+            !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+            !make_tmap_bf16_3d(&im.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC))
+            return cudaErrorInvalidValue;
+        k_tc_intra<<<dim3((unsigned)p.NT, p.HV), 256, kIntraSmem, st>>>(p, io.g, beta, ws, im);
         note_launch("tc_intra", st);
     }
     if (stages >= 2) {

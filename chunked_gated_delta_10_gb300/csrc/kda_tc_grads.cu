@@ -1,7 +1,7 @@
 // Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
 // K = V = 128, chunks of 64), and the grouped-value-head reduction.
 //
-// One CTA per (chunk, value head), 128 threads. Inputs: q, k, v, dO (TMA),
+// One CTA per (chunk, value head), 256 threads. Inputs: q, k, v, dO (TMA),
 // and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
 // (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
 // Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
@@ -50,7 +50,10 @@ struct GS {
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
     static constexpr int DW = DSO + TDD;
     static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, DINV = DM + TCC, TT = DINV + TCC;
-    static constexpr int EGC = TT + TCC, BETA = EGC + 512, DB = BETA + 256, BARS = DB + 256, END = BARS + 64;
+    static constexpr int EGC = TT + TCC, BETA = EGC + 512;
+    // fixed-order exchanges between the two threads of a channel / the two column halves of a row
+    static constexpr int XRD = BETA + 256, XGC = XRD + 1024, XT1 = XGC + 1024, XDB = XT1 + 512;
+    static constexpr int BARS = XDB + 1024, END = BARS + 64;
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
@@ -60,21 +63,29 @@ struct GradMaps {
     CUtensorMap q, k, v, d_o;
 };
 
-__global__ void __launch_bounds__(128, 1)
+// 256 threads. Channel-oriented work: thread (d = tid % 128, half = tid / 128)
+// owns key channel d for chunk rows 32 * half .. 32 * half + 31. Row-oriented
+// work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16),
+// column half warp / 4.
+__global__ void __launch_bounds__(256, 1)
     k_tc_grads(Prob p, const float* __restrict__ g, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
                bf16* __restrict__ dk_out, bf16* __restrict__ dv_out, float* __restrict__ dg_out,
                bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     float* sbeta = reinterpret_cast<float*>(sm + GS::BETA);
-    float* sdb = reinterpret_cast<float*>(sm + GS::DB);
     const float* segc = reinterpret_cast<const float*>(sm + GS::EGC);
+    float* xrd = reinterpret_cast<float*>(sm + GS::XRD);
+    float* xgc = reinterpret_cast<float*>(sm + GS::XGC);
+    float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
+    float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);  // [0] loads, [1] mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
     int* fail = reinterpret_cast<int*>(tslot + 1);
     auto S = [&](int off) { return smem_u32(sm + off); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = tid & 127, half = tid >> 7, q4 = warp & 3, wh = warp >> 2;
     const int HV = p.HV, H = p.H, G = HV / H, hv = blockIdx.y, h = hv / G;
     const int64_t gc = blockIdx.x, ch = gc * HV + hv;
     int64_t r0;
@@ -88,15 +99,14 @@ __global__ void __launch_bounds__(128, 1)
         *fail = 0;
     }
     if (warp == 0) tmem_alloc(tslot, 512);
-    if (tid < kC) {
-        sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
-        sdb[tid] = 0.f;
-    }
+    if (tid < kC) sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lb = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
+    const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
+    const bool rv = lane < 16;
     if (tid == 0) {
         mbar_expect_tx(&bars[0], 6 * TCD + 2 * TDD + TCC + 512);
         const int row = (int)r0;
@@ -113,23 +123,21 @@ __global__ void __launch_bounds__(128, 1)
         bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
         bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
     }
-
-    // Gamma2 (log2 units) of channel d = tid; reference and last valid rows.
-    const int d = tid;
+    // Gamma2 of channel d for this thread's 32 rows (same order of additions as tc_intra)
+    float G2[32];
+    chunk_cumsum_log2(g, r0, c, HV, hv, d, half, xt1, G2);
     const int rmid = (c - 1) >> 1;
-    float ref = 0.f, gC = 0.f;
-    {
-        float acc = 0.f;
-#pragma unroll 8
-        for (int r = 0; r < kC; ++r) {
-            if (r < c) acc += g[((r0 + r) * HV + hv) * D + d];
-            const float gm = acc * kLog2e;
-            if (r == rmid) ref = gm;
-            if (r == c - 1) gC = gm;
-        }
+    if (half == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+            if (i == rmid) xgc[d] = G2[i];
     }
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+        if (32 * half + i == c - 1) xgc[128 + d] = G2[i];
+    __syncthreads();
+    const float ref = xgc[d], gC = xgc[128 + d];
 
-    float rowdot = 0.f;
     if (!wait_all(&bars[0], 0, ws.status, 41, fail)) goto cleanup;
     if (tid == 0) {  // phase A
         tc_fence_after();
@@ -146,57 +154,54 @@ __global__ void __launch_bounds__(128, 1)
             mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
         mma_commit(&bars[1]);
     }
-    for (int c8 = 0; c8 < D; c8 += 8) {  // <S_in[d,:], dS_out[d,:]>
-        const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
-        const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    {  // <S_in[d, v], dS_out[d, v]> over this thread's 64 columns v
+        float rd = 0.f;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
-            rowdot = fmaf(fa.x, fb.x, rowdot);
-            rowdot = fmaf(fa.y, fb.y, rowdot);
+        for (int c8 = 64 * half; c8 < 64 * half + 64; c8 += 8) {
+            const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
+            const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
+            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
+                rd = fmaf(fa.x, fb.x, rd);
+                rd = fmaf(fa.y, fb.y, rd);
+            }
         }
+        xrd[half * 128 + d] = rd;
     }
     if (!wait_all(&bars[1], 0, ws.status, 42, fail)) goto cleanup;
     tc_fence_after();
-    {  // epilogue A: dw rows and dN rows (row r = 16 warp + lane for lane < 16)
-        const int r = 16 * warp + lane;
-        const bool rv = lane < 16;
+    {  // epilogue A: dw row segment (64 columns) and dN row segment (32 columns)
         float x[32];
-        for (int cb = 0; cb < 4; ++cb) {
-            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, r, 32 * cb + 8 * u, kC, x + 8 * u);
-        }
         for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lb + 256 + 32 * cb, x);
+            const int col = 64 * wh + 32 * cb;
+            tmem_ld32(tmem + lb + 128 + col, x);
             tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 32; ++u) x[u] = (32 * cb + u <= r && r < c) ? p.scale * x[u] : 0.f;
             if (rv)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DN, r, 32 * cb + 8 * u, kC, x + 8 * u);
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, col + 8 * u, kC, x + 8 * u);
         }
+        tmem_ld32(tmem + lb + 256 + 32 * wh, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = (32 * wh + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
+        if (rv)
+            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DN, rrow, 32 * wh + 8 * u, kC, x + 8 * u);
     }
     tc_fence_before();
-    {  // decayed factor tiles of channel d (rows >= c are zero)
-        float acc = 0.f;
-#pragma unroll 4
-        for (int r = 0; r < kC; ++r) {
-            float kv = 0.f, qv = 0.f;
-            if (r < c) {
-                acc += g[((r0 + r) * HV + hv) * D + d];
-                kv = ld_tile(sm + GS::K, r, d, kC);
-                qv = ld_tile(sm + GS::Q, r, d, kC);
-            }
-            const float gm = acc * kLog2e;
-            const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm);
-            st_tile(sm + GS::KR, r, d, kC, kv * ep);
-            st_tile(sm + GS::KC, r, d, kC, kv * em);
-            st_tile(sm + GS::QR, r, d, kC, qv * ep);
-            st_tile(sm + GS::KT, r, d, kC, kv * E);
-        }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {  // decayed factor tiles, channel d, this thread's rows (rows >= c are zero)
+        const int r = 32 * half + i;
+        const bool in = r < c;
+        const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
+        const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
+        const float gm = G2[i];
+        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm);
+        st_tile(sm + GS::KR, r, d, kC, kv * ep);
+        st_tile(sm + GS::KC, r, d, kC, kv * em);
+        st_tile(sm + GS::QR, r, d, kC, qv * ep);
+        st_tile(sm + GS::KT, r, d, kC, kv * E);
     }
     fence_async_smem();
     __syncthreads();
@@ -223,34 +228,33 @@ __global__ void __launch_bounds__(128, 1)
     if (!wait_all(&bars[1], 1, ws.status, 43, fail)) goto cleanup;
     tc_fence_after();
     {  // epilogue B: dbeta (INV part), dINV columns, dv rows
-        const int r = 16 * warp + lane;
-        const bool rv = lane < 16;
+        const float br = rv ? sbeta[rrow] : 0.f;
         float x[32];
         float db = 0.f;
-        const float br = rv ? sbeta[r] : 0.f;
-        for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 32; ++u) {
-                    const int j = 32 * cb + u;
-                    db = fmaf(ld_tile(sm + GS::INV, j, r, kC), x[u], db);
-                    st_tile(sm + GS::DINV, j, r, kC, br * x[u]);
-                }
+        tmem_ld32(tmem + lb + 128 + 32 * wh, x);
+        tmem_ld_wait();
+        if (rv) {
+#pragma unroll
+            for (int u = 0; u < 32; ++u) {
+                const int j = 32 * wh + u;
+                db = fmaf(ld_tile(sm + GS::INV, j, rrow, kC), x[u], db);
+                st_tile(sm + GS::DINV, j, rrow, kC, br * x[u]);
+            }
+            xdb[wh * 64 + rrow] = db;
         }
-        if (rv) sdb[r] = db;
-        bf16* dvrow = dv_out + ((r0 + r) * HV + hv) * D;
-        for (int cb = 0; cb < 4; ++cb) {
-            tmem_ld32(tmem + lb + 320 + 32 * cb, x);
+        bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D;
+        for (int cb = 0; cb < 2; ++cb) {
+            const int col = 64 * wh + 32 * cb;
+            tmem_ld32(tmem + lb + 320 + col, x);
             tmem_ld_wait();
-            if (rv && r < c)
+            if (rv && rrow < c)
                 for (int u = 0; u < 32; u += 8) {
                     uint4 vv;
                     vv.x = pack2(br * x[u], br * x[u + 1]);
                     vv.y = pack2(br * x[u + 2], br * x[u + 3]);
                     vv.z = pack2(br * x[u + 4], br * x[u + 5]);
                     vv.w = pack2(br * x[u + 6], br * x[u + 7]);
-                    *reinterpret_cast<uint4*>(dvrow + 32 * cb + u) = vv;
+                    *reinterpret_cast<uint4*>(dvrow + col + u) = vv;
                 }
         }
     }
@@ -267,14 +271,11 @@ __global__ void __launch_bounds__(128, 1)
     if (!wait_all(&bars[1], 0, ws.status, 44, fail)) goto cleanup;
     tc_fence_after();
     {
-        const int r = 16 * warp + lane;
         float x[32];
-        for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lb + 128 + 32 * cb, x);
-            tmem_ld_wait();
-            if (lane < 16)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::TT, r, 32 * cb + 8 * u, kC, x + 8 * u);
-        }
+        tmem_ld32(tmem + lb + 128 + 32 * wh, x);
+        tmem_ld_wait();
+        if (rv)
+            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::TT, rrow, 32 * wh + 8 * u, kC, x + 8 * u);
     }
     tc_fence_before();
     fence_async_smem();
@@ -288,31 +289,31 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (!wait_all(&bars[1], 1, ws.status, 45, fail)) goto cleanup;
     tc_fence_after();
-    {  // epilogue D: dbeta (Akk part), dM rows
-        const int r = 16 * warp + lane;
-        const bool rv = lane < 16;
-        const float br = rv ? sbeta[r] : 0.f;
-        float db = rv ? sdb[r] : 0.f;
+    {  // epilogue D: dbeta (Akk part), dM row segments
+        const float br = rv ? sbeta[rrow] : 0.f;
         float a[32], m[32];
-        for (int cb = 0; cb < 2; ++cb) {
-            tmem_ld32(tmem + lb + 320 + 32 * cb, a);
-            tmem_ld32(tmem + lb + 192 + 32 * cb, m);
-            tmem_ld_wait();
+        float db = 0.f;
+        tmem_ld32(tmem + lb + 320 + 32 * wh, a);
+        tmem_ld32(tmem + lb + 192 + 32 * wh, m);
+        tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int j = 32 * cb + u;
-                const bool in = j < r && r < c;
-                db = in ? fmaf(a[u], m[u], db) : db;
-                a[u] = in ? br * a[u] : 0.f;
-            }
-            if (rv)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DM, r, 32 * cb + 8 * u, kC, a + 8 * u);
+        for (int u = 0; u < 32; ++u) {
+            const int j = 32 * wh + u;
+            const bool in = j < rrow && rrow < c;
+            db = in ? fmaf(a[u], m[u], db) : db;
+            a[u] = in ? br * a[u] : 0.f;
         }
-        if (rv && r < c) db_out[(r0 + r) * HV + hv] = __float2bfloat16_rn(db);
+        if (rv) {
+            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DM, rrow, 32 * wh + 8 * u, kC, a + 8 * u);
+            xdb[128 + wh * 64 + rrow] = db;
+        }
     }
     tc_fence_before();
     fence_async_smem();
     __syncthreads();
+    if (tid < kC && tid < c)
+        db_out[(r0 + tid) * HV + hv] =
+            __float2bfloat16_rn((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid]));
     if (tid == 0) {  // phase E
         tc_fence_after();
         const uint32_t ik = idesc_bf16(128, 64, true, false), im = idesc_bf16(128, 64, true, true);
@@ -326,30 +327,28 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (!wait_all(&bars[1], 0, ws.status, 46, fail)) goto cleanup;
     tc_fence_after();
-    {  // final epilogue, channel d = tid: dq, dk, dGamma -> dg
-        float dG[kC];
-        float acc = 0.f, dGC = 0.f;
+    {  // final epilogue, channel d, rows 32 * half .. +31: dq, dk, dGamma -> dg
+        float dG[32];
+        float dGC = 0.f;
         const float sc = p.scale;
 #pragma unroll
-        for (int rb = 0; rb < 4; ++rb) {
+        for (int rb = 0; rb < 2; ++rb) {
+            const uint32_t cb = (uint32_t)(32 * half + 16 * rb);
             float aQt[16], aKh[16], aKr[16], aKc[16], aQr[16], aXk[16];
-            tmem_ld16(tmem + lb + 0 + 16 * rb, aQt);
-            tmem_ld16(tmem + lb + 64 + 16 * rb, aKh);
-            tmem_ld16(tmem + lb + 128 + 16 * rb, aKr);
-            tmem_ld16(tmem + lb + 192 + 16 * rb, aKc);
-            tmem_ld16(tmem + lb + 256 + 16 * rb, aQr);
-            tmem_ld16(tmem + lb + 448 + 16 * rb, aXk);
+            tmem_ld16(tmem + lb + 0 + cb, aQt);
+            tmem_ld16(tmem + lb + 64 + cb, aKh);
+            tmem_ld16(tmem + lb + 128 + cb, aKr);
+            tmem_ld16(tmem + lb + 192 + cb, aKc);
+            tmem_ld16(tmem + lb + 256 + cb, aQr);
+            tmem_ld16(tmem + lb + 448 + cb, aXk);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int r = 16 * rb + i;
-                float kv = 0.f, qv = 0.f;
-                if (r < c) {
-                    acc += g[((r0 + r) * HV + hv) * D + d];
-                    kv = ld_tile(sm + GS::K, r, d, kC);
-                    qv = ld_tile(sm + GS::Q, r, d, kC);
-                }
-                const float gm = acc * kLog2e;
+                const int ii = 16 * rb + i, r = 32 * half + ii;
+                const bool in = r < c;
+                const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
+                const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
+                const float gm = G2[ii];
                 const float E = exp2f(gm), ep = exp2f(gm - ref), em = exp2f(ref - gm), eh = exp2f(gC - gm);
                 const float b = sbeta[r];
                 const float dQt = sc * aQt[i], bX = b * aXk[i];
@@ -360,8 +359,8 @@ __global__ void __launch_bounds__(128, 1)
                 // in-chunk pair's contributions to its two rows cancel in the chunk sum as they do exactly.
                 const float kt_b = bfr(kv * E), qr_b = bfr(qv * ep), kr_b = bfr(kv * ep), kc_b = bfr(kv * em);
                 const float dgv = dQt * qv * E - khk + bX * kt_b + aQr[i] * qr_b + aKr[i] * kr_b - aKc[i] * kc_b;
-                dG[r] = r < c ? dgv : 0.f;
-                if (r < c) {
+                dG[ii] = in ? dgv : 0.f;
+                if (in) {
                     dGC += khk;
                     if (G == 1) {
                         const int64_t o = ((r0 + r) * H + h) * D + d;
@@ -375,15 +374,25 @@ __global__ void __launch_bounds__(128, 1)
                 }
             }
         }
-        dGC += segc[d] * rowdot;
+        xgc[half * 128 + d] = dGC;
+        __syncthreads();
+        const float dGCt = segc[d] * (xrd[d] + xrd[128 + d]) + (xgc[d] + xgc[128 + d]);
 #pragma unroll
-        for (int r = 0; r < kC; ++r)
-            if (r == c - 1) dG[r] += dGC;
+        for (int i = 0; i < 32; ++i)
+            if (32 * half + i == c - 1) dG[i] += dGCt;
         float run = 0.f;
 #pragma unroll
-        for (int r = kC - 1; r >= 0; --r) {
-            run += dG[r];
-            if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = run;
+        for (int i = 31; i >= 0; --i) {
+            run += dG[i];
+            dG[i] = run;
+        }
+        if (half == 1) xt1[d] = run;
+        __syncthreads();
+        const float carry = half == 0 ? xt1[d] : 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * half + i;
+            if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = dG[i] + carry;
         }
     }
 cleanup:
@@ -427,7 +436,7 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
         !make_tmap_bf16_3d(&m.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
         !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC))
         return cudaErrorInvalidValue;
-    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 128, kGradsSmem, st>>>(
+    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 256, kGradsSmem, st>>>(
         p, io.g, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
     if (p.HV != p.H) {

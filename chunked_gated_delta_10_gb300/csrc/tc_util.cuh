@@ -222,5 +222,31 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* st
     return *(volatile int*)fail == 0;
 }
 
+// In-chunk cumulative sum of g for channel d over rows [32 * half, 32 * half + 32)
+// in log2 units (rows >= c add nothing), split over two threads per channel:
+// half 0 sums rows 0..31, half 1 adds half 0's total. `tot` is 128 floats of
+// shared scratch. Every caller uses this exact order of additions, so the
+// decay factors recomputed in the gradient kernel match the ones used here.
+__device__ __forceinline__ void chunk_cumsum_log2(const float* __restrict__ g, int64_t r0, int c, int HV, int hv,
+                                                  int d, int half, float* tot, float (&G2)[32]) {
+    float gv[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int r = 32 * half + i;
+        gv[i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        acc += gv[i];
+        G2[i] = acc;
+    }
+    if (half == 0) tot[d] = acc;
+    __syncthreads();
+    const float off = half ? tot[d] : 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) G2[i] = (G2[i] + off) * 1.4426950408889634f;
+}
+
 }  // namespace tc
 }  // namespace kda
