@@ -49,7 +49,8 @@ struct Layout {
 
 // The backward of bf16 inputs with K = V = 128 runs on the tensor-core path.
 bool use_tc(const kda_dims* d, int pass) {
-    return pass == KDA_PASS_BWD && d->dtype == KDA_DTYPE_BF16 && d->K == 128 && d->V == 128;
+    // (the state passes put sequences on grid z, which holds at most 65535)
+    return pass == KDA_PASS_BWD && d->dtype == KDA_DTYPE_BF16 && d->K == 128 && d->V == 128 && d->num_seqs <= 65535;
 }
 
 Layout layout(const Prob& p, int pass, bool tc) {

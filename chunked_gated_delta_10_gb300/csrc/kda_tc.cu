@@ -49,52 +49,77 @@ constexpr int HALF = 64;               // V columns per state-pass CTA
 // 2 x 2 block formula [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]] at
 // 32 and 64. Out and scratch X (1024 floats) are shared; 128 threads.
 // ---------------------------------------------------------------------------
+// The strictly lower L is stored skewed: element (r, m) at r * 64 + ((m + r) & 63),
+// so a warp writing one row per lane hits 32 different banks.
+__device__ __forceinline__ int lsk(int r, int m) { return r * kC + ((m + r) & (kC - 1)); }
+
 __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < kC * kC; i += nth) Out[i] = 0.f;
     __syncthreads();
     if (warp < 4 && lane < 16) {
+        // diagonal 16 x 16 block `warp`, column j = lane, right-looking: once x[m] is
+        // known, every later row's partial sum takes its term (independent FMAs).
         const int b = warp * 16, j = lane;
-        float x[16];
+        float acc[16], x[16];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            float s = 0.f;
+        for (int rr = 0; rr < 16; ++rr) acc[rr] = 0.f;
 #pragma unroll
-            for (int m = 0; m < rr; ++m) s = fmaf(L[(b + rr) * kC + b + m], x[m], s);
-            x[rr] = rr == j ? 1.f : (rr > j ? -s : 0.f);
+        for (int m = 0; m < 16; ++m) {
+            x[m] = m == j ? 1.f : (m > j ? -acc[m] : 0.f);
+#pragma unroll
+            for (int rr = m + 1; rr < 16; ++rr) acc[rr] = fmaf(L[lsk(b + rr, b + m)], x[m], acc[rr]);
         }
 #pragma unroll
         for (int rr = 0; rr < 16; ++rr) Out[(b + rr) * kC + b + j] = x[rr];
     }
     __syncthreads();
-    // 16 -> 32: blocks (1,0) and (3,2); 512 entries
+    // 16 -> 32: blocks (1,0) and (3,2). X = L21 D0 (D0 lower triangular, zeros included), then -D1 X.
     for (int e = tid; e < 512; e += nth) {
         const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
         float s = 0.f;
-        for (int m = c; m < 16; ++m) s = fmaf(L[(base + 16 + a) * kC + base + m], Out[(base + m) * kC + base + c], s);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s = fmaf(L[lsk(base + 16 + a, base + m)], Out[(base + m) * kC + base + c], s);
         X[e] = s;
     }
     __syncthreads();
     for (int e = tid; e < 512; e += nth) {
         const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
         float s = 0.f;
-        for (int m = 0; m <= a; ++m) s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
         Out[(base + 16 + a) * kC + base + c] = -s;
     }
     __syncthreads();
-    // 32 -> 64: block rows 32..63, columns 0..31; 1024 entries
-    for (int e = tid; e < 1024; e += nth) {
-        const int a = e >> 5, c = e & 31;
-        float s = 0.f;
-        for (int m = c; m < 32; ++m) s = fmaf(L[(32 + a) * kC + m], Out[m * kC + c], s);
-        X[e] = s;
+    // 32 -> 64: rows 32..63, columns 0..31; each thread a 1 x 4 strip (4 independent sums)
+    for (int e = tid; e < 256; e += nth) {
+        const int a = e >> 3, c0 = (e & 7) * 4;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float l = L[lsk(32 + a, m)];
+            const float4 o = *reinterpret_cast<const float4*>(Out + m * kC + c0);
+            s0 = fmaf(l, o.x, s0);
+            s1 = fmaf(l, o.y, s1);
+            s2 = fmaf(l, o.z, s2);
+            s3 = fmaf(l, o.w, s3);
+        }
+        *reinterpret_cast<float4*>(X + a * 32 + c0) = make_float4(s0, s1, s2, s3);
     }
     __syncthreads();
-    for (int e = tid; e < 1024; e += nth) {
-        const int a = e >> 5, c = e & 31;
-        float s = 0.f;
-        for (int m = 0; m <= a; ++m) s = fmaf(Out[(32 + a) * kC + 32 + m], X[m * 32 + c], s);
-        Out[(32 + a) * kC + c] = -s;
+    for (int e = tid; e < 256; e += nth) {
+        const int a = e >> 3, c0 = (e & 7) * 4;
+        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 32; ++m) {
+            const float l = Out[(32 + a) * kC + 32 + m];
+            const float4 xv = *reinterpret_cast<const float4*>(X + m * 32 + c0);
+            s0 = fmaf(l, xv.x, s0);
+            s1 = fmaf(l, xv.y, s1);
+            s2 = fmaf(l, xv.z, s2);
+            s3 = fmaf(l, xv.w, s3);
+        }
+        *reinterpret_cast<float4*>(Out + (32 + a) * kC + c0) = make_float4(-s0, -s1, -s2, -s3);
     }
     __syncthreads();
 }
@@ -127,7 +152,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     int* fail = reinterpret_cast<int*>(tslot + 1);
     float* Akk = reinterpret_cast<float*>(sm + IS::AKK);
     float* Fi = reinterpret_cast<float*>(sm + IS::FI);
-    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // phase-0 scratch (3 x 128 floats)
+    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // phase-0 scratch (6 x 128 floats)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = tid & 127, half = tid >> 7;
@@ -158,19 +183,19 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         }
     }
     float G2[32];
-    chunk_cumsum_log2(g, r0, c, HV, hv, d, half, tmp, G2);
+    quarter_cumsum_log2<2>(g, r0, c, HV, hv, d, 2 * half, tmp, G2);
     // reference row (middle of the chunk, always in rows 0..31) and last valid row
     const int rmid = (c - 1) >> 1;
     if (half == 0) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-            if (i == rmid) tmp[128 + d] = G2[i];
+            if (i == rmid) tmp[512 + d] = G2[i];
     }
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-        if (32 * half + i == c - 1) tmp[256 + d] = G2[i];
+        if (32 * half + i == c - 1) tmp[640 + d] = G2[i];
     __syncthreads();
-    const float ref = tmp[128 + d], gC = tmp[256 + d];
+    const float ref = tmp[512 + d], gC = tmp[640 + d];
     if (half == 0) ws.egc[ch * D + d] = exp2f(gC);
     if (!wait_all(&bars[0], 0, ws.status, 11, fail)) goto cleanup;
     // decayed factors; in place: q -> scale Q~, k -> K^, v -> beta V
@@ -214,7 +239,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         tmem_ld_wait();
         if (R < kC) {
             const int r = R;
-            for (int j = 0; j < 32; ++j) Akk[r * kC + c0 + j] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
+            for (int j = 0; j < 32; ++j) Akk[lsk(r, c0 + j)] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
         } else {
             const int r = R - kC;
             uint8_t* gA = ws.aqk + ch * TCC;
@@ -281,7 +306,8 @@ cleanup:
 }
 
 // ---------------------------------------------------------------------------
-// tc_state_fwd: one CTA per (sequence, value head, V half); 128 threads,
+// tc_state_fwd: one CTA per (V half, value head, sequence) -- the two halves of
+// one head are adjacent in launch order so their shared tile reads hit L2; 128 threads,
 // thread t owns state row t (64 fp32 columns). Double-buffered chunk inputs.
 // ---------------------------------------------------------------------------
 struct FwdBuf {
@@ -301,7 +327,7 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, n = blockIdx.x, hv = blockIdx.y, z = blockIdx.z, v0 = z * HALF;
+    const int HV = p.HV, z = blockIdx.x, hv = blockIdx.y, n = blockIdx.z, v0 = z * HALF;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, n = blockIdx.x, hv = blockIdx.y, z = blockIdx.z, v0 = z * HALF;
+    const int HV = p.HV, z = blockIdx.x, hv = blockIdx.y, n = blockIdx.z, v0 = z * HALF;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
@@ -587,11 +613,11 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         note_launch("tc_intra", st);
     }
     if (stages >= 2) {
-        k_tc_state_fwd<<<dim3(p.N, p.HV, 2), 128, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
+        k_tc_state_fwd<<<dim3(2, p.HV, p.N), 128, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
         note_launch("tc_state_fwd", st);
     }
     if (stages >= 3) {
-        k_tc_ds_rev<<<dim3(p.N, p.HV, 2), 128, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
+        k_tc_ds_rev<<<dim3(2, p.HV, p.N), 128, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
         note_launch("tc_ds_rev", st);
     }
     if (stages >= 4) {

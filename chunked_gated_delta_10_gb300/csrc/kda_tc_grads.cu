@@ -1,7 +1,7 @@
 // Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
 // K = V = 128, chunks of 64), and the grouped-value-head reduction.
 //
-// One CTA per (chunk, value head), 256 threads. Inputs: q, k, v, dO (TMA),
+// One CTA per (chunk, value head), 512 threads. Inputs: q, k, v, dO (TMA),
 // and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
 // (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
 // Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
@@ -50,10 +50,12 @@ struct GS {
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
     static constexpr int DW = DSO + TDD;
     static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, DINV = DM + TCC, TT = DINV + TCC;
-    static constexpr int EGC = TT + TCC, BETA = EGC + 512;
-    // fixed-order exchanges between the two threads of a channel / the two column halves of a row
-    static constexpr int XRD = BETA + 256, XGC = XRD + 1024, XT1 = XGC + 1024, XDB = XT1 + 512;
-    static constexpr int BARS = XDB + 1024, END = BARS + 64;
+    static constexpr int EGC = TT + TCC, BETA = EGC + 512, BARS = BETA + 256, END = BARS + 64;
+    // exchange scratch: before phase C the TT tile area holds the gate-cumsum quarter totals
+    // and the reference / last-row gates; after phase A the dead dO tile holds the fixed-order
+    // partial sums of <S_in, dS_out>, the Gamma_C terms, the dg quarter totals and dbeta.
+    static constexpr int XTOT = TT, XRG = TT + 2048;
+    static constexpr int XRD = DO, XGC = DO + 2048, XT1 = DO + 4096, XDB = DO + 6144;
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
@@ -63,11 +65,11 @@ struct GradMaps {
     CUtensorMap q, k, v, d_o;
 };
 
-// 256 threads. Channel-oriented work: thread (d = tid % 128, half = tid / 128)
-// owns key channel d for chunk rows 32 * half .. 32 * half + 31. Row-oriented
-// work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16),
-// column half warp / 4.
-__global__ void __launch_bounds__(256, 1)
+// 512 threads. Channel-oriented work: thread (d = tid % 128, quarter = tid / 128)
+// owns key channel d for chunk rows 16 * quarter .. 16 * quarter + 15. Row-oriented
+// work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16), column
+// quarter warp / 4. Every cross-thread sum is combined in a fixed order.
+__global__ void __launch_bounds__(512, 1)
     k_tc_grads(Prob p, const float* __restrict__ g, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
                bf16* __restrict__ dk_out, bf16* __restrict__ dv_out, float* __restrict__ dg_out,
                bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
@@ -75,6 +77,8 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* sm = align1024(smraw);
     float* sbeta = reinterpret_cast<float*>(sm + GS::BETA);
     const float* segc = reinterpret_cast<const float*>(sm + GS::EGC);
+    float* xtot = reinterpret_cast<float*>(sm + GS::XTOT);
+    float* xrg = reinterpret_cast<float*>(sm + GS::XRG);
     float* xrd = reinterpret_cast<float*>(sm + GS::XRD);
     float* xgc = reinterpret_cast<float*>(sm + GS::XGC);
     float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(256, 1)
     auto S = [&](int off) { return smem_u32(sm + off); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = tid & 127, half = tid >> 7, q4 = warp & 3, wh = warp >> 2;
+    const int d = tid & 127, qtr = tid >> 7, q4 = warp & 3, cq = warp >> 2;
     const int HV = p.HV, H = p.H, G = HV / H, hv = blockIdx.y, h = hv / G;
     const int64_t gc = blockIdx.x, ch = gc * HV + hv;
     int64_t r0;
@@ -123,21 +127,22 @@ __global__ void __launch_bounds__(256, 1)
         bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
         bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
     }
-    // Gamma2 of channel d for this thread's 32 rows (same order of additions as tc_intra)
-    float G2[32];
-    chunk_cumsum_log2(g, r0, c, HV, hv, d, half, xt1, G2);
+    // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
+    float G2[16];
+    quarter_cumsum_log2<1>(g, r0, c, HV, hv, d, qtr, xtot, G2);
     const int rmid = (c - 1) >> 1;
-    if (half == 0) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i == rmid) xgc[d] = G2[i];
+    for (int i = 0; i < 16; ++i) {
+        if (16 * qtr + i == rmid) xrg[d] = G2[i];
+        if (16 * qtr + i == c - 1) xrg[128 + d] = G2[i];
     }
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (32 * half + i == c - 1) xgc[128 + d] = G2[i];
     __syncthreads();
-    const float ref = xgc[d], gC = xgc[128 + d];
+    const float ref = xrg[d], gC = xrg[128 + d];
+    // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
+    // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
+    const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
 
+    float rd = 0.f;
     if (!wait_all(&bars[0], 0, ws.status, 41, fail)) goto cleanup;
     if (tid == 0) {  // phase A
         tc_fence_after();
@@ -154,50 +159,44 @@ __global__ void __launch_bounds__(256, 1)
             mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
         mma_commit(&bars[1]);
     }
-    {  // <S_in[d, v], dS_out[d, v]> over this thread's 64 columns v
-        float rd = 0.f;
 #pragma unroll
-        for (int c8 = 64 * half; c8 < 64 * half + 64; c8 += 8) {
-            const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
-            const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
-            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
+        const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
+        const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
-                rd = fmaf(fa.x, fb.x, rd);
-                rd = fmaf(fa.y, fb.y, rd);
-            }
+        for (int u = 0; u < 4; ++u) {
+            const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
+            rd = fmaf(fa.x, fb.x, rd);
+            rd = fmaf(fa.y, fb.y, rd);
         }
-        xrd[half * 128 + d] = rd;
     }
     if (!wait_all(&bars[1], 0, ws.status, 42, fail)) goto cleanup;
     tc_fence_after();
-    {  // epilogue A: dw row segment (64 columns) and dN row segment (32 columns)
+    xrd[qtr * 128 + d] = rd;  // the dO tile is dead from here on
+    {  // epilogue A: dw row segment (32 columns) and dN row segment (16 columns)
         float x[32];
-        for (int cb = 0; cb < 2; ++cb) {
-            const int col = 64 * wh + 32 * cb;
-            tmem_ld32(tmem + lb + 128 + col, x);
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, col + 8 * u, kC, x + 8 * u);
-        }
-        tmem_ld32(tmem + lb + 256 + 32 * wh, x);
+        tmem_ld32(tmem + lb + 128 + 32 * cq, x);
+        tmem_ld_wait();
+        if (rv)
+            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, 32 * cq + 8 * u, kC, x + 8 * u);
+        tmem_ld16(tmem + lb + 256 + 16 * cq, x);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) x[u] = (32 * wh + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
+        for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
         if (rv)
-            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DN, rrow, 32 * wh + 8 * u, kC, x + 8 * u);
+            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
     }
     tc_fence_before();
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {  // decayed factor tiles, channel d, this thread's rows (rows >= c are zero)
-        const int r = 32 * half + i;
+    for (int i = 0; i < 16; ++i) {  // decayed factor tiles, channel d, this thread's rows (rows >= c are zero)
+        const int r = 16 * qtr + i;
         const bool in = r < c;
         const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
         const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
         const float gm = G2[i];
-        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm);
+        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = ep * e_ref;
         st_tile(sm + GS::KR, r, d, kC, kv * ep);
         st_tile(sm + GS::KC, r, d, kC, kv * em);
         st_tile(sm + GS::QR, r, d, kC, qv * ep);
@@ -231,31 +230,30 @@ __global__ void __launch_bounds__(256, 1)
         const float br = rv ? sbeta[rrow] : 0.f;
         float x[32];
         float db = 0.f;
-        tmem_ld32(tmem + lb + 128 + 32 * wh, x);
+        tmem_ld16(tmem + lb + 128 + 16 * cq, x);
         tmem_ld_wait();
         if (rv) {
 #pragma unroll
-            for (int u = 0; u < 32; ++u) {
-                const int j = 32 * wh + u;
+            for (int u = 0; u < 16; ++u) {
+                const int j = 16 * cq + u;
                 db = fmaf(ld_tile(sm + GS::INV, j, rrow, kC), x[u], db);
                 st_tile(sm + GS::DINV, j, rrow, kC, br * x[u]);
             }
-            xdb[wh * 64 + rrow] = db;
+            xdb[cq * 64 + rrow] = db;
         }
-        bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D;
-        for (int cb = 0; cb < 2; ++cb) {
-            const int col = 64 * wh + 32 * cb;
-            tmem_ld32(tmem + lb + 320 + col, x);
-            tmem_ld_wait();
-            if (rv && rrow < c)
-                for (int u = 0; u < 32; u += 8) {
-                    uint4 vv;
-                    vv.x = pack2(br * x[u], br * x[u + 1]);
-                    vv.y = pack2(br * x[u + 2], br * x[u + 3]);
-                    vv.z = pack2(br * x[u + 4], br * x[u + 5]);
-                    vv.w = pack2(br * x[u + 6], br * x[u + 7]);
-                    *reinterpret_cast<uint4*>(dvrow + col + u) = vv;
-                }
+        tmem_ld32(tmem + lb + 320 + 32 * cq, x);
+        tmem_ld_wait();
+        if (rv && rrow < c) {
+            bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D + 32 * cq;
+#pragma unroll
+            for (int u = 0; u < 32; u += 8) {
+                uint4 vv;
+                vv.x = pack2(br * x[u], br * x[u + 1]);
+                vv.y = pack2(br * x[u + 2], br * x[u + 3]);
+                vv.z = pack2(br * x[u + 4], br * x[u + 5]);
+                vv.w = pack2(br * x[u + 6], br * x[u + 7]);
+                *reinterpret_cast<uint4*>(dvrow + u) = vv;
+            }
         }
     }
     tc_fence_before();
@@ -271,11 +269,11 @@ __global__ void __launch_bounds__(256, 1)
     if (!wait_all(&bars[1], 0, ws.status, 44, fail)) goto cleanup;
     tc_fence_after();
     {
-        float x[32];
-        tmem_ld32(tmem + lb + 128 + 32 * wh, x);
+        float x[16];
+        tmem_ld16(tmem + lb + 128 + 16 * cq, x);
         tmem_ld_wait();
         if (rv)
-            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::TT, rrow, 32 * wh + 8 * u, kC, x + 8 * u);
+            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
     }
     tc_fence_before();
     fence_async_smem();
@@ -291,29 +289,30 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     {  // epilogue D: dbeta (Akk part), dM row segments
         const float br = rv ? sbeta[rrow] : 0.f;
-        float a[32], m[32];
+        float a[16], m[16];
         float db = 0.f;
-        tmem_ld32(tmem + lb + 320 + 32 * wh, a);
-        tmem_ld32(tmem + lb + 192 + 32 * wh, m);
+        tmem_ld16(tmem + lb + 320 + 16 * cq, a);
+        tmem_ld16(tmem + lb + 192 + 16 * cq, m);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 32; ++u) {
-            const int j = 32 * wh + u;
+        for (int u = 0; u < 16; ++u) {
+            const int j = 16 * cq + u;
             const bool in = j < rrow && rrow < c;
             db = in ? fmaf(a[u], m[u], db) : db;
             a[u] = in ? br * a[u] : 0.f;
         }
         if (rv) {
-            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DM, rrow, 32 * wh + 8 * u, kC, a + 8 * u);
-            xdb[128 + wh * 64 + rrow] = db;
+            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DM, rrow, 16 * cq + 8 * u, kC, a + 8 * u);
+            xdb[256 + cq * 64 + rrow] = db;
         }
     }
     tc_fence_before();
     fence_async_smem();
     __syncthreads();
     if (tid < kC && tid < c)
-        db_out[(r0 + tid) * HV + hv] =
-            __float2bfloat16_rn((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid]));
+        db_out[(r0 + tid) * HV + hv] = __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
+                                                           ((xdb[256 + tid] + xdb[320 + tid]) +
+                                                            (xdb[384 + tid] + xdb[448 + tid])));
     if (tid == 0) {  // phase E
         tc_fence_after();
         const uint32_t ik = idesc_bf16(128, 64, true, false), im = idesc_bf16(128, 64, true, true);
@@ -327,29 +326,29 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (!wait_all(&bars[1], 0, ws.status, 46, fail)) goto cleanup;
     tc_fence_after();
-    {  // final epilogue, channel d, rows 32 * half .. +31: dq, dk, dGamma -> dg
-        float dG[32];
+    {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
+        float dG[16];
         float dGC = 0.f;
         const float sc = p.scale;
 #pragma unroll
         for (int rb = 0; rb < 2; ++rb) {
-            const uint32_t cb = (uint32_t)(32 * half + 16 * rb);
-            float aQt[16], aKh[16], aKr[16], aKc[16], aQr[16], aXk[16];
-            tmem_ld16(tmem + lb + 0 + cb, aQt);
-            tmem_ld16(tmem + lb + 64 + cb, aKh);
-            tmem_ld16(tmem + lb + 128 + cb, aKr);
-            tmem_ld16(tmem + lb + 192 + cb, aKc);
-            tmem_ld16(tmem + lb + 256 + cb, aQr);
-            tmem_ld16(tmem + lb + 448 + cb, aXk);
+            const uint32_t cb = (uint32_t)(16 * qtr + 8 * rb);
+            float aQt[8], aKh[8], aKr[8], aKc[8], aQr[8], aXk[8];
+            tmem_ld8(tmem + lb + 0 + cb, aQt);
+            tmem_ld8(tmem + lb + 64 + cb, aKh);
+            tmem_ld8(tmem + lb + 128 + cb, aKr);
+            tmem_ld8(tmem + lb + 192 + cb, aKc);
+            tmem_ld8(tmem + lb + 256 + cb, aQr);
+            tmem_ld8(tmem + lb + 448 + cb, aXk);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int ii = 16 * rb + i, r = 32 * half + ii;
+            for (int i = 0; i < 8; ++i) {
+                const int ii = 8 * rb + i, r = 16 * qtr + ii;
                 const bool in = r < c;
                 const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
                 const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
                 const float gm = G2[ii];
-                const float E = exp2f(gm), ep = exp2f(gm - ref), em = exp2f(ref - gm), eh = exp2f(gC - gm);
+                const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = ep * e_ref, eh = em * e_cr;
                 const float b = sbeta[r];
                 const float dQt = sc * aQt[i], bX = b * aXk[i];
                 const float dqv = dQt * E + aQr[i] * ep;
@@ -374,24 +373,26 @@ __global__ void __launch_bounds__(256, 1)
                 }
             }
         }
-        xgc[half * 128 + d] = dGC;
+        xgc[qtr * 128 + d] = dGC;
         __syncthreads();
-        const float dGCt = segc[d] * (xrd[d] + xrd[128 + d]) + (xgc[d] + xgc[128 + d]);
+        const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
+                           ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (32 * half + i == c - 1) dG[i] += dGCt;
+        for (int i = 0; i < 16; ++i)
+            if (16 * qtr + i == c - 1) dG[i] += dGCt;
         float run = 0.f;
 #pragma unroll
-        for (int i = 31; i >= 0; --i) {
+        for (int i = 15; i >= 0; --i) {
             run += dG[i];
             dG[i] = run;
         }
-        if (half == 1) xt1[d] = run;
+        xt1[qtr * 128 + d] = run;
         __syncthreads();
-        const float carry = half == 0 ? xt1[d] : 0.f;
+        float carry = 0.f;  // later quarters' totals, added in the order 3, 2, 1
+        for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * half + i;
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * qtr + i;
             if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = dG[i] + carry;
         }
     }
@@ -436,7 +437,7 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
         !make_tmap_bf16_3d(&m.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
         !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC))
         return cudaErrorInvalidValue;
-    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 256, kGradsSmem, st>>>(
+    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 512, kGradsSmem, st>>>(
         p, io.g, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
     if (p.HV != p.H) {

@@ -92,6 +92,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// As tmem_ld32 with 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float* v) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 // As tmem_ld32 with 16 consecutive columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
@@ -222,30 +231,41 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* st
     return *(volatile int*)fail == 0;
 }
 
-// In-chunk cumulative sum of g for channel d over rows [32 * half, 32 * half + 32)
-// in log2 units (rows >= c add nothing), split over two threads per channel:
-// half 0 sums rows 0..31, half 1 adds half 0's total. `tot` is 128 floats of
-// shared scratch. Every caller uses this exact order of additions, so the
-// decay factors recomputed in the gradient kernel match the ones used here.
-__device__ __forceinline__ void chunk_cumsum_log2(const float* __restrict__ g, int64_t r0, int c, int HV, int hv,
-                                                  int d, int half, float* tot, float (&G2)[32]) {
-    float gv[32];
+// In-chunk cumulative sum of g for key channel d in log2 units, in one
+// canonical order that every kernel reproduces exactly whatever its thread
+// layout: rows are split in four quarters of 16; for row r of quarter q,
+//   G2(r) = (off_q + run_q(r)) * log2(e),  run_q(r) = sum of g over rows 16q..r
+// (in row order), off_0 = 0, off_q = off_{q-1} + T_{q-1}, T_q = run_q(15).
+// Rows >= c add nothing. The calling thread owns quarters q0 .. q0+NQ-1;
+// `tot` is 4 x 128 floats of shared scratch. Contains a __syncthreads().
+template <int NQ>
+__device__ __forceinline__ void quarter_cumsum_log2(const float* __restrict__ g, int64_t r0, int c, int HV, int hv,
+                                                    int d, int q0, float* tot, float (&G2)[16 * NQ]) {
+    float run[16 * NQ];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = 32 * half + i;
-        gv[i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
-    }
-    float acc = 0.f;
+    for (int qi = 0; qi < NQ; ++qi) {
+        float gv[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        acc += gv[i];
-        G2[i] = acc;
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * (q0 + qi) + i;
+            gv[i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            acc += gv[i];
+            run[16 * qi + i] = acc;
+        }
+        tot[(q0 + qi) * 128 + d] = acc;
     }
-    if (half == 0) tot[d] = acc;
     __syncthreads();
-    const float off = half ? tot[d] : 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) G2[i] = (G2[i] + off) * 1.4426950408889634f;
+    for (int qi = 0; qi < NQ; ++qi) {
+        float off = 0.f;
+        for (int qq = 0; qq < q0 + qi; ++qq) off += tot[qq * 128 + d];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) G2[16 * qi + i] = (off + run[16 * qi + i]) * 1.4426950408889634f;
+    }
 }
 
 }  // namespace tc
