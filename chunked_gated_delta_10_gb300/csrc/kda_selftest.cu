@@ -42,6 +42,15 @@ __global__ void __launch_bounds__(128) k_umma_selftest(int M, int N, int Kd, int
     tc_fence_after();
     const uint32_t tmem = *tslot;
     bool ok = true;
+    if (mode & 8) {
+        // bounded-wait check: wait on a barrier phase that nothing completes, with a
+        // short limit; the wait must give up, record status 7 and let the kernel finish.
+        if (tid == 0) mbar_wait(&bars[0], 0, status, 7, 2000000LL);
+        __syncthreads();
+        tc_fence_before();
+        if (warp == 0) tmem_dealloc(tmem, ncols);
+        return;
+    }
     if (tid == 0) {
         if (a_tma) {
             mbar_expect_tx(&bars[0], (uint32_t)(Ar * Ac * 2));
@@ -81,7 +90,7 @@ extern "C" kda_status kda_selftest_umma(int32_t M, int32_t N, int32_t Kd, int32_
                                         float* raw, int* status, kda_stream_t stream) {
     using namespace kda;
     if (!(M == 64 || M == 128) || !(N == 64 || N == 128 || N == 256) || !(Kd == 64 || Kd == 128) || mode < 0 ||
-        mode > 7 || !A || !B || !raw || !status)
+        mode > 15 || !A || !B || !raw || !status)
         return KDA_ERR_INVALID_ARG;
     CUtensorMap tm;
     memset(&tm, 0, sizeof(tm));

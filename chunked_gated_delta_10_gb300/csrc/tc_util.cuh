@@ -46,13 +46,14 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
         : "memory");
     return done != 0;
 }
-// Wait for phase `parity` of `bar` to complete, for at most kWaitCycles.
+// Wait for phase `parity` of `bar` to complete, for at most `limit` SM cycles.
 // On time-out, writes `code` to *status (if non-null) and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status, int code,
+                                         long long limit = kWaitCycles) {
     if (mbar_try(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             if (status) *(volatile int*)status = code;
             return false;
         }

@@ -25,6 +25,9 @@ extern "C" {
  *             set:    A is given as Kd x M row-major (used MN-major).
  *   mode bit 1: the same for B (N x Kd, or Kd x N).
  *   mode bit 2: load A with a TMA tiled load (only with bit 0 clear).
+ *   mode bit 3: instead of the MMA, check the bounded device wait: the kernel
+ *             waits on an mbarrier phase that nothing completes, gives up after
+ *             about a millisecond, writes 7 to *status and exits normally.
  * A, B: bf16 device arrays. M in {64, 128}; N in {64, 128, 256}; Kd in {64, 128}.
  * status: device int, set nonzero if a bounded wait gave up (caller zeroes it).
  * Errors: KDA_ERR_INVALID_ARG for other sizes / null pointers; KDA_ERR_CUDA.

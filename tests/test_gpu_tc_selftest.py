@@ -58,3 +58,19 @@ def test_m64_lane_layout(lib, N, Kd, mode):
     alt = np.abs(raw[:64] - ref).max() / np.abs(ref).max()
     print(f"M=64 N={N} Kd={Kd} mode={mode}: quarter-lane layout err {err:.2e}, lanes 0..63 err {alt:.2e}")
     assert err < 1e-5
+
+
+def test_bounded_wait_reports_timeout_and_context_stays_usable(lib):
+    """A device wait on a barrier that nothing completes gives up, records a
+    status code the host reads, and leaves the CUDA context usable."""
+    A = torch.zeros(128, 64, dtype=torch.bfloat16, device="cuda")
+    B = torch.zeros(64, 64, dtype=torch.bfloat16, device="cuda")
+    raw = torch.zeros(128, 64, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.kda_selftest_umma(128, 64, 64, 8, A.data_ptr(), B.data_ptr(), raw.data_ptr(), status.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(status.item()) == 7
+    got, ref = _run(lib, 128, 64, 64, 0)  # the next launch on the same context works
+    assert np.abs(got - ref).max() / np.abs(ref).max() < 1e-5
