@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             tma_load_3d(sm + IS::V + b * (TCD / 2), &maps.v, 64 * b, hv, (int)r0, &bars[0]);
         }
     }
+    const ColAddr a64(d, kC), a128(d, 128);  // this thread's column in the 64- and 128-row tiles
     float G2[32];
     quarter_cumsum_log2<2>(g, r0, c, HV, hv, d, 2 * half, tmp, G2);
     // reference row (middle of the chunk, always in rows 0..31) and last valid row
@@ -203,18 +204,18 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     for (int i = 0; i < 32; ++i) {
         const int r = 32 * half + i;
         const bool in = r < c;
-        const float kv = in ? ld_tile(sm + IS::K, r, d, kC) : 0.f;
-        const float qv = in ? ld_tile(sm + IS::Q, r, d, kC) : 0.f;
-        const float vv = in ? ld_tile(sm + IS::V, r, d, kC) : 0.f;
+        const float kv = in ? ld_col(sm + IS::K, a64, r) : 0.f;
+        const float qv = in ? ld_col(sm + IS::Q, a64, r) : 0.f;
+        const float vv = in ? ld_col(sm + IS::V, a64, r) : 0.f;
         const float b = sb[r], gm = G2[i];
-        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = exp2f(gm), eh = exp2f(gC - gm);
-        st_tile(sm + IS::KQ, r, d, 128, kv * ep);
-        st_tile(sm + IS::KQ, kC + r, d, 128, qv * ep);
-        st_tile(sm + IS::KC, r, d, kC, kv * em);
-        st_tile(sm + IS::XK, r, d, kC, b * kv * E);
-        st_tile(sm + IS::V, r, d, kC, b * vv);
-        st_tile(sm + IS::K, r, d, kC, kv * eh);
-        st_tile(sm + IS::Q, r, d, kC, p.scale * qv * E);
+        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = fast_exp2(gm), eh = fast_exp2(gC - gm);
+        st_col(sm + IS::KQ, a128, r, kv * ep);
+        st_col(sm + IS::KQ, a128, kC + r, qv * ep);
+        st_col(sm + IS::KC, a64, r, kv * em);
+        st_col(sm + IS::XK, a64, r, b * kv * E);
+        st_col(sm + IS::V, a64, r, b * vv);
+        st_col(sm + IS::K, a64, r, kv * eh);
+        st_col(sm + IS::Q, a64, r, p.scale * qv * E);
     }
     fence_async_smem();
     tc_fence_before();
@@ -285,10 +286,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         float col[32];
         tmem_ld32(tmem + lb + 64 + c0, col);
         tmem_ld_wait();
-        for (int j = 0; j < 32; ++j) st_tile(sm + IS::WST, c0 + j, dd, kC, col[j]);
+        const ColAddr ad(dd, kC);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_col(sm + IS::WST, ad, c0 + j, col[j]);
         tmem_ld32(tmem + lb + 128 + c0, col);
         tmem_ld_wait();
-        for (int j = 0; j < 32; ++j) st_tile(sm + IS::UST, c0 + j, dd, kC, col[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_col(sm + IS::UST, ad, c0 + j, col[j]);
     }
     tc_fence_before();
     fence_async_smem();
@@ -397,7 +401,9 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
                 const int vv = 16 * warp + lane;
                 const uint8_t* tU = b + FwdBuf::U;
 #pragma unroll
-                for (int r = 0; r < kC; ++r) st_tile(tDl, r, vv, kC, ld_tile(tU, r, vv, kC) - acc[r]);
+                const ColAddr av(vv, kC);
+#pragma unroll
+                for (int r = 0; r < kC; ++r) st_col(tDl, av, r, ld_col(tU, av, r) - acc[r]);
             }
         }
         tc_fence_before();
@@ -536,7 +542,9 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
             if (lane < 16) {
                 const int vv = 16 * warp + lane;
 #pragma unroll
-                for (int r = 0; r < kC; ++r) st_tile(tDd, r, vv, kC, acc[r]);
+                const ColAddr av(vv, kC);
+#pragma unroll
+                for (int r = 0; r < kC; ++r) st_col(tDd, av, r, acc[r]);
             }
         }
         tc_fence_before();

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(512, 1)
         bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
         bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
     }
+    const ColAddr ad(d, kC);  // this thread's column in the 64-row tiles
     // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
     float G2[16];
     quarter_cumsum_log2<1>(g, r0, c, HV, hv, d, qtr, xtot, G2);
@@ -193,14 +194,14 @@ __global__ void __launch_bounds__(512, 1)
     for (int i = 0; i < 16; ++i) {  // decayed factor tiles, channel d, this thread's rows (rows >= c are zero)
         const int r = 16 * qtr + i;
         const bool in = r < c;
-        const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
-        const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
+        const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
+        const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
         const float gm = G2[i];
-        const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = ep * e_ref;
-        st_tile(sm + GS::KR, r, d, kC, kv * ep);
-        st_tile(sm + GS::KC, r, d, kC, kv * em);
-        st_tile(sm + GS::QR, r, d, kC, qv * ep);
-        st_tile(sm + GS::KT, r, d, kC, kv * E);
+        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
+        st_col(sm + GS::KR, ad, r, kv * ep);
+        st_col(sm + GS::KC, ad, r, kv * em);
+        st_col(sm + GS::QR, ad, r, qv * ep);
+        st_col(sm + GS::KT, ad, r, kv * E);
     }
     fence_async_smem();
     __syncthreads();
@@ -234,10 +235,12 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld_wait();
         if (rv) {
 #pragma unroll
+            const ColAddr ar(rrow, kC);
+#pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int j = 16 * cq + u;
-                db = fmaf(ld_tile(sm + GS::INV, j, rrow, kC), x[u], db);
-                st_tile(sm + GS::DINV, j, rrow, kC, br * x[u]);
+                db = fmaf(ld_col(sm + GS::INV, ar, j), x[u], db);
+                st_col(sm + GS::DINV, ar, j, br * x[u]);
             }
             xdb[cq * 64 + rrow] = db;
         }
@@ -345,10 +348,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int i = 0; i < 8; ++i) {
                 const int ii = 8 * rb + i, r = 16 * qtr + ii;
                 const bool in = r < c;
-                const float kv = in ? ld_tile(sm + GS::K, r, d, kC) : 0.f;
-                const float qv = in ? ld_tile(sm + GS::Q, r, d, kC) : 0.f;
+                const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
+                const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
                 const float gm = G2[ii];
-                const float ep = exp2f(gm - ref), em = exp2f(ref - gm), E = ep * e_ref, eh = em * e_cr;
+                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
                 const float b = sbeta[r];
                 const float dQt = sc * aQt[i], bX = b * aXk[i];
                 const float dqv = dQt * E + aQr[i] * ep;

@@ -232,6 +232,31 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* st
     return *(volatile int*)fail == 0;
 }
 
+// Column addressing of a bf16 operand tile: for a fixed column c, the byte offset
+// of element (r, c) is o[r % 8] + 128 r (the swizzle only permutes the 16-byte
+// chunks of a row, by r % 8). Inside fully unrolled row loops every access is
+// then a single shared-memory load or store with an immediate offset.
+struct ColAddr {
+    uint32_t o[8];
+    __device__ __forceinline__ ColAddr(int c, int R) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) o[k] = (uint32_t)((c >> 6) * R * 128 + (((c & 63) * 2) ^ (k << 4)));
+    }
+    __device__ __forceinline__ uint32_t at(int r) const { return o[r & 7] + (uint32_t)(r * 128); }
+};
+__device__ __forceinline__ float ld_col(const uint8_t* tile, const ColAddr& a, int r) {
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + a.at(r)));
+}
+__device__ __forceinline__ void st_col(uint8_t* tile, const ColAddr& a, int r, float x) {
+    *reinterpret_cast<__nv_bfloat16*>(tile + a.at(r)) = __float2bfloat16_rn(x);
+}
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // In-chunk cumulative sum of g for key channel d in log2 units, in one
 // canonical order that every kernel reproduces exactly whatever its thread
 // layout: rows are split in four quarters of 16; for row r of quarter q,
