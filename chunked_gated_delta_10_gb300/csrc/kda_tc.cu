@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     int64_t r0;
     int c;
     chunk_rows(p, gc, r0, c);
+    float G2[32];  // g of channel d, this thread's 32 rows; Gamma2 after the cumsum below
+    load_g_quarters<2>(g, r0, c, HV, hv, d, 2 * half, G2);
     if (tid == 0) {
         *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
         if (*fail) *(volatile int*)ws.status = 10;
@@ -183,8 +185,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         }
     }
     const ColAddr a64(d, kC), a128(d, 128);  // this thread's column in the 64- and 128-row tiles
-    float G2[32];
-    quarter_cumsum_log2<2>(g, r0, c, HV, hv, d, 2 * half, tmp, G2);
+    quarter_cumsum_log2<2>(G2, d, 2 * half, tmp, G2);
     // reference row (middle of the chunk, always in rows 0..31) and last valid row
     const int rmid = (c - 1) >> 1;
     if (half == 0) {
@@ -209,12 +210,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         const float vv = in ? ld_col(sm + IS::V, a64, r) : 0.f;
         const float b = sb[r], gm = G2[i];
         const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = fast_exp2(gm), eh = fast_exp2(gC - gm);
-        st_col(sm + IS::KQ, a128, r, kv * ep);
-        st_col(sm + IS::KQ, a128, kC + r, qv * ep);
-        st_col(sm + IS::KC, a64, r, kv * em);
-        st_col(sm + IS::XK, a64, r, b * kv * E);
-        st_col(sm + IS::V, a64, r, b * vv);
-        st_col(sm + IS::K, a64, r, kv * eh);
+        const uint32_t o = a64.at(r);
+        st_bf16_pair(sm + IS::KQ + a128.at(r), sm + IS::KQ + a128.at(kC + r), kv * ep, qv * ep);
+        st_bf16_pair(sm + IS::KC + o, sm + IS::XK + o, kv * em, b * kv * E);
+        st_bf16_pair(sm + IS::V + o, sm + IS::K + o, b * vv, kv * eh);
         st_col(sm + IS::Q, a64, r, p.scale * qv * E);
     }
     fence_async_smem();
@@ -288,11 +287,11 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         tmem_ld_wait();
         const ColAddr ad(dd, kC);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) st_col(sm + IS::WST, ad, c0 + j, col[j]);
+        for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::WST, ad, c0 + j, col[j], col[j + 1]);
         tmem_ld32(tmem + lb + 128 + c0, col);
         tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) st_col(sm + IS::UST, ad, c0 + j, col[j]);
+        for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::UST, ad, c0 + j, col[j], col[j + 1]);
     }
     tc_fence_before();
     fence_async_smem();
@@ -400,10 +399,10 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
             if (lane < 16) {
                 const int vv = 16 * warp + lane;
                 const uint8_t* tU = b + FwdBuf::U;
-#pragma unroll
                 const ColAddr av(vv, kC);
 #pragma unroll
-                for (int r = 0; r < kC; ++r) st_col(tDl, av, r, ld_col(tU, av, r) - acc[r]);
+                for (int r = 0; r < kC; r += 2)
+                    st_col_pair(tDl, av, r, ld_col(tU, av, r) - acc[r], ld_col(tU, av, r + 1) - acc[r + 1]);
             }
         }
         tc_fence_before();
@@ -541,10 +540,9 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
             tmem_ld_wait();
             if (lane < 16) {
                 const int vv = 16 * warp + lane;
-#pragma unroll
                 const ColAddr av(vv, kC);
 #pragma unroll
-                for (int r = 0; r < kC; ++r) st_col(tDd, av, r, acc[r]);
+                for (int r = 0; r < kC; r += 2) st_col_pair(tDd, av, r, acc[r], acc[r + 1]);
             }
         }
         tc_fence_before();
@@ -608,7 +606,7 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if (rows > 0 && !make_tmap_bf16_3d(&tm_do, io.d_o, D, (uint64_t)p.HV, (uint64_t)rows, (uint64_t)D * 2,
                                        (uint64_t)p.HV * D * 2, 64, 1, kC))
         return cudaErrorInvalidValue;
-    const bf16 *q = (const bf16*)io.q, *k = (const bf16*)io.k, *v = (const bf16*)io.v, *beta = (const bf16*)io.beta;
+    const bf16* beta = (const bf16*)io.beta;
     if (p.NT > 0 && stages >= 1) {
         IntraMaps im;
         memset(&im, 0, sizeof(im));

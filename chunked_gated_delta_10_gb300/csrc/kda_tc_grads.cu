@@ -59,8 +59,6 @@ struct GS {
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
-__device__ __forceinline__ float bfr(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
 struct GradMaps {
     CUtensorMap q, k, v, d_o;
 };
@@ -95,23 +93,14 @@ __global__ void __launch_bounds__(512, 1)
     int64_t r0;
     int c;
     chunk_rows(p, gc, r0, c);
+    float G2[16];  // g of channel d, this thread's 16 rows; Gamma2 after the cumsum below
+    load_g_quarters<1>(g, r0, c, HV, hv, d, qtr, G2);
 
-    if (tid == 0) {
+    if (tid == 0) {  // all input copies start right after the g loads
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
         fence_mbar_init();
         *fail = 0;
-    }
-    if (warp == 0) tmem_alloc(tslot, 512);
-    if (tid < kC) sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
-    const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
-    const bool rv = lane < 16;
-    if (tid == 0) {
         mbar_expect_tx(&bars[0], 6 * TCD + 2 * TDD + TCC + 512);
         const int row = (int)r0;
         for (int b = 0; b < 2; ++b) {
@@ -127,17 +116,27 @@ __global__ void __launch_bounds__(512, 1)
         bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
         bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
     }
+    if (warp == 0) tmem_alloc(tslot, 512);
+    if (tid < kC) sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     const ColAddr ad(d, kC);  // this thread's column in the 64-row tiles
     // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
-    float G2[16];
-    quarter_cumsum_log2<1>(g, r0, c, HV, hv, d, qtr, xtot, G2);
+    quarter_cumsum_log2<1>(G2, d, qtr, xtot, G2);
     const int rmid = (c - 1) >> 1;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         if (16 * qtr + i == rmid) xrg[d] = G2[i];
         if (16 * qtr + i == c - 1) xrg[128 + d] = G2[i];
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
+    const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
+    const bool rv = lane < 16;
     const float ref = xrg[d], gC = xrg[128 + d];
     // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
     // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
@@ -198,10 +197,9 @@ __global__ void __launch_bounds__(512, 1)
         const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
         const float gm = G2[i];
         const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
-        st_col(sm + GS::KR, ad, r, kv * ep);
-        st_col(sm + GS::KC, ad, r, kv * em);
-        st_col(sm + GS::QR, ad, r, qv * ep);
-        st_col(sm + GS::KT, ad, r, kv * E);
+        const uint32_t o = ad.at(r);
+        st_bf16_pair(sm + GS::KR + o, sm + GS::KC + o, kv * ep, kv * em);
+        st_bf16_pair(sm + GS::QR + o, sm + GS::KT + o, qv * ep, kv * E);
     }
     fence_async_smem();
     __syncthreads();
@@ -234,14 +232,11 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld16(tmem + lb + 128 + 16 * cq, x);
         tmem_ld_wait();
         if (rv) {
-#pragma unroll
             const ColAddr ar(rrow, kC);
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = 16 * cq + u;
-                db = fmaf(ld_col(sm + GS::INV, ar, j), x[u], db);
-                st_col(sm + GS::DINV, ar, j, br * x[u]);
-            }
+            for (int u = 0; u < 16; ++u) db = fmaf(ld_col(sm + GS::INV, ar, 16 * cq + u), x[u], db);
+#pragma unroll
+            for (int u = 0; u < 16; u += 2) st_col_pair(sm + GS::DINV, ar, 16 * cq + u, br * x[u], br * x[u + 1]);
             xdb[cq * 64 + rrow] = db;
         }
         tmem_ld32(tmem + lb + 320 + 32 * cq, x);
@@ -350,6 +345,9 @@ __global__ void __launch_bounds__(512, 1)
                 const bool in = r < c;
                 const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
                 const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
+                // the bf16 factor values the MMAs used (zero on rows >= c)
+                const float kt_b = ld_col(sm + GS::KT, ad, r), qr_b = ld_col(sm + GS::QR, ad, r);
+                const float kr_b = ld_col(sm + GS::KR, ad, r), kc_b = ld_col(sm + GS::KC, ad, r);
                 const float gm = G2[ii];
                 const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
                 const float b = sbeta[r];
@@ -359,15 +357,14 @@ __global__ void __launch_bounds__(512, 1)
                 const float khk = aKh[i] * kv * eh;
                 // The factor values of the dGamma pair terms are the bf16 values the MMAs used, so that each
                 // in-chunk pair's contributions to its two rows cancel in the chunk sum as they do exactly.
-                const float kt_b = bfr(kv * E), qr_b = bfr(qv * ep), kr_b = bfr(kv * ep), kc_b = bfr(kv * em);
                 const float dgv = dQt * qv * E - khk + bX * kt_b + aQr[i] * qr_b + aKr[i] * kr_b - aKc[i] * kc_b;
                 dG[ii] = in ? dgv : 0.f;
                 if (in) {
                     dGC += khk;
                     if (G == 1) {
                         const int64_t o = ((r0 + r) * H + h) * D + d;
-                        dq_out[o] = __float2bfloat16_rn(dqv);
-                        dk_out[o] = __float2bfloat16_rn(dkv);
+                        st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o), reinterpret_cast<uint8_t*>(dk_out + o),
+                                     dqv, dkv);
                     } else {
                         const int64_t o = ((r0 + r) * HV + hv) * D + d;
                         ws.dqp[o] = dqv;

@@ -250,6 +250,16 @@ __device__ __forceinline__ float ld_col(const uint8_t* tile, const ColAddr& a, i
 __device__ __forceinline__ void st_col(uint8_t* tile, const ColAddr& a, int r, float x) {
     *reinterpret_cast<__nv_bfloat16*>(tile + a.at(r)) = __float2bfloat16_rn(x);
 }
+// Two values rounded to bf16 by one packed conversion, stored as 16-bit halves at two addresses.
+__device__ __forceinline__ void st_bf16_pair(uint8_t* pa, uint8_t* pb, float a, float b) {
+    const uint32_t v = pack2(a, b);
+    *reinterpret_cast<uint16_t*>(pa) = (uint16_t)(v & 0xffffu);
+    *reinterpret_cast<uint16_t*>(pb) = (uint16_t)(v >> 16);
+}
+// Rows r and r + 1 of the column a of a tile, one packed conversion.
+__device__ __forceinline__ void st_col_pair(uint8_t* tile, const ColAddr& a, int r, float x0, float x1) {
+    st_bf16_pair(tile + a.at(r), tile + a.at(r + 1), x0, x1);
+}
 // 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -262,24 +272,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // layout: rows are split in four quarters of 16; for row r of quarter q,
 //   G2(r) = (off_q + run_q(r)) * log2(e),  run_q(r) = sum of g over rows 16q..r
 // (in row order), off_0 = 0, off_q = off_{q-1} + T_{q-1}, T_q = run_q(15).
-// Rows >= c add nothing. The calling thread owns quarters q0 .. q0+NQ-1;
-// `tot` is 4 x 128 floats of shared scratch. Contains a __syncthreads().
+// Rows >= c add nothing. The calling thread owns quarters q0 .. q0+NQ-1:
+// load_g_quarters fetches its g values (issued early, ahead of other
+// copies, since the cumsum heads each kernel's critical path) and
+// quarter_cumsum_log2 forms G2; `tot` is 4 x 128 floats of shared scratch.
+// quarter_cumsum_log2 contains a __syncthreads().
 template <int NQ>
-__device__ __forceinline__ void quarter_cumsum_log2(const float* __restrict__ g, int64_t r0, int c, int HV, int hv,
-                                                    int d, int q0, float* tot, float (&G2)[16 * NQ]) {
-    float run[16 * NQ];
+__device__ __forceinline__ void load_g_quarters(const float* __restrict__ g, int64_t r0, int c, int HV, int hv, int d,
+                                                int q0, float (&gv)[16 * NQ]) {
 #pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) {
-        float gv[16];
+    for (int qi = 0; qi < NQ; ++qi)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = 16 * (q0 + qi) + i;
-            gv[i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
+            gv[16 * qi + i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
         }
+}
+template <int NQ>
+__device__ __forceinline__ void quarter_cumsum_log2(const float (&gv)[16 * NQ], int d, int q0, float* tot,
+                                                    float (&G2)[16 * NQ]) {
+    float run[16 * NQ];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
         float acc = 0.f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            acc += gv[i];
+            acc += gv[16 * qi + i];
             run[16 * qi + i] = acc;
         }
         tot[(q0 + qi) * 128 + d] = acc;
