@@ -13,11 +13,11 @@
 //                 then w^T = (beta K~)^T INV^T and u^T = (beta V)^T INV^T.
 //                 Writes w, u, K^, scale*Q~, Aqk, INV and e^(Gamma_C).
 //   tc_state_fwd  per (sequence, value head, 64-column half of V): the chunk
-//                 loop delta^T = u^T - S^T w^T, S <- e^(Gamma_C) S + K^^T delta
+//                 loop delta = u - w S, S <- e^(Gamma_C) S + K^^T delta
 //                 with S in registers (fp32) and a bf16 copy in shared memory;
 //                 writes S_in and delta of every chunk.
 //   tc_ds_rev     per (sequence, value head, V half), chunks in reverse:
-//                 dDelta^T = dO^T Aqk + dS^T K^^T,
+//                 dDelta = Aqk^T dO + K^ dS,
 //                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
 //                 dDelta and dh0.
 //
@@ -380,9 +380,9 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 64, true, false);
+            const uint32_t id = idesc_bf16(64, 64, false, true);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_mnmajor(smem_u32(tS), D, ks), desc_kmajor(smem_u32(b + FwdBuf::W), kC, ks), id,
+                mma_bf16(tmem, desc_kmajor(smem_u32(b + FwdBuf::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
                          ks > 0);
             mma_commit(&bars[2]);
             bulk_store(ws.sin + ch * TDD + z * (TDD / 2), tS, TDD / 2);
@@ -391,18 +391,21 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
         if (!wait_all(&bars[2], mph, ws.status, 22, fail)) break;
         mph ^= 1;
         tc_fence_after();
-        {  // delta^T rows: M = 64 layout, row v = 16 * warp + lane for lane < 16
-            float acc[kC];
+        {  // delta rows: M = 64 layout, chunk row r = 16 * warp + lane for lane < 16
+            float acc[HALF];
             tmem_ld32(tmem + lane_base, acc);
             tmem_ld32(tmem + lane_base + 32, acc + 32);
             tmem_ld_wait();
             if (lane < 16) {
-                const int vv = 16 * warp + lane;
-                const uint8_t* tU = b + FwdBuf::U;
-                const ColAddr av(vv, kC);
+                const int r = 16 * warp + lane;
 #pragma unroll
-                for (int r = 0; r < kC; r += 2)
-                    st_col_pair(tDl, av, r, ld_col(tU, av, r) - acc[r], ld_col(tU, av, r + 1) - acc[r + 1]);
+                for (int c8 = 0; c8 < HALF; c8 += 8) {
+                    float x[8];
+                    ld_tile_row8(b + FwdBuf::U, r, c8, kC, x);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
+                    st_tile_row8(tDl, r, c8, kC, x);
+                }
             }
         }
         tc_fence_before();
@@ -448,7 +451,9 @@ __global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __
 
 // ---------------------------------------------------------------------------
 // tc_ds_rev: one CTA per (sequence, value head, V half), chunks in reverse;
-// thread t owns dS row t (64 fp32 columns). Single-buffered chunk inputs.
+// thread t owns dS row t (64 fp32 columns). Single-buffered chunk inputs in two
+// groups: K^, Q~s, Aqk and dO (first MMA group) are refetched for the next
+// chunk as soon as that group completes, w and e^Gamma_C at the end of the step.
 // ---------------------------------------------------------------------------
 struct RevBuf {
     static constexpr int KH = 0, W = TCD, QS = 2 * TCD, AQK = 3 * TCD, DO = 3 * TCD + TCC, EGC = 3 * TCD + TCC + 8192,
@@ -463,8 +468,8 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
     uint8_t* b = sm;
     uint8_t* tS = sm + RevBuf::BYTES;        // bf16 dS, 128 x 64
     uint8_t* tDd = tS + D * HALF * 2;        // bf16 dDelta, 64 x 64
-    uint64_t* bars = reinterpret_cast<uint64_t*>(tDd + kC * HALF * 2);  // full, mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tDd + kC * HALF * 2);  // full (group 1), mma, full (group 2)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -476,6 +481,7 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
+        mbar_init(&bars[2], 1);
         fence_mbar_init();
         *fail = 0;
     }
@@ -486,40 +492,46 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
 #pragma unroll
         for (int j = 0; j < HALF; ++j) S[j] = src ? src[j] : 0.f;
     }
-    auto issue = [&](int it) {
+    auto issue1 = [&](int it) {  // operands of the first MMA group
         const int64_t ch = (c0 + it) * HV + hv;
-        mbar_expect_tx(&bars[0], 3 * TCD + TCC + 8192 + 512);
+        mbar_expect_tx(&bars[0], 2 * TCD + TCC + 8192);
         bulk_load(b + RevBuf::KH, ws.kh + ch * TCD, TCD, &bars[0]);
-        bulk_load(b + RevBuf::W, ws.w + ch * TCD, TCD, &bars[0]);
         bulk_load(b + RevBuf::QS, ws.qs + ch * TCD, TCD, &bars[0]);
         bulk_load(b + RevBuf::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
-        bulk_load(b + RevBuf::EGC, ws.egc + ch * D, 512, &bars[0]);
         tma_load_3d(b + RevBuf::DO, &tm_do, v0, hv, (int)(bos + (int64_t)it * kC), &bars[0]);
+    };
+    auto issue2 = [&](int it) {  // w (second MMA group) and e^Gamma_C (state update)
+        const int64_t ch = (c0 + it) * HV + hv;
+        mbar_expect_tx(&bars[2], TCD + 512);
+        bulk_load(b + RevBuf::W, ws.w + ch * TCD, TCD, &bars[2]);
+        bulk_load(b + RevBuf::EGC, ws.egc + ch * D, 512, &bars[2]);
     };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    if (tid == 0 && nts > 0) issue(nts - 1);
+    if (tid == 0 && nts > 0) {
+        issue1(nts - 1);
+        issue2(nts - 1);
+    }
     uint32_t fph = 0, mph = 0;
     for (int it = nts - 1; it >= 0; --it) {
         const int64_t ch = (c0 + it) * HV + hv;
         if (!wait_all(&bars[0], fph, ws.status, 31, fail)) break;
-        fph ^= 1;
 #pragma unroll
         for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tS, tid, c8, D, S + c8);
         fence_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            // dDelta^T = dO^T Aqk + dS^T K^^T (M = 64)
-            const uint32_t ida = idesc_bf16(64, 64, true, true), idb = idesc_bf16(64, 64, true, false);
+            // dDelta = Aqk^T dO + K^ dS (M = 64: chunk rows)
+            const uint32_t ida = idesc_bf16(64, 64, true, true), idb = idesc_bf16(64, 64, false, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem, desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks),
-                         desc_mnmajor(smem_u32(b + RevBuf::AQK), kC, ks), ida, ks > 0);
+                mma_bf16(tmem, desc_mnmajor(smem_u32(b + RevBuf::AQK), kC, ks),
+                         desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks), ida, ks > 0);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_mnmajor(smem_u32(tS), D, ks), desc_kmajor(smem_u32(b + RevBuf::KH), kC, ks), idb,
+                mma_bf16(tmem, desc_kmajor(smem_u32(b + RevBuf::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
                          1);
             // dS_acc = Q~s^T dO (M = 128)
             const uint32_t idc = idesc_bf16(128, 64, true, true);
@@ -533,21 +545,22 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
         if (!wait_all(&bars[1], mph, ws.status, 32, fail)) break;
         mph ^= 1;
         tc_fence_after();
+        if (tid == 0 && it > 0) issue1(it - 1);  // the first group's operands are consumed
         {
             float acc[kC];
             tmem_ld32(tmem + lane_base, acc);
             tmem_ld32(tmem + lane_base + 32, acc + 32);
             tmem_ld_wait();
-            if (lane < 16) {
-                const int vv = 16 * warp + lane;
-                const ColAddr av(vv, kC);
+            if (lane < 16) {  // chunk row r = 16 * warp + lane
+                const int r = 16 * warp + lane;
 #pragma unroll
-                for (int r = 0; r < kC; r += 2) st_col_pair(tDd, av, r, acc[r], acc[r + 1]);
+                for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tDd, r, c8, kC, acc + c8);
             }
         }
         tc_fence_before();
         fence_async_smem();
-        __syncthreads();
+        if (!wait_all(&bars[2], fph, ws.status, 34, fail)) break;  // its barrier also publishes dDelta
+        fph ^= 1;
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id = idesc_neg_a(idesc_bf16(128, 64, true, true));
@@ -573,7 +586,7 @@ __global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __res
         tc_fence_before();
         if (tid == 0) bulk_wait_read();
         __syncthreads();
-        if (tid == 0 && it > 0) issue(it - 1);
+        if (tid == 0 && it > 0) issue2(it - 1);
     }
     if (dh0 && *(volatile int*)fail == 0) {
         float* dst = dh0 + (((int64_t)n * HV + hv) * D + tid) * D + v0;

@@ -211,6 +211,18 @@ __device__ __forceinline__ void st_tile_row8(uint8_t* tile, int r, int c0, int R
     *reinterpret_cast<uint4*>(tile + tile_off(r, c0, R)) = v;
 }
 
+// Row r, columns c0 .. c0+7 of a bf16 tile with R rows, as one 16-byte load.
+__device__ __forceinline__ void ld_tile_row8(const uint8_t* tile, int r, int c0, int R, float* x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + tile_off(r, c0, R));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
 // Bulk copy shared -> global (16-byte aligned, size % 16 == 0) and its group ops.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
