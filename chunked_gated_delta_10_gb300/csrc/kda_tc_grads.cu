@@ -189,32 +189,45 @@ __global__ void __launch_bounds__(512, 1)
             for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
     }
     tc_fence_before();
+    // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
+    // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero)
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {  // decayed factor tiles, channel d, this thread's rows (rows >= c are zero)
-        const int r = 16 * qtr + i;
-        const bool in = r < c;
-        const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
-        const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
-        const float gm = G2[i];
-        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
-        const uint32_t o = ad.at(r);
-        st_bf16_pair(sm + GS::KR + o, sm + GS::KC + o, kv * ep, kv * em);
-        st_bf16_pair(sm + GS::QR + o, sm + GS::KT + o, qv * ep, kv * E);
+    for (int h8 = 0; h8 < 2; ++h8) {
+        float kr[8], kc[8], qr[8], kt[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 16 * qtr + 8 * h8 + i;
+            const bool in = r < c;
+            const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
+            const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
+            const float gm = G2[8 * h8 + i];
+            const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
+            kr[i] = kv * ep;
+            kc[i] = kv * em;
+            qr[i] = qv * ep;
+            kt[i] = kv * E;
+        }
+        const int c0 = 16 * qtr + 8 * h8;
+        st_tile_row8(sm + GS::KR, d, c0, D, kr);
+        st_tile_row8(sm + GS::KC, d, c0, D, kc);
+        st_tile_row8(sm + GS::QR, d, c0, D, qr);
+        st_tile_row8(sm + GS::KT, d, c0, D, kt);
     }
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {  // phase B
         tc_fence_after();
-        const uint32_t i64 = idesc_bf16(64, 64, false, false);
+        const uint32_t i64 = idesc_bf16(64, 64, false, false), i64t = idesc_bf16(64, 64, true, false),
+                       i64tt = idesc_bf16(64, 64, true, true);
         for (int ks = 0; ks < D / 16; ++ks)
             mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks), i64, ks > 0);
         for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 128, desc_kmajor(S(GS::KT), kC, ks), desc_kmajor(S(GS::DW), kC, ks), i64, 1);
+            mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
         for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), kC, ks), desc_kmajor(S(GS::KC), kC, ks), i64, ks > 0);
-        const uint32_t imk = idesc_bf16(128, 64, true, false);
+            mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt, ks > 0);
+        const uint32_t imk = idesc_bf16(128, 64, false, false);
         for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 256, desc_mnmajor(S(GS::KC), kC, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
+            mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
         const uint32_t ixv = idesc_bf16(64, 128, true, true);
         for (int ks = 0; ks < kC / 16; ++ks)
             mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv, ks > 0);
@@ -313,13 +326,13 @@ __global__ void __launch_bounds__(512, 1)
                                                             (xdb[384 + tid] + xdb[448 + tid])));
     if (tid == 0) {  // phase E
         tc_fence_after();
-        const uint32_t ik = idesc_bf16(128, 64, true, false), im = idesc_bf16(128, 64, true, true);
+        const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
         for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 128, desc_mnmajor(S(GS::KC), kC, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
+            mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
         for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 192, desc_mnmajor(S(GS::QR), kC, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
+            mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
         for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), kC, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+            mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
         mma_commit(&bars[1]);
     }
     if (!wait_all(&bars[1], 0, ws.status, 46, fail)) goto cleanup;
@@ -339,15 +352,17 @@ __global__ void __launch_bounds__(512, 1)
             tmem_ld8(tmem + lb + 256 + cb, aQr);
             tmem_ld8(tmem + lb + 448 + cb, aXk);
             tmem_ld_wait();
+            // the bf16 factor values the MMAs used (zero on rows >= c): row d of the transposed tiles
+            const uint4 fkt = ld_raw16(sm + GS::KT, d, (int)cb, D), fqr = ld_raw16(sm + GS::QR, d, (int)cb, D);
+            const uint4 fkr = ld_raw16(sm + GS::KR, d, (int)cb, D), fkc = ld_raw16(sm + GS::KC, d, (int)cb, D);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int ii = 8 * rb + i, r = 16 * qtr + ii;
                 const bool in = r < c;
                 const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
                 const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
-                // the bf16 factor values the MMAs used (zero on rows >= c)
-                const float kt_b = ld_col(sm + GS::KT, ad, r), qr_b = ld_col(sm + GS::QR, ad, r);
-                const float kr_b = ld_col(sm + GS::KR, ad, r), kc_b = ld_col(sm + GS::KC, ad, r);
+                const float kt_b = bf16_at(fkt, i), qr_b = bf16_at(fqr, i);
+                const float kr_b = bf16_at(fkr, i), kc_b = bf16_at(fkc, i);
                 const float gm = G2[ii];
                 const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
                 const float b = sbeta[r];

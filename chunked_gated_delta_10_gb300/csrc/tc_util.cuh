@@ -223,6 +223,15 @@ __device__ __forceinline__ void ld_tile_row8(const uint8_t* tile, int r, int c0,
     }
 }
 
+// The same 16 bytes unconverted, and element i (0..7) of such a group as fp32.
+__device__ __forceinline__ uint4 ld_raw16(const uint8_t* tile, int r, int c0, int R) {
+    return *reinterpret_cast<const uint4*>(tile + tile_off(r, c0, R));
+}
+__device__ __forceinline__ float bf16_at(const uint4& v, int i) {
+    const uint32_t w = i < 2 ? v.x : i < 4 ? v.y : i < 6 ? v.z : v.w;
+    return __uint_as_float((i & 1) ? (w & 0xffff0000u) : (w << 16));
+}
+
 // Bulk copy shared -> global (16-byte aligned, size % 16 == 0) and its group ops.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
