@@ -12,11 +12,11 @@
 //                 INV = (I + Akk)^-1 by blocked forward substitution in fp32,
 //                 then w^T = (beta K~)^T INV^T and u^T = (beta V)^T INV^T.
 //                 Writes w, u, K^, scale*Q~, Aqk, INV and e^(Gamma_C).
-//   tc_state_fwd  per (sequence, value head, 64-column half of V): the chunk
-//                 loop delta = u - w S, S <- e^(Gamma_C) S + K^^T delta
-//                 with S in registers (fp32) and a bf16 copy in shared memory;
-//                 writes S_in and delta of every chunk.
-//   tc_ds_rev     per (sequence, value head, V half), chunks in reverse:
+//   tc_state_fwd  per (sequence, value head): the chunk loop delta = u - w S,
+//                 S <- e^(Gamma_C) S + K^^T delta with S in registers (fp32)
+//                 and a bf16 copy in shared memory; writes S_in and delta of
+//                 every chunk.
+//   tc_ds_rev     per (sequence, value head), chunks in reverse:
 //                 dDelta = Aqk^T dO + K^ dS,
 //                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
 //                 dDelta and dh0.
@@ -41,7 +41,6 @@ constexpr int D = 128;                 // K = V on this path
 constexpr int TCD = kC * D * 2;        // bytes of a 64 x 128 bf16 tile
 constexpr int TCC = kC * kC * 2;       // 64 x 64
 constexpr int TDD = D * D * 2;         // 128 x 128
-constexpr int HALF = 64;               // V columns per state-pass CTA
 
 // ---------------------------------------------------------------------------
 // (I + L)^-1 for a strictly lower triangular 64 x 64 L (fp32, shared), by
@@ -309,294 +308,316 @@ cleanup:
 }
 
 // ---------------------------------------------------------------------------
-// tc_state_fwd: one CTA per (V half, value head, sequence) -- the two halves of
-// one head are adjacent in launch order so their shared tile reads hit L2; 128 threads,
-// thread t owns state row t (64 fp32 columns). Double-buffered chunk inputs.
+// tc_state_fwd: one CTA per (value head, sequence), 256 threads; thread t owns
+// state row k = t % 128, columns 64 (t / 128) .. +63 in fp32 registers. A bf16
+// copy of S in shared memory feeds the MMAs and is the S_in checkpoint. Chunk
+// inputs: u and e^Gamma_C double-buffered; w and K^ single-buffered, each
+// refetched as soon as its MMA has consumed it. delta overwrites u in place.
 // ---------------------------------------------------------------------------
-struct FwdBuf {
-    static constexpr int W = 0, KH = TCD, U = 2 * TCD, EGC = 2 * TCD + TCD / 2, BYTES = 2 * TCD + TCD / 2 + 1024;
+struct FwdSm {
+    static constexpr int W = 0, KH = TCD, U = 2 * TCD, UBUF = TCD + 1024;  // u tile, then e^Gamma_C (512 B)
+    static constexpr int S = U + 2 * UBUF, BARS = S + TDD, END = BARS + 64;
 };
-constexpr int kFwdSmem = 1024 + 2 * FwdBuf::BYTES + D * HALF * 2 + kC * HALF * 2 + 64;
+constexpr int kFwdSmem = 1024 + FwdSm::END;
 
-__global__ void __launch_bounds__(128, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
+__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
                                                           TcWs ws) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
-    uint8_t* buf0 = sm;
-    uint8_t* tS = sm + 2 * FwdBuf::BYTES;   // bf16 S, 128 rows x 64 cols
-    uint8_t* tDl = tS + D * HALF * 2;       // bf16 delta, 64 rows x 64 cols
-    uint64_t* bars = reinterpret_cast<uint64_t*>(tDl + kC * HALF * 2);  // full[2], mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
+    uint8_t* tS = sm + FwdSm::S;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FwdSm::BARS);  // u[2], w, K^, mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, z = blockIdx.x, hv = blockIdx.y, n = blockIdx.z, v0 = z * HALF;
+    const int k = tid & 127, vh = tid >> 7;
+    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 128);
-    float S[HALF];
+    if (warp == 0) tmem_alloc(tslot, 256);
+    float S[64];
     {
-        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + tid) * D + v0 : nullptr;
+        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
     }
-    auto issue = [&](int it) {
-        const int64_t ch = (c0 + it) * HV + hv;
-        uint8_t* b = buf0 + (it & 1) * FwdBuf::BYTES;
-        uint64_t* full = &bars[it & 1];
-        mbar_expect_tx(full, 2 * TCD + TCD / 2 + 512);
-        bulk_load(b + FwdBuf::W, ws.w + ch * TCD, TCD, full);
-        bulk_load(b + FwdBuf::KH, ws.kh + ch * TCD, TCD, full);
-        bulk_load(b + FwdBuf::U, ws.u + ch * TCD + z * (TCD / 2), TCD / 2, full);
-        bulk_load(b + FwdBuf::EGC, ws.egc + ch * D, 512, full);
+    auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
+    auto issue_u = [&](int it) {
+        uint8_t* b = sm + FwdSm::U + (it & 1) * FwdSm::UBUF;
+        mbar_expect_tx(&bars[it & 1], TCD + 512);
+        bulk_load(b, ws.u + chunk(it) * TCD, TCD, &bars[it & 1]);
+        bulk_load(b + TCD, ws.egc + chunk(it) * D, 512, &bars[it & 1]);
+    };
+    auto issue_w = [&](int it) {
+        mbar_expect_tx(&bars[2], TCD);
+        bulk_load(sm + FwdSm::W, ws.w + chunk(it) * TCD, TCD, &bars[2]);
+    };
+    auto issue_kh = [&](int it) {
+        mbar_expect_tx(&bars[3], TCD);
+        bulk_load(sm + FwdSm::KH, ws.kh + chunk(it) * TCD, TCD, &bars[3]);
     };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    if (tid == 0) {
-        if (nts > 0) issue(0);
-        if (nts > 1) issue(1);
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
+    if (tid == 0 && nts > 0) {
+        issue_w(0);
+        issue_kh(0);
+        issue_u(0);
+        if (nts > 1) issue_u(1);
     }
     uint32_t mph = 0;
     for (int it = 0; it < nts; ++it) {
-        const int64_t ch = (c0 + it) * HV + hv;
-        uint8_t* b = buf0 + (it & 1) * FwdBuf::BYTES;
-        if (!wait_all(&bars[it & 1], (it >> 1) & 1, ws.status, 21, fail)) break;
-        // bf16 copy of S (row tid) for the MMAs, and the S_in checkpoint
+        const int64_t ch = chunk(it);
+        const uint32_t ph = (uint32_t)it & 1;  // phase of the single-buffered w and K^ barriers
+        uint8_t* tU = sm + FwdSm::U + (it & 1) * FwdSm::UBUF;
+        // bf16 copy of S (row k, this thread's 64 columns) for the MMAs and the S_in checkpoint
 #pragma unroll
-        for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tS, tid, c8, D, S + c8);
+        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        if (!wait_all(&bars[2], ph, ws.status, 21, fail)) break;
+        if (tid == 0) {  // delta accumulator = w S (chunk rows on TMEM lanes, M = 64, N = 128)
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 64, false, true);
+            const uint32_t id = idesc_bf16(64, 128, false, true);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_kmajor(smem_u32(b + FwdBuf::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
                          ks > 0);
-            mma_commit(&bars[2]);
-            bulk_store(ws.sin + ch * TDD + z * (TDD / 2), tS, TDD / 2);
+            mma_commit(&bars[4]);
+            bulk_store(ws.sin + ch * TDD, tS, TDD);
             bulk_commit();
         }
-        if (!wait_all(&bars[2], mph, ws.status, 22, fail)) break;
+        if (!wait_all(&bars[4], mph, ws.status, 22, fail)) break;
         mph ^= 1;
+        if (tid == 0 && it + 1 < nts) issue_w(it + 1);  // w is consumed
+        if (!wait_all(&bars[it & 1], (it >> 1) & 1, ws.status, 24, fail)) break;
         tc_fence_after();
-        {  // delta rows: M = 64 layout, chunk row r = 16 * warp + lane for lane < 16
-            float acc[HALF];
-            tmem_ld32(tmem + lane_base, acc);
-            tmem_ld32(tmem + lane_base + 32, acc + 32);
-            tmem_ld_wait();
-            if (lane < 16) {
-                const int r = 16 * warp + lane;
+        {  // delta = u - w S in place of u: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+            const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
 #pragma unroll
-                for (int c8 = 0; c8 < HALF; c8 += 8) {
-                    float x[8];
-                    ld_tile_row8(b + FwdBuf::U, r, c8, kC, x);
+            for (int h = 0; h < 2; ++h) {
+                float acc[32];
+                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld_wait();
+                if (lane < 16) {
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
-                    st_tile_row8(tDl, r, c8, kC, x);
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        float x[8];
+                        ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
+                        st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+                    }
                 }
             }
         }
         tc_fence_before();
         fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        if (!wait_all(&bars[3], ph, ws.status, 25, fail)) break;
+        if (tid == 0) {  // S accumulator = K^^T delta (M = 128, N = 128)
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 64, true, true);
+            const uint32_t id = idesc_bf16(128, 128, true, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + FwdBuf::KH), kC, ks), desc_mnmajor(smem_u32(tDl), kC, ks),
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + FwdSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          id, ks > 0);
-            mma_commit(&bars[2]);
-            bulk_store(ws.vn + ch * TCD + z * (TCD / 2), tDl, TCD / 2);
+            mma_commit(&bars[4]);
+            bulk_store(ws.vn + ch * TCD, tU, TCD);
             bulk_commit();
         }
-        if (!wait_all(&bars[2], mph, ws.status, 23, fail)) break;
+        if (!wait_all(&bars[4], mph, ws.status, 23, fail)) break;
         mph ^= 1;
+        if (tid == 0 && it + 1 < nts) issue_kh(it + 1);  // K^ is consumed
         tc_fence_after();
         {
-            const float e = reinterpret_cast<const float*>(b + FwdBuf::EGC)[tid];
-            float acc[HALF];
-            tmem_ld32(tmem + lane_base + 64, acc);
-            tmem_ld32(tmem + lane_base + 96, acc + 32);
-            tmem_ld_wait();
+            const float e = reinterpret_cast<const float*>(tU + TCD)[k];
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) S[j] = fmaf(e, S[j], acc[j]);
+            for (int h = 0; h < 2; ++h) {
+                float acc[32];
+                tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
+            }
         }
         tc_fence_before();
-        if (tid == 0) bulk_wait_read();
+        if (tid == 0) bulk_wait_read();  // S_in and delta copies have read tS and the u buffer
         __syncthreads();
-        if (tid == 0 && it + 2 < nts) issue(it + 2);
+        if (tid == 0 && it + 2 < nts) issue_u(it + 2);
     }
     if (ht && *(volatile int*)fail == 0) {
-        float* dst = ht + (((int64_t)n * HV + hv) * D + tid) * D + v0;
+        float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) dst[j] = S[j];
+        for (int j = 0; j < 64; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 // ---------------------------------------------------------------------------
-// tc_ds_rev: one CTA per (sequence, value head, V half), chunks in reverse;
-// thread t owns dS row t (64 fp32 columns). Single-buffered chunk inputs in two
-// groups: K^, Q~s, Aqk and dO (first MMA group) are refetched for the next
-// chunk as soon as that group completes, w and e^Gamma_C at the end of the step.
+// tc_ds_rev: one CTA per (value head, sequence), chunks in reverse; 256
+// threads, thread t owns dS row k = t % 128, columns 64 (t / 128) .. +63.
+// Chunk inputs are single-buffered in two groups, each refetched for the next
+// chunk as soon as its MMAs have consumed it: K^, Q~s, Aqk and dO after the
+// first MMA group, w and e^Gamma_C after the second. dDelta is staged in the
+// dS tile once the dS_out copy has read it.
 // ---------------------------------------------------------------------------
-struct RevBuf {
-    static constexpr int KH = 0, W = TCD, QS = 2 * TCD, AQK = 3 * TCD, DO = 3 * TCD + TCC, EGC = 3 * TCD + TCC + 8192,
-                         BYTES = 3 * TCD + TCC + 8192 + 1024;
+struct RevSm {
+    static constexpr int KH = 0, QS = TCD, AQK = 2 * TCD, DO = 2 * TCD + TCC, W = 3 * TCD + TCC, EGC = 4 * TCD + TCC;
+    static constexpr int S = EGC + 1024, BARS = S + TDD, END = BARS + 64;
 };
-constexpr int kRevSmem = 1024 + RevBuf::BYTES + D * HALF * 2 + kC * HALF * 2 + 64;
+constexpr int kRevSmem = 1024 + RevSm::END;
 
-__global__ void __launch_bounds__(128, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
+__global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
                                                        TcWs ws, const __grid_constant__ CUtensorMap tm_do) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
-    uint8_t* b = sm;
-    uint8_t* tS = sm + RevBuf::BYTES;        // bf16 dS, 128 x 64
-    uint8_t* tDd = tS + D * HALF * 2;        // bf16 dDelta, 64 x 64
-    uint64_t* bars = reinterpret_cast<uint64_t*>(tDd + kC * HALF * 2);  // full (group 1), mma, full (group 2)
+    uint8_t* tS = sm + RevSm::S;  // bf16 dS (128 x 128), later dDelta (64 x 128)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + RevSm::BARS);  // group 1, group 2, mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, z = blockIdx.x, hv = blockIdx.y, n = blockIdx.z, v0 = z * HALF;
+    const int k = tid & 127, vh = tid >> 7;
+    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
 
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_init(&bars[2], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 128);
-    float S[HALF];
+    if (warp == 0) tmem_alloc(tslot, 256);
+    float S[64];
     {
-        const float* src = dht ? dht + (((int64_t)n * HV + hv) * D + tid) * D + v0 : nullptr;
+        const float* src = dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
     }
+    auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
     auto issue1 = [&](int it) {  // operands of the first MMA group
-        const int64_t ch = (c0 + it) * HV + hv;
-        mbar_expect_tx(&bars[0], 2 * TCD + TCC + 8192);
-        bulk_load(b + RevBuf::KH, ws.kh + ch * TCD, TCD, &bars[0]);
-        bulk_load(b + RevBuf::QS, ws.qs + ch * TCD, TCD, &bars[0]);
-        bulk_load(b + RevBuf::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
-        tma_load_3d(b + RevBuf::DO, &tm_do, v0, hv, (int)(bos + (int64_t)it * kC), &bars[0]);
+        const int64_t ch = chunk(it);
+        mbar_expect_tx(&bars[0], 3 * TCD + TCC);
+        bulk_load(sm + RevSm::KH, ws.kh + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + RevSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + RevSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
+        const int row = (int)(bos + (int64_t)it * kC);
+        tma_load_3d(sm + RevSm::DO, &tm_do, 0, hv, row, &bars[0]);
+        tma_load_3d(sm + RevSm::DO + TCD / 2, &tm_do, 64, hv, row, &bars[0]);
     };
     auto issue2 = [&](int it) {  // w (second MMA group) and e^Gamma_C (state update)
-        const int64_t ch = (c0 + it) * HV + hv;
-        mbar_expect_tx(&bars[2], TCD + 512);
-        bulk_load(b + RevBuf::W, ws.w + ch * TCD, TCD, &bars[2]);
-        bulk_load(b + RevBuf::EGC, ws.egc + ch * D, 512, &bars[2]);
+        const int64_t ch = chunk(it);
+        mbar_expect_tx(&bars[1], TCD + 512);
+        bulk_load(sm + RevSm::W, ws.w + ch * TCD, TCD, &bars[1]);
+        bulk_load(sm + RevSm::EGC, ws.egc + ch * D, 512, &bars[1]);
     };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
     if (tid == 0 && nts > 0) {
         issue1(nts - 1);
         issue2(nts - 1);
     }
-    uint32_t fph = 0, mph = 0;
+    uint32_t mph = 0;
     for (int it = nts - 1; it >= 0; --it) {
-        const int64_t ch = (c0 + it) * HV + hv;
-        if (!wait_all(&bars[0], fph, ws.status, 31, fail)) break;
+        const int64_t ch = chunk(it);
+        const uint32_t ph = (uint32_t)(nts - 1 - it) & 1;
+        // bf16 copy of dS (row k, this thread's 64 columns): MMA operand and the dS_out checkpoint
 #pragma unroll
-        for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tS, tid, c8, D, S + c8);
+        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
-        __syncthreads();
+        if (!wait_all(&bars[0], ph, ws.status, 31, fail)) break;
         if (tid == 0) {
             tc_fence_after();
-            // dDelta = Aqk^T dO + K^ dS (M = 64: chunk rows)
-            const uint32_t ida = idesc_bf16(64, 64, true, true), idb = idesc_bf16(64, 64, false, true);
+            // dDelta = Aqk^T dO + K^ dS (chunk rows on TMEM lanes, M = 64, N = 128)
+            const uint32_t ida = idesc_bf16(64, 128, true, true), idb = idesc_bf16(64, 128, false, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem, desc_mnmajor(smem_u32(b + RevBuf::AQK), kC, ks),
-                         desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks), ida, ks > 0);
+                mma_bf16(tmem, desc_mnmajor(smem_u32(sm + RevSm::AQK), kC, ks),
+                         desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), ida, ks > 0);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_kmajor(smem_u32(b + RevBuf::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + RevSm::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
                          1);
-            // dS_acc = Q~s^T dO (M = 128)
-            const uint32_t idc = idesc_bf16(128, 64, true, true);
+            // dS accumulator = Q~s^T dO (M = 128, N = 128)
+            const uint32_t idc = idesc_bf16(128, 128, true, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + RevBuf::QS), kC, ks),
-                         desc_mnmajor(smem_u32(b + RevBuf::DO), kC, ks), idc, ks > 0);
-            mma_commit(&bars[1]);
-            bulk_store(ws.dso + ch * TDD + z * (TDD / 2), tS, TDD / 2);
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::QS), kC, ks),
+                         desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), idc, ks > 0);
+            mma_commit(&bars[2]);
+            bulk_store(ws.dso + ch * TDD, tS, TDD);
             bulk_commit();
         }
-        if (!wait_all(&bars[1], mph, ws.status, 32, fail)) break;
+        if (!wait_all(&bars[2], mph, ws.status, 32, fail)) break;
         mph ^= 1;
+        if (tid == 0) {
+            if (it > 0) issue1(it - 1);  // the first group's operands are consumed
+            bulk_wait_read();            // the dS_out copy has read tS
+        }
+        __syncthreads();
         tc_fence_after();
-        if (tid == 0 && it > 0) issue1(it - 1);  // the first group's operands are consumed
-        {
-            float acc[kC];
-            tmem_ld32(tmem + lane_base, acc);
-            tmem_ld32(tmem + lane_base + 32, acc + 32);
-            tmem_ld_wait();
-            if (lane < 16) {  // chunk row r = 16 * warp + lane
-                const int r = 16 * warp + lane;
+        {  // dDelta rows into tS: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+            const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
 #pragma unroll
-                for (int c8 = 0; c8 < HALF; c8 += 8) st_tile_row8(tDd, r, c8, kC, acc + c8);
+            for (int h = 0; h < 2; ++h) {
+                float acc[32];
+                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tS, r, cb + 32 * h + c8, kC, acc + c8);
+                }
             }
         }
         tc_fence_before();
         fence_async_smem();
-        if (!wait_all(&bars[2], fph, ws.status, 34, fail)) break;  // its barrier also publishes dDelta
-        fph ^= 1;
-        if (tid == 0) {
+        if (!wait_all(&bars[1], ph, ws.status, 34, fail)) break;
+        if (tid == 0) {  // dS accumulator -= w^T dDelta
             tc_fence_after();
-            const uint32_t id = idesc_neg_a(idesc_bf16(128, 64, true, true));
+            const uint32_t id = idesc_neg_a(idesc_bf16(128, 128, true, true));
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 64, desc_mnmajor(smem_u32(b + RevBuf::W), kC, ks), desc_mnmajor(smem_u32(tDd), kC, ks),
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::W), kC, ks), desc_mnmajor(smem_u32(tS), kC, ks),
                          id, 1);
-            mma_commit(&bars[1]);
-            bulk_store(ws.dvn + ch * TCD + z * (TCD / 2), tDd, TCD / 2);
+            mma_commit(&bars[2]);
+            bulk_store(ws.dvn + ch * TCD, tS, TCD);
             bulk_commit();
         }
-        if (!wait_all(&bars[1], mph, ws.status, 33, fail)) break;
+        const float e = reinterpret_cast<const float*>(sm + RevSm::EGC)[k];
+        if (!wait_all(&bars[2], mph, ws.status, 33, fail)) break;
         mph ^= 1;
+        if (tid == 0 && it > 0) issue2(it - 1);  // w and e^Gamma_C are consumed
         tc_fence_after();
-        {
-            const float e = reinterpret_cast<const float*>(b + RevBuf::EGC)[tid];
-            float acc[HALF];
-            tmem_ld32(tmem + lane_base + 64, acc);
-            tmem_ld32(tmem + lane_base + 96, acc + 32);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float acc[32];
+            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < HALF; ++j) S[j] = fmaf(e, S[j], acc[j]);
+            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
         }
         tc_fence_before();
-        if (tid == 0) bulk_wait_read();
+        if (tid == 0) bulk_wait_read();  // the dDelta copy has read tS
         __syncthreads();
-        if (tid == 0 && it > 0) issue2(it - 1);
     }
     if (dh0 && *(volatile int*)fail == 0) {
-        float* dst = dh0 + (((int64_t)n * HV + hv) * D + tid) * D + v0;
+        float* dst = dh0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) dst[j] = S[j];
+        for (int j = 0; j < 64; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
 template <typename F>
@@ -632,11 +653,11 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         note_launch("tc_intra", st);
     }
     if (stages >= 2) {
-        k_tc_state_fwd<<<dim3(2, p.HV, p.N), 128, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
+        k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
         note_launch("tc_state_fwd", st);
     }
     if (stages >= 3) {
-        k_tc_ds_rev<<<dim3(2, p.HV, p.N), 128, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
+        k_tc_ds_rev<<<dim3(p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
         note_launch("tc_ds_rev", st);
     }
     if (stages >= 4) {
