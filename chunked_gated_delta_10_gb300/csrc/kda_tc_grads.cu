@@ -46,90 +46,81 @@ constexpr int TCD = kC * D * 2, TCC = kC * kC * 2, TDD = D * D * 2;
 struct GS {
     static constexpr int Q = 0, K = TCD, V = 2 * TCD, DO = 3 * TCD, DL = 4 * TCD, DDL = 5 * TCD;
     static constexpr int SIN = 6 * TCD, DSO = SIN + TDD;
-    // after phase A the S_in / dS_out area holds the decayed factor tiles
+    // after phase A the S_in / dS_out area holds the decayed factor tiles, stored transposed
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
     static constexpr int DW = DSO + TDD;
     static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, DINV = DM + TCC, TT = DINV + TCC;
-    static constexpr int EGC = TT + TCC, BETA = EGC + 512, BARS = BETA + 256, END = BARS + 64;
-    // exchange scratch: before phase C the TT tile area holds the gate-cumsum quarter totals
-    // and the reference / last-row gates; after phase A the dead dO tile holds the fixed-order
-    // partial sums of <S_in, dS_out>, the Gamma_C terms, the dg quarter totals and dbeta.
-    static constexpr int XTOT = TT, XRG = TT + 2048;
-    static constexpr int XRD = DO, XGC = DO + 2048, XT1 = DO + 4096, XDB = DO + 6144;
+    // the g tile (64 x 128 fp32) of a chunk lands on DN .. TT, which the previous chunk no longer needs after phase E
+    static constexpr int GT = DN;
+    static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048, NXT = BARS + 64;
+    static constexpr int END = NXT + 64;
+    // scratch in the dw tile while that tile is dead: cumsum quarter totals and the reference / last-row gates
+    // (chunk start), dbeta partials (epilogues B and D), Gamma_C terms and dg quarter totals (final epilogue)
+    static constexpr int XTOT = DW, XRG = DW + 2048, XDB = DW + 4096, XGC = DW + 8192, XT1 = DW + 10240;
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
+__device__ __forceinline__ float bfr(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 struct GradMaps {
-    CUtensorMap q, k, v, d_o;
+    CUtensorMap q, k, v, d_o, g;
 };
 
-// 512 threads. Channel-oriented work: thread (d = tid % 128, quarter = tid / 128)
-// owns key channel d for chunk rows 16 * quarter .. 16 * quarter + 15. Row-oriented
-// work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16), column
-// quarter warp / 4. Every cross-thread sum is combined in a fixed order.
+// One work item = one (chunk, value head), index w = chunk * HV + hv; items are dealt to the
+// persistent CTAs round-robin.
+struct Item {
+    int64_t r0, ch;
+    int hv, h, c, valid;
+};
+__device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) {
+    Item it;
+    it.hv = (int)(w % p.HV);
+    it.h = it.hv / (p.HV / p.H);
+    it.ch = w;
+    it.valid = valid ? 1 : 0;
+    chunk_rows(p, w / p.HV, it.r0, it.c);
+    return it;
+}
+
+// Persistent, 512 threads, one CTA per SM. Channel-oriented work: thread (d = tid % 128,
+// quarter = tid / 128) owns key channel d for chunk rows 16 * quarter .. 16 * quarter + 15.
+// Row-oriented work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16),
+// column quarter warp / 4. Every cross-thread sum is combined in a fixed order. The
+// inputs of the next item are fetched in five groups, each as soon as the current item's
+// phases have consumed its regions: dO, delta after phase A; q, k after the factor pass;
+// v, d_delta after phase B; INV after phase D; S_in, dS_out, g and e^Gamma_C after phase E.
 __global__ void __launch_bounds__(512, 1)
-    k_tc_grads(Prob p, const float* __restrict__ g, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
-               bf16* __restrict__ dk_out, bf16* __restrict__ dv_out, float* __restrict__ dg_out,
-               bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
+    k_tc_grads(Prob p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out, bf16* __restrict__ dk_out,
+               bf16* __restrict__ dv_out, float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws,
+               const __grid_constant__ GradMaps maps) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
-    float* sbeta = reinterpret_cast<float*>(sm + GS::BETA);
-    const float* segc = reinterpret_cast<const float*>(sm + GS::EGC);
     float* xtot = reinterpret_cast<float*>(sm + GS::XTOT);
     float* xrg = reinterpret_cast<float*>(sm + GS::XRG);
     float* xrd = reinterpret_cast<float*>(sm + GS::XRD);
     float* xgc = reinterpret_cast<float*>(sm + GS::XGC);
     float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
     float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);  // [0] loads, [1] mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    const float* gt = reinterpret_cast<const float*>(sm + GS::GT);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);  // [0, 1] inputs (by item parity), [2] mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
+    Item* nx = reinterpret_cast<Item*>(sm + GS::NXT);  // the next item of this CTA (written by thread 0)
     auto S = [&](int off) { return smem_u32(sm + off); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = tid & 127, qtr = tid >> 7, q4 = warp & 3, cq = warp >> 2;
-    const int HV = p.HV, H = p.H, G = HV / H, hv = blockIdx.y, h = hv / G;
-    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
-    int64_t r0;
-    int c;
-    chunk_rows(p, gc, r0, c);
-    float G2[16];  // g of channel d, this thread's 16 rows; Gamma2 after the cumsum below
-    load_g_quarters<1>(g, r0, c, HV, hv, d, qtr, G2);
+    const int HV = p.HV, H = p.H, G = HV / H;
+    const int64_t total = p.NT * HV;
 
-    if (tid == 0) {  // all input copies start right after the g loads
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+    if (tid == 0) {
+        mbar_init(&bars[0], 5);
+        mbar_init(&bars[1], 5);
+        mbar_init(&bars[2], 1);
         fence_mbar_init();
         *fail = 0;
-        mbar_expect_tx(&bars[0], 6 * TCD + 2 * TDD + TCC + 512);
-        const int row = (int)r0;
-        for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + GS::Q + b * (TCD / 2), &maps.q, 64 * b, h, row, &bars[0]);
-            tma_load_3d(sm + GS::K + b * (TCD / 2), &maps.k, 64 * b, h, row, &bars[0]);
-            tma_load_3d(sm + GS::V + b * (TCD / 2), &maps.v, 64 * b, hv, row, &bars[0]);
-            tma_load_3d(sm + GS::DO + b * (TCD / 2), &maps.d_o, 64 * b, hv, row, &bars[0]);
-        }
-        bulk_load(sm + GS::DL, ws.vn + ch * TCD, TCD, &bars[0]);
-        bulk_load(sm + GS::DDL, ws.dvn + ch * TCD, TCD, &bars[0]);
-        bulk_load(sm + GS::SIN, ws.sin + ch * TDD, TDD, &bars[0]);
-        bulk_load(sm + GS::DSO, ws.dso + ch * TDD, TDD, &bars[0]);
-        bulk_load(sm + GS::INV, ws.inv + ch * TCC, TCC, &bars[0]);
-        bulk_load(sm + GS::EGC, ws.egc + ch * D, 512, &bars[0]);
     }
     if (warp == 0) tmem_alloc(tslot, 512);
-    if (tid < kC) sbeta[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const ColAddr ad(d, kC);  // this thread's column in the 64-row tiles
-    // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
-    quarter_cumsum_log2<1>(G2, d, qtr, xtot, G2);
-    const int rmid = (c - 1) >> 1;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        if (16 * qtr + i == rmid) xrg[d] = G2[i];
-        if (16 * qtr + i == c - 1) xrg[128 + d] = G2[i];
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -137,281 +128,385 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
     const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
     const bool rv = lane < 16;
-    const float ref = xrg[d], gC = xrg[128 + d];
-    // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
-    // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
-    const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
 
-    float rd = 0.f;
-    if (!wait_all(&bars[0], 0, ws.status, 41, fail)) goto cleanup;
-    if (tid == 0) {  // phase A
-        tc_fence_after();
-        const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
-                       i64 = idesc_bf16(64, 64, false, false);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks), idesc_neg_a(i64n),
-                     ks > 0);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
-        mma_commit(&bars[1]);
-    }
-#pragma unroll
-    for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
-        const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
-        const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
-        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
-            rd = fmaf(fa.x, fb.x, rd);
-            rd = fmaf(fa.y, fb.y, rd);
+    // the five input groups of an item into input barrier `b` (issued by thread 0)
+    auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta
+        mbar_expect_tx(b, 2 * TCD);
+        tma_load_3d(sm + GS::DO, &maps.d_o, 0, n.hv, (int)n.r0, b);
+        tma_load_3d(sm + GS::DO + TCD / 2, &maps.d_o, 64, n.hv, (int)n.r0, b);
+        bulk_load(sm + GS::DL, ws.vn + n.ch * TCD, TCD, b);
+    };
+    auto issue_qk = [&](const Item& n, uint64_t* b) {
+        mbar_expect_tx(b, 2 * TCD);
+        for (int x = 0; x < 2; ++x) {
+            tma_load_3d(sm + GS::Q + x * (TCD / 2), &maps.q, 64 * x, n.h, (int)n.r0, b);
+            tma_load_3d(sm + GS::K + x * (TCD / 2), &maps.k, 64 * x, n.h, (int)n.r0, b);
         }
+    };
+    auto issue_b = [&](const Item& n, uint64_t* b) {  // v, d_delta
+        mbar_expect_tx(b, 2 * TCD);
+        tma_load_3d(sm + GS::V, &maps.v, 0, n.hv, (int)n.r0, b);
+        tma_load_3d(sm + GS::V + TCD / 2, &maps.v, 64, n.hv, (int)n.r0, b);
+        bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD, b);
+    };
+    auto issue_d = [&](const Item& n, uint64_t* b) {  // INV
+        mbar_expect_tx(b, TCC);
+        bulk_load(sm + GS::INV, ws.inv + n.ch * TCC, TCC, b);
+    };
+    auto issue_e = [&](const Item& n, uint64_t* b, int slot) {  // S_in, dS_out, g, e^Gamma_C
+        mbar_expect_tx(b, 2 * TDD + kC * D * 4 + 512);
+        bulk_load(sm + GS::SIN, ws.sin + n.ch * TDD, TDD, b);
+        bulk_load(sm + GS::DSO, ws.dso + n.ch * TDD, TDD, b);
+        tma_load_3d(sm + GS::GT, &maps.g, 0, n.hv, (int)n.r0, b);
+        bulk_load(sm + GS::EGC + 512 * slot, ws.egc + n.ch * D, 512, b);
+    };
+
+    int64_t w = blockIdx.x;
+    Item cur = make_item(p, w < total ? w : 0, w < total);
+    const ColAddr ad(d, kC);  // this thread's column in the 64-row q / k tiles
+    if (tid < kC) {
+        float* sb = reinterpret_cast<float*>(sm + GS::BETA);
+        sb[tid] = (w < total && tid < cur.c) ? __bfloat162float(beta[(cur.r0 + tid) * HV + cur.hv]) : 0.f;
     }
-    if (!wait_all(&bars[1], 0, ws.status, 42, fail)) goto cleanup;
-    tc_fence_after();
-    xrd[qtr * 128 + d] = rd;  // the dO tile is dead from here on
-    {  // epilogue A: dw row segment (32 columns) and dN row segment (16 columns)
-        float x[32];
-        tmem_ld32(tmem + lb + 128 + 32 * cq, x);
-        tmem_ld_wait();
-        if (rv)
-            for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, 32 * cq + 8 * u, kC, x + 8 * u);
-        tmem_ld16(tmem + lb + 256 + 16 * cq, x);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
-        if (rv)
-            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+    if (tid == 0 && w < total) {
+        issue_a(cur, &bars[0]);
+        issue_qk(cur, &bars[0]);
+        issue_b(cur, &bars[0]);
+        issue_d(cur, &bars[0]);
+        issue_e(cur, &bars[0], 0);
     }
-    tc_fence_before();
-    // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
-    // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero)
-#pragma unroll
-    for (int h8 = 0; h8 < 2; ++h8) {
-        float kr[8], kc[8], qr[8], kt[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = 16 * qtr + 8 * h8 + i;
-            const bool in = r < c;
-            const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
-            const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
-            const float gm = G2[8 * h8 + i];
-            const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
-            kr[i] = kv * ep;
-            kc[i] = kv * em;
-            qr[i] = qv * ep;
-            kt[i] = kv * E;
+    uint32_t mph = 0;
+    for (int i = 0; w < total; ++i, w += gridDim.x) {
+        const int slot = i & 1;
+        if (tid == 0) {
+            const int64_t wn = w + gridDim.x;
+            *nx = make_item(p, wn < total ? wn : w, wn < total);
         }
-        const int c0 = 16 * qtr + 8 * h8;
-        st_tile_row8(sm + GS::KR, d, c0, D, kr);
-        st_tile_row8(sm + GS::KC, d, c0, D, kc);
-        st_tile_row8(sm + GS::QR, d, c0, D, qr);
-        st_tile_row8(sm + GS::KT, d, c0, D, kt);
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // phase B
-        tc_fence_after();
-        const uint32_t i64 = idesc_bf16(64, 64, false, false), i64t = idesc_bf16(64, 64, true, false),
-                       i64tt = idesc_bf16(64, 64, true, true);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks), i64, ks > 0);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt, ks > 0);
-        const uint32_t imk = idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
-        const uint32_t ixv = idesc_bf16(64, 128, true, true);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv, ks > 0);
-        const uint32_t ixk = idesc_bf16(128, 64, true, true);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk, ks > 0);
-        mma_commit(&bars[1]);
-    }
-    if (!wait_all(&bars[1], 1, ws.status, 43, fail)) goto cleanup;
-    tc_fence_after();
-    {  // epilogue B: dbeta (INV part), dINV columns, dv rows
-        const float br = rv ? sbeta[rrow] : 0.f;
-        float x[32];
-        float db = 0.f;
-        tmem_ld16(tmem + lb + 128 + 16 * cq, x);
-        tmem_ld_wait();
-        if (rv) {
-            const ColAddr ar(rrow, kC);
+        uint64_t* nbar = &bars[slot ^ 1];
+        const float* sbeta = reinterpret_cast<const float*>(sm + GS::BETA + 256 * slot);
+        const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
+        const int64_t r0 = cur.r0;
+        const int c = cur.c, hv = cur.hv, h = cur.h;
+        if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 41, fail)) break;
+        const bool has_next = nx->valid != 0;
+        // beta of the next item: loaded now, stored to its shared slot at the end of this item
+        const float nbeta =
+            (has_next && tid < nx->c) ? __bfloat162float(beta[(nx->r0 + tid) * HV + nx->hv]) : 0.f;
+        // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
+        float G2[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) db = fmaf(ld_col(sm + GS::INV, ar, 16 * cq + u), x[u], db);
-#pragma unroll
-            for (int u = 0; u < 16; u += 2) st_col_pair(sm + GS::DINV, ar, 16 * cq + u, br * x[u], br * x[u + 1]);
-            xdb[cq * 64 + rrow] = db;
+        for (int x = 0; x < 16; ++x) {
+            const int r = 16 * qtr + x;
+            G2[x] = r < c ? gt[r * D + d] : 0.f;
         }
-        tmem_ld32(tmem + lb + 320 + 32 * cq, x);
-        tmem_ld_wait();
-        if (rv && rrow < c) {
-            bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D + 32 * cq;
+        quarter_cumsum_log2<1>(G2, d, qtr, xtot, G2);
+        const int rmid = (c - 1) >> 1;
 #pragma unroll
-            for (int u = 0; u < 32; u += 8) {
-                uint4 vv;
-                vv.x = pack2(br * x[u], br * x[u + 1]);
-                vv.y = pack2(br * x[u + 2], br * x[u + 3]);
-                vv.z = pack2(br * x[u + 4], br * x[u + 5]);
-                vv.w = pack2(br * x[u + 6], br * x[u + 7]);
-                *reinterpret_cast<uint4*>(dvrow + u) = vv;
+        for (int x = 0; x < 16; ++x) {
+            if (16 * qtr + x == rmid) xrg[d] = G2[x];
+            if (16 * qtr + x == c - 1) xrg[128 + d] = G2[x];
+        }
+        __syncthreads();
+        const float ref = xrg[d], gC = xrg[128 + d];
+        // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
+        // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
+        const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
+
+        if (tid == 0) {  // phase A
+            tc_fence_after();
+            const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
+                           i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
+                         idesc_neg_a(i64n), ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
+                         ks > 0);
+            mma_commit(&bars[2]);
+        }
+        float rd = 0.f;
+#pragma unroll
+        for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
+            const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
+            const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
+            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
+                rd = fmaf(fa.x, fb.x, rd);
+                rd = fmaf(fa.y, fb.y, rd);
             }
         }
-    }
-    tc_fence_before();
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // phase C: T = dINV INV^T
+        xrd[qtr * 128 + d] = rd;
+        if (!wait_all(&bars[2], mph, ws.status, 42, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && has_next) issue_a(*nx, nbar);  // dO and delta are consumed
         tc_fence_after();
-        const uint32_t i64 = idesc_bf16(64, 64, false, false);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 128, desc_kmajor(S(GS::DINV), kC, ks), desc_kmajor(S(GS::INV), kC, ks), i64, ks > 0);
-        mma_commit(&bars[1]);
-    }
-    if (!wait_all(&bars[1], 0, ws.status, 44, fail)) goto cleanup;
-    tc_fence_after();
-    {
-        float x[16];
-        tmem_ld16(tmem + lb + 128 + 16 * cq, x);
-        tmem_ld_wait();
-        if (rv)
-            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-    }
-    tc_fence_before();
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {  // phase D: dAkk = -INV^T T
-        tc_fence_after();
-        const uint32_t id = idesc_neg_a(idesc_bf16(64, 64, true, true));
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), id, ks > 0);
-        mma_commit(&bars[1]);
-    }
-    if (!wait_all(&bars[1], 1, ws.status, 45, fail)) goto cleanup;
-    tc_fence_after();
-    {  // epilogue D: dbeta (Akk part), dM row segments
-        const float br = rv ? sbeta[rrow] : 0.f;
-        float a[16], m[16];
-        float db = 0.f;
-        tmem_ld16(tmem + lb + 320 + 16 * cq, a);
-        tmem_ld16(tmem + lb + 192 + 16 * cq, m);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int j = 16 * cq + u;
-            const bool in = j < rrow && rrow < c;
-            db = in ? fmaf(a[u], m[u], db) : db;
-            a[u] = in ? br * a[u] : 0.f;
-        }
-        if (rv) {
-            for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DM, rrow, 16 * cq + 8 * u, kC, a + 8 * u);
-            xdb[256 + cq * 64 + rrow] = db;
-        }
-    }
-    tc_fence_before();
-    fence_async_smem();
-    __syncthreads();
-    if (tid < kC && tid < c)
-        db_out[(r0 + tid) * HV + hv] = __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
-                                                           ((xdb[256 + tid] + xdb[320 + tid]) +
-                                                            (xdb[384 + tid] + xdb[448 + tid])));
-    if (tid == 0) {  // phase E
-        tc_fence_after();
-        const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
-        mma_commit(&bars[1]);
-    }
-    if (!wait_all(&bars[1], 0, ws.status, 46, fail)) goto cleanup;
-    tc_fence_after();
-    {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
-        float dG[16];
-        float dGC = 0.f;
-        const float sc = p.scale;
-#pragma unroll
-        for (int rb = 0; rb < 2; ++rb) {
-            const uint32_t cb = (uint32_t)(16 * qtr + 8 * rb);
-            float aQt[8], aKh[8], aKr[8], aKc[8], aQr[8], aXk[8];
-            tmem_ld8(tmem + lb + 0 + cb, aQt);
-            tmem_ld8(tmem + lb + 64 + cb, aKh);
-            tmem_ld8(tmem + lb + 128 + cb, aKr);
-            tmem_ld8(tmem + lb + 192 + cb, aKc);
-            tmem_ld8(tmem + lb + 256 + cb, aQr);
-            tmem_ld8(tmem + lb + 448 + cb, aXk);
+        {  // epilogue A: dw row segment (32 columns), dN row segment (16 columns), dv row segment (32 columns)
+            const float br = rv ? sbeta[rrow] : 0.f;
+            float x[32];
+            tmem_ld32(tmem + lb + 128 + 32 * cq, x);
             tmem_ld_wait();
-            // the bf16 factor values the MMAs used (zero on rows >= c): row d of the transposed tiles
-            const uint4 fkt = ld_raw16(sm + GS::KT, d, (int)cb, D), fqr = ld_raw16(sm + GS::QR, d, (int)cb, D);
-            const uint4 fkr = ld_raw16(sm + GS::KR, d, (int)cb, D), fkc = ld_raw16(sm + GS::KC, d, (int)cb, D);
+            if (rv)
+                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, 32 * cq + 8 * u, kC, x + 8 * u);
+            tmem_ld16(tmem + lb + 256 + 16 * cq, x);
+            tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int ii = 8 * rb + i, r = 16 * qtr + ii;
-                const bool in = r < c;
-                const float kv = in ? ld_col(sm + GS::K, ad, r) : 0.f;
-                const float qv = in ? ld_col(sm + GS::Q, ad, r) : 0.f;
-                const float kt_b = bf16_at(fkt, i), qr_b = bf16_at(fqr, i);
-                const float kr_b = bf16_at(fkr, i), kc_b = bf16_at(fkc, i);
-                const float gm = G2[ii];
-                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
-                const float b = sbeta[r];
-                const float dQt = sc * aQt[i], bX = b * aXk[i];
-                const float dqv = dQt * E + aQr[i] * ep;
-                const float dkv = aKh[i] * eh + bX * E + aKr[i] * ep + aKc[i] * em;
-                const float khk = aKh[i] * kv * eh;
-                // The factor values of the dGamma pair terms are the bf16 values the MMAs used, so that each
-                // in-chunk pair's contributions to its two rows cancel in the chunk sum as they do exactly.
-                const float dgv = dQt * qv * E - khk + bX * kt_b + aQr[i] * qr_b + aKr[i] * kr_b - aKc[i] * kc_b;
-                dG[ii] = in ? dgv : 0.f;
-                if (in) {
-                    dGC += khk;
-                    if (G == 1) {
-                        const int64_t o = ((r0 + r) * H + h) * D + d;
-                        st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o), reinterpret_cast<uint8_t*>(dk_out + o),
-                                     dqv, dkv);
-                    } else {
-                        const int64_t o = ((r0 + r) * HV + hv) * D + d;
-                        ws.dqp[o] = dqv;
-                        ws.dkp[o] = dkv;
-                    }
+            for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
+            if (rv)
+                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+            tmem_ld32(tmem + lb + 320 + 32 * cq, x);
+            tmem_ld_wait();
+            if (rv && rrow < c) {
+                bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D + 32 * cq;
+#pragma unroll
+                for (int u = 0; u < 32; u += 8) {
+                    uint4 vv;
+                    vv.x = pack2(br * x[u], br * x[u + 1]);
+                    vv.y = pack2(br * x[u + 2], br * x[u + 3]);
+                    vv.z = pack2(br * x[u + 4], br * x[u + 5]);
+                    vv.w = pack2(br * x[u + 6], br * x[u + 7]);
+                    *reinterpret_cast<uint4*>(dvrow + u) = vv;
                 }
             }
         }
-        xgc[qtr * 128 + d] = dGC;
-        __syncthreads();
-        const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
-                           ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
+        tc_fence_before();
+        __syncthreads();  // every warp has read dXv before its columns take the q, k stash
+        tc_fence_after();
+        // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
+        // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). The raw
+        // (k, q) pairs go to TMEM columns 384 + 16 quarter .. +15 for the final epilogue.
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            if (16 * qtr + i == c - 1) dG[i] += dGCt;
-        float run = 0.f;
+        for (int h8 = 0; h8 < 2; ++h8) {
+            float kr[8], kc[8], qr[8], kt[8];
+            uint32_t kq[8];
 #pragma unroll
-        for (int i = 15; i >= 0; --i) {
-            run += dG[i];
-            dG[i] = run;
+            for (int x = 0; x < 8; ++x) {
+                const int r = 16 * qtr + 8 * h8 + x;
+                const bool in = r < c;
+                const uint32_t kbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
+                const uint32_t qbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
+                kq[x] = kbits | (qbits << 16);
+                const float kv = __uint_as_float(kbits << 16), qv = __uint_as_float(qbits << 16);
+                const float gm = G2[8 * h8 + x];
+                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
+                kr[x] = kv * ep;
+                kc[x] = kv * em;
+                qr[x] = qv * ep;
+                kt[x] = kv * E;
+            }
+            const int c0 = 16 * qtr + 8 * h8;
+            st_tile_row8(sm + GS::KR, d, c0, D, kr);
+            st_tile_row8(sm + GS::KC, d, c0, D, kc);
+            st_tile_row8(sm + GS::QR, d, c0, D, qr);
+            st_tile_row8(sm + GS::KT, d, c0, D, kt);
+            tmem_st8(tmem + lb + 384 + (uint32_t)c0, kq);
         }
-        xt1[qtr * 128 + d] = run;
+        tmem_st_wait();
+        tc_fence_before();
+        fence_async_smem();
         __syncthreads();
-        float carry = 0.f;  // later quarters' totals, added in the order 3, 2, 1
-        for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * qtr + i;
-            if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = dG[i] + carry;
+        if (tid == 0) {  // phase B
+            tc_fence_after();
+            if (has_next) issue_qk(*nx, nbar);  // q and k are consumed
+            const uint32_t i64 = idesc_bf16(64, 64, false, false), i64t = idesc_bf16(64, 64, true, false),
+                           i64tt = idesc_bf16(64, 64, true, true);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks), i64, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt, ks > 0);
+            const uint32_t imk = idesc_bf16(128, 64, false, false);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
+            const uint32_t ixk = idesc_bf16(128, 64, true, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk, ks > 0);
+            mma_commit(&bars[2]);
         }
+        if (!wait_all(&bars[2], mph, ws.status, 43, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && has_next) issue_b(*nx, nbar);  // v and d_delta are consumed
+        tc_fence_after();
+        {  // epilogue B: dbeta (INV part), dINV columns
+            const float br = rv ? sbeta[rrow] : 0.f;
+            float x[16];
+            float db = 0.f;
+            tmem_ld16(tmem + lb + 128 + 16 * cq, x);
+            tmem_ld_wait();
+            if (rv) {
+                const ColAddr ar(rrow, kC);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) db = fmaf(ld_col(sm + GS::INV, ar, 16 * cq + u), x[u], db);
+#pragma unroll
+                for (int u = 0; u < 16; u += 2)
+                    st_col_pair(sm + GS::DINV, ar, 16 * cq + u, br * x[u], br * x[u + 1]);
+                xdb[cq * 64 + rrow] = db;
+            }
+        }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {  // phase C: T = dINV INV^T
+            tc_fence_after();
+            const uint32_t i64 = idesc_bf16(64, 64, false, false);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_kmajor(S(GS::DINV), kC, ks), desc_kmajor(S(GS::INV), kC, ks), i64, ks > 0);
+            mma_commit(&bars[2]);
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 44, fail)) break;
+        mph ^= 1;
+        tc_fence_after();
+        {
+            float x[16];
+            tmem_ld16(tmem + lb + 128 + 16 * cq, x);
+            tmem_ld_wait();
+            if (rv)
+                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+        }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {  // phase D: dAkk = -INV^T T
+            tc_fence_after();
+            const uint32_t id = idesc_neg_a(idesc_bf16(64, 64, true, true));
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), id, ks > 0);
+            mma_commit(&bars[2]);
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 45, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && has_next) issue_d(*nx, nbar);  // INV is consumed
+        tc_fence_after();
+        {  // epilogue D: dbeta (Akk part), dM row segments
+            const float br = rv ? sbeta[rrow] : 0.f;
+            float a[16], m[16];
+            float db = 0.f;
+            tmem_ld16(tmem + lb + 320 + 16 * cq, a);
+            tmem_ld16(tmem + lb + 192 + 16 * cq, m);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int j = 16 * cq + u;
+                const bool in = j < rrow && rrow < c;
+                db = in ? fmaf(a[u], m[u], db) : db;
+                a[u] = in ? br * a[u] : 0.f;
+            }
+            if (rv) {
+                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DM, rrow, 16 * cq + 8 * u, kC, a + 8 * u);
+                xdb[256 + cq * 64 + rrow] = db;
+            }
+        }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid < kC && tid < c)
+            db_out[(r0 + tid) * HV + hv] =
+                __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
+                                    ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
+        if (tid == 0) {  // phase E
+            tc_fence_after();
+            const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+            mma_commit(&bars[2]);
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 46, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && has_next) issue_e(*nx, nbar, slot ^ 1);  // factor tiles, dN, dM, dINV, T are consumed
+        tc_fence_after();
+        {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
+            float dG[16];
+            float dGC = 0.f;
+            const float sc = p.scale;
+#pragma unroll
+            for (int rb = 0; rb < 2; ++rb) {
+                const uint32_t cb = (uint32_t)(16 * qtr + 8 * rb);
+                float aQt[8], aKh[8], aKr[8], aKc[8], aQr[8], aXk[8];
+                uint32_t kq[8];
+                tmem_ld8(tmem + lb + 0 + cb, aQt);
+                tmem_ld8(tmem + lb + 64 + cb, aKh);
+                tmem_ld8(tmem + lb + 128 + cb, aKr);
+                tmem_ld8(tmem + lb + 192 + cb, aKc);
+                tmem_ld8(tmem + lb + 256 + cb, aQr);
+                tmem_ld8(tmem + lb + 448 + cb, aXk);
+                tmem_ld8u(tmem + lb + 384 + cb, kq);
+                tmem_ld_wait();
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    const int ii = 8 * rb + x, r = 16 * qtr + ii;
+                    const bool in = r < c;
+                    const float kv = __uint_as_float(kq[x] << 16), qv = __uint_as_float(kq[x] & 0xffff0000u);
+                    const float gm = G2[ii];
+                    const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
+                    const float b = sbeta[r];
+                    const float dQt = sc * aQt[x], bX = b * aXk[x];
+                    const float dqv = dQt * E + aQr[x] * ep;
+                    const float dkv = aKh[x] * eh + bX * E + aKr[x] * ep + aKc[x] * em;
+                    const float khk = aKh[x] * kv * eh;
+                    // The factor values of the dGamma pair terms are the bf16 values the MMAs used, so that
+                    // each in-chunk pair's contributions to its two rows cancel in the chunk sum as they do
+                    // exactly.
+                    const float kt_b = bfr(kv * E), qr_b = bfr(qv * ep), kr_b = bfr(kv * ep), kc_b = bfr(kv * em);
+                    const float dgv =
+                        dQt * qv * E - khk + bX * kt_b + aQr[x] * qr_b + aKr[x] * kr_b - aKc[x] * kc_b;
+                    dG[ii] = in ? dgv : 0.f;
+                    if (in) {
+                        dGC += khk;
+                        if (G == 1) {
+                            const int64_t o = ((r0 + r) * H + h) * D + d;
+                            st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o),
+                                         reinterpret_cast<uint8_t*>(dk_out + o), dqv, dkv);
+                        } else {
+                            const int64_t o = ((r0 + r) * HV + hv) * D + d;
+                            ws.dqp[o] = dqv;
+                            ws.dkp[o] = dkv;
+                        }
+                    }
+                }
+            }
+            xgc[qtr * 128 + d] = dGC;
+            __syncthreads();
+            const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
+                               ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
+#pragma unroll
+            for (int x = 0; x < 16; ++x)
+                if (16 * qtr + x == c - 1) dG[x] += dGCt;
+            float run = 0.f;
+#pragma unroll
+            for (int x = 15; x >= 0; --x) {
+                run += dG[x];
+                dG[x] = run;
+            }
+            xt1[qtr * 128 + d] = run;
+            __syncthreads();
+            float carry = 0.f;  // later quarters' totals, added in the order 3, 2, 1
+            for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
+#pragma unroll
+            for (int x = 0; x < 16; ++x) {
+                const int r = 16 * qtr + x;
+                if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = dG[x] + carry;
+            }
+        }
+        if (tid < kC) reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nbeta;
+        const Item nc = *nx;
+        tc_fence_before();
+        __syncthreads();  // the next item's scratch and TMEM accumulators are reused from here
+        tc_fence_after();
+        cur = nc;
     }
-cleanup:
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 512);
@@ -450,10 +545,16 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
     if (!make_tmap_bf16_3d(&m.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
         !make_tmap_bf16_3d(&m.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
         !make_tmap_bf16_3d(&m.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC))
+        !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
+        !make_tmap_f32_3d(&m.g, io.g, D, p.HV, rows, D * 4, (uint64_t)p.HV * D * 4, D, 1, kC))
         return cudaErrorInvalidValue;
-    k_tc_grads<<<dim3((unsigned)p.NT, p.HV), 512, kGradsSmem, st>>>(
-        p, io.g, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t items = p.NT * p.HV;  // persistent: one CTA per SM, items dealt round-robin
+    const unsigned grid = (unsigned)(items < nsm ? items : nsm);
+    k_tc_grads<<<grid, 512, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv,
+                                               io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
     if (p.HV != p.H) {
         k_tc_gva_reduce<<<1024, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq, (bf16*)io.dk);
