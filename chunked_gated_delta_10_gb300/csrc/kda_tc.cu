@@ -124,16 +124,19 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 }
 
 // ---------------------------------------------------------------------------
-// tc_intra: 256 threads (two per key channel: rows 0..31 and 32..63); inputs
-// staged by TMA and transformed in place (q -> scale Q~, k -> K^, v -> beta V).
-// 112 KB of shared memory, two CTAs per SM.
+// tc_intra: persistent, two 256-thread CTAs per SM (two threads per key channel:
+// rows 0..31 and 32..63), each walking its (chunk, value head) items round-robin.
+// Inputs staged by TMA and transformed in place (q -> scale Q~, k -> K^,
+// v -> beta V). The next item's q and k are fetched once the K^ / Q~ copies have
+// read their tiles, its v once the second MMA has consumed beta V, and its g
+// (registers) and beta while the current item finishes. 112 KB of shared memory.
 // ---------------------------------------------------------------------------
 struct IS {
     static constexpr int Q = 0, K = TCD, V = 2 * TCD, KQ = 3 * TCD, KC = 5 * TCD, XK = 6 * TCD, MISC = 7 * TCD;
     // aliases: after the first MMA, KQ holds Akk / INV in fp32; after the last, W and U staging.
     // after the first MMA, KC holds the bf16 INV tile and the inversion scratch.
     static constexpr int AKK = KQ, FI = KQ + 16384, TINV = KC, XS = KC + TCC, WST = KQ, UST = KQ + TCD;
-    static constexpr int END = MISC + 256 + 64;
+    static constexpr int END = MISC + 512 + 64;  // beta (two item slots), barriers
 };
 constexpr int kIntraSmem = IS::END;
 
@@ -145,160 +148,205 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                                                       const bf16* __restrict__ beta, TcWs ws,
                                                       const __grid_constant__ IntraMaps maps) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    float* sb = reinterpret_cast<float*>(sm + IS::MISC);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + IS::MISC + 256);  // [0] loads, [1] mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + IS::MISC + 512);  // [0, 1] inputs (by item parity), [2] mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
     float* Akk = reinterpret_cast<float*>(sm + IS::AKK);
     float* Fi = reinterpret_cast<float*>(sm + IS::FI);
-    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // phase-0 scratch (6 x 128 floats)
+    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // item-start scratch (6 x 128 floats)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = tid & 127, half = tid >> 7;
-    const int HV = p.HV, H = p.H, hv = blockIdx.y, h = hv / (HV / H);
-    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
-    int64_t r0;
-    int c;
-    chunk_rows(p, gc, r0, c);
-    float G2[32];  // g of channel d, this thread's 32 rows; Gamma2 after the cumsum below
-    load_g_quarters<2>(g, r0, c, HV, hv, d, 2 * half, G2);
+    const int HV = p.HV, H = p.H, G = HV / H;
+    const int64_t total = p.NT * HV;
     if (tid == 0) {
         *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
         if (*fail) *(volatile int*)ws.status = 10;
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        mbar_init(&bars[0], 2);
+        mbar_init(&bars[1], 2);
+        mbar_init(&bars[2], 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(tslot, 256);
-    if (tid < kC) sb[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + hv]) : 0.f;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (tid == 0 && *fail == 0) {
-        mbar_expect_tx(&bars[0], 3 * TCD);
-        for (int b = 0; b < 2; ++b) {
-            tma_load_3d(sm + IS::Q + b * (TCD / 2), &maps.q, 64 * b, h, (int)r0, &bars[0]);
-            tma_load_3d(sm + IS::K + b * (TCD / 2), &maps.k, 64 * b, h, (int)r0, &bars[0]);
-            tma_load_3d(sm + IS::V + b * (TCD / 2), &maps.v, 64 * b, hv, (int)r0, &bars[0]);
-        }
-    }
-    const ColAddr a64(d, kC), a128(d, 128);  // this thread's column in the 64- and 128-row tiles
-    quarter_cumsum_log2<2>(G2, d, 2 * half, tmp, G2);
-    // reference row (middle of the chunk, always in rows 0..31) and last valid row
-    const int rmid = (c - 1) >> 1;
-    if (half == 0) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-            if (i == rmid) tmp[512 + d] = G2[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-        if (32 * half + i == c - 1) tmp[640 + d] = G2[i];
-    __syncthreads();
-    const float ref = tmp[512 + d], gC = tmp[640 + d];
-    if (half == 0) ws.egc[ch * D + d] = exp2f(gC);
-    if (!wait_all(&bars[0], 0, ws.status, 11, fail)) goto cleanup;
-    // decayed factors; in place: q -> scale Q~, k -> K^, v -> beta V
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int r = 32 * half + i;
-        const bool in = r < c;
-        const float kv = in ? ld_col(sm + IS::K, a64, r) : 0.f;
-        const float qv = in ? ld_col(sm + IS::Q, a64, r) : 0.f;
-        const float vv = in ? ld_col(sm + IS::V, a64, r) : 0.f;
-        const float b = sb[r], gm = G2[i];
-        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = fast_exp2(gm), eh = fast_exp2(gC - gm);
-        const uint32_t o = a64.at(r);
-        st_bf16_pair(sm + IS::KQ + a128.at(r), sm + IS::KQ + a128.at(kC + r), kv * ep, qv * ep);
-        st_bf16_pair(sm + IS::KC + o, sm + IS::XK + o, kv * em, b * kv * E);
-        st_bf16_pair(sm + IS::V + o, sm + IS::K + o, b * vv, kv * eh);
-        st_col(sm + IS::Q, a64, r, p.scale * qv * E);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-        const uint32_t id = idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, desc_kmajor(smem_u32(sm + IS::KQ), 128, ks), desc_kmajor(smem_u32(sm + IS::KC), kC, ks), id,
-                     ks > 0);
-        mma_commit(&bars[1]);
-        bulk_store(ws.kh + ch * TCD, sm + IS::K, TCD);
-        bulk_store(ws.qs + ch * TCD, sm + IS::Q, TCD);
-        bulk_commit();
-    }
-    if (!wait_all(&bars[1], 0, ws.status, 12, fail)) goto cleanup;
-    tc_fence_after();
-    {  // Akk (rows 0..63) and Aqk (rows 64..127): lane row 32 * (warp % 4) + lane, 32 columns per warp half
-        const int R = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
-        float row[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0, row);
-        tmem_ld_wait();
-        if (R < kC) {
-            const int r = R;
-            for (int j = 0; j < 32; ++j) Akk[lsk(r, c0 + j)] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
-        } else {
-            const int r = R - kC;
-            uint8_t* gA = ws.aqk + ch * TCC;
-            for (int u = 0; u < 32; u += 8) {
-                float x[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) x[t] = (c0 + u + t <= r) ? p.scale * row[u + t] : 0.f;
-                uint4 vv;
-                vv.x = pack2(x[0], x[1]);
-                vv.y = pack2(x[2], x[3]);
-                vv.z = pack2(x[4], x[5]);
-                vv.w = pack2(x[6], x[7]);
-                *reinterpret_cast<uint4*>(gA + tile_off(r, c0 + u, kC)) = vv;
+    if (*(volatile int*)fail) goto cleanup;
+    {
+        const ColAddr a64(d, kC), a128(d, 128);  // this thread's column in the 64- and 128-row tiles
+        auto issue_qk = [&](int64_t r0, int h, uint64_t* b) {
+            mbar_expect_tx(b, 2 * TCD);
+            for (int x = 0; x < 2; ++x) {
+                tma_load_3d(sm + IS::Q + x * (TCD / 2), &maps.q, 64 * x, h, (int)r0, b);
+                tma_load_3d(sm + IS::K + x * (TCD / 2), &maps.k, 64 * x, h, (int)r0, b);
             }
+        };
+        auto issue_v = [&](int64_t r0, int hv, uint64_t* b) {
+            mbar_expect_tx(b, TCD);
+            for (int x = 0; x < 2; ++x) tma_load_3d(sm + IS::V + x * (TCD / 2), &maps.v, 64 * x, hv, (int)r0, b);
+        };
+        int64_t w = blockIdx.x;
+        int64_t r0;
+        int c;
+        chunk_rows(p, w / HV, r0, c);
+        float G2[32];  // g of channel d, this thread's 32 rows (the next item's during the item's last phase)
+        load_g_quarters<2>(g, r0, c, HV, (int)(w % HV), d, 2 * half, G2);
+        if (tid < kC) {
+            float* sb0 = reinterpret_cast<float*>(sm + IS::MISC);
+            sb0[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + (int)(w % HV)]) : 0.f;
         }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
-    for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
-        const int r = e >> 3, c0 = (e & 7) * 8;
-        st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
-    }
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, true, false);
-        const uint32_t ti = smem_u32(sm + IS::TINV);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 64, desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), desc_kmajor(ti, kC, ks), id, ks > 0);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + IS::V), kC, ks), desc_kmajor(ti, kC, ks), id, ks > 0);
-        mma_commit(&bars[1]);
-        bulk_store(ws.inv + ch * TCC, sm + IS::TINV, TCC);
-        bulk_commit();
-    }
-    if (!wait_all(&bars[1], 1, ws.status, 13, fail)) goto cleanup;
-    tc_fence_after();
-    {  // w^T, u^T: lane = channel 32 * (warp % 4) + lane, 32 chunk rows per warp half
-        const int dd = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
-        const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-        float col[32];
-        tmem_ld32(tmem + lb + 64 + c0, col);
-        tmem_ld_wait();
-        const ColAddr ad(dd, kC);
+        if (tid == 0) {
+            issue_qk(r0, (int)(w % HV) / G, &bars[0]);
+            issue_v(r0, (int)(w % HV), &bars[0]);
+        }
+        uint32_t mph = 0;
+        for (int i = 0; w < total; ++i, w += gridDim.x) {
+            const int slot = i & 1;
+            const int64_t ch = w;
+            chunk_rows(p, w / HV, r0, c);
+            const int64_t wn = w + gridDim.x;
+            const bool has_next = wn < total;
+            const int hvn = (int)(wn % HV);
+            int64_t r0n = r0;
+            int cn = c;
+            if (has_next) chunk_rows(p, wn / HV, r0n, cn);
+            const float* sb = reinterpret_cast<const float*>(sm + IS::MISC + 256 * slot);
+
+            quarter_cumsum_log2<2>(G2, d, 2 * half, tmp, G2);
+            // reference row (middle of the chunk, always in rows 0..31) and last valid row
+            const int rmid = (c - 1) >> 1;
+            if (half == 0) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::WST, ad, c0 + j, col[j], col[j + 1]);
-        tmem_ld32(tmem + lb + 128 + c0, col);
-        tmem_ld_wait();
+                for (int x = 0; x < 32; ++x)
+                    if (x == rmid) tmp[512 + d] = G2[x];
+            }
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::UST, ad, c0 + j, col[j], col[j + 1]);
-    }
-    tc_fence_before();
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
-        bulk_store(ws.u + ch * TCD, sm + IS::UST, TCD);
-        bulk_commit();
+            for (int x = 0; x < 32; ++x)
+                if (32 * half + x == c - 1) tmp[640 + d] = G2[x];
+            __syncthreads();
+            const float ref = tmp[512 + d], gC = tmp[640 + d];
+            if (half == 0) ws.egc[ch * D + d] = exp2f(gC);
+            if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
+            // decayed factors; in place: q -> scale Q~, k -> K^, v -> beta V
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+                const int r = 32 * half + x;
+                const bool in = r < c;
+                const float kv = in ? ld_col(sm + IS::K, a64, r) : 0.f;
+                const float qv = in ? ld_col(sm + IS::Q, a64, r) : 0.f;
+                const float vv = in ? ld_col(sm + IS::V, a64, r) : 0.f;
+                const float b = sb[r], gm = G2[x];
+                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = fast_exp2(gm),
+                            eh = fast_exp2(gC - gm);
+                const uint32_t o = a64.at(r);
+                st_bf16_pair(sm + IS::KQ + a128.at(r), sm + IS::KQ + a128.at(kC + r), kv * ep, qv * ep);
+                st_bf16_pair(sm + IS::KC + o, sm + IS::XK + o, kv * em, b * kv * E);
+                st_bf16_pair(sm + IS::V + o, sm + IS::K + o, b * vv, kv * eh);
+                st_col(sm + IS::Q, a64, r, p.scale * qv * E);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (tid == 0) {
+                const uint32_t id = idesc_bf16(128, 64, false, false);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16(tmem, desc_kmajor(smem_u32(sm + IS::KQ), 128, ks),
+                             desc_kmajor(smem_u32(sm + IS::KC), kC, ks), id, ks > 0);
+                mma_commit(&bars[2]);
+                bulk_store(ws.kh + ch * TCD, sm + IS::K, TCD);
+                bulk_store(ws.qs + ch * TCD, sm + IS::Q, TCD);
+                bulk_commit();
+            }
+            // beta of the next item: loaded now, stored to its shared slot at the end of this item
+            const float nbeta =
+                (has_next && tid < cn) ? __bfloat162float(beta[(r0n + tid) * HV + hvn]) : 0.f;
+            if (!wait_all(&bars[2], mph, ws.status, 12, fail)) break;
+            mph ^= 1;
+            if (tid == 0 && has_next) {
+                bulk_wait_read();  // the K^ and scale Q~ copies have read their tiles
+                issue_qk(r0n, hvn / G, &bars[slot ^ 1]);
+            }
+            tc_fence_after();
+            {  // Akk (rows 0..63) and Aqk (rows 64..127): lane row 32 * (warp % 4) + lane, 32 columns per warp half
+                const int R = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+                float row[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0, row);
+                tmem_ld_wait();
+                if (R < kC) {
+                    const int r = R;
+                    for (int j = 0; j < 32; ++j) Akk[lsk(r, c0 + j)] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
+                } else {
+                    const int r = R - kC;
+                    uint8_t* gA = ws.aqk + ch * TCC;
+                    for (int u = 0; u < 32; u += 8) {
+                        float xx[8];
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) xx[t] = (c0 + u + t <= r) ? p.scale * row[u + t] : 0.f;
+                        uint4 vv;
+                        vv.x = pack2(xx[0], xx[1]);
+                        vv.y = pack2(xx[2], xx[3]);
+                        vv.z = pack2(xx[4], xx[5]);
+                        vv.w = pack2(xx[6], xx[7]);
+                        *reinterpret_cast<uint4*>(gA + tile_off(r, c0 + u, kC)) = vv;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();
+            tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
+            for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
+                const int r = e >> 3, c0 = (e & 7) * 8;
+                st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
+            }
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, true, false);
+                const uint32_t ti = smem_u32(sm + IS::TINV);
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem + 64, desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), desc_kmajor(ti, kC, ks), id,
+                             ks > 0);
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + IS::V), kC, ks), desc_kmajor(ti, kC, ks), id,
+                             ks > 0);
+                mma_commit(&bars[2]);
+                bulk_store(ws.inv + ch * TCC, sm + IS::TINV, TCC);
+                bulk_commit();
+            }
+            if (!wait_all(&bars[2], mph, ws.status, 13, fail)) break;
+            mph ^= 1;
+            if (tid == 0 && has_next) issue_v(r0n, hvn, &bars[slot ^ 1]);  // beta V is consumed
+            if (has_next) load_g_quarters<2>(g, r0n, cn, HV, hvn, d, 2 * half, G2);
+            tc_fence_after();
+            {  // w^T, u^T: lane = channel 32 * (warp % 4) + lane, 32 chunk rows per warp half
+                const int dd = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+                const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
+                float col[32];
+                tmem_ld32(tmem + lb + 64 + c0, col);
+                tmem_ld_wait();
+                const ColAddr ad(dd, kC);
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::WST, ad, c0 + j, col[j], col[j + 1]);
+                tmem_ld32(tmem + lb + 128 + c0, col);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::UST, ad, c0 + j, col[j], col[j + 1]);
+            }
+            if (tid < kC) reinterpret_cast<float*>(sm + IS::MISC + 256 * (slot ^ 1))[tid] = nbeta;
+            tc_fence_before();
+            fence_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
+                bulk_store(ws.u + ch * TCD, sm + IS::UST, TCD);
+                bulk_commit();
+                bulk_wait_read();  // the scratch and INV areas are rewritten by the next item
+            }
+            __syncthreads();
+        }
     }
 cleanup:
     if (tid == 0) bulk_wait_all();
@@ -649,7 +697,12 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
             !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
             !make_tmap_bf16_3d(&im.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC))
             return cudaErrorInvalidValue;
-        k_tc_intra<<<dim3((unsigned)p.NT, p.HV), 256, kIntraSmem, st>>>(p, io.g, beta, ws, im);
+        int dev = 0, nsm = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        const int64_t items = p.NT * p.HV;  // persistent: two CTAs per SM, items dealt round-robin
+        const unsigned grid = (unsigned)(items < 2 * (int64_t)nsm ? items : 2 * (int64_t)nsm);
+        k_tc_intra<<<grid, 256, kIntraSmem, st>>>(p, io.g, beta, ws, im);
         note_launch("tc_intra", st);
     }
     if (stages >= 2) {
