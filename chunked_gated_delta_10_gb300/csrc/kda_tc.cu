@@ -54,7 +54,7 @@ __device__ __forceinline__ int lsk(int r, int m) { return r * kC + ((m + r) & (k
 
 __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < kC * kC; i += nth) Out[i] = 0.f;
+    for (int i = tid; i < kC * kC / 4; i += nth) reinterpret_cast<float4*>(Out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
     if (warp < 4 && lane < 16) {
         // diagonal 16 x 16 block `warp`, column j = lane, right-looking: once x[m] is
@@ -74,20 +74,31 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     }
     __syncthreads();
     // 16 -> 32: blocks (1,0) and (3,2). X = L21 D0 (D0 lower triangular, zeros included), then -D1 X.
-    for (int e = tid; e < 512; e += nth) {
-        const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
-        float s = 0.f;
+    // Each thread forms a 1 x 2 strip (256 strips per product).
+    for (int e = tid; e < 256; e += nth) {
+        const int pr = e >> 7, base = 32 * pr, a = (e >> 3) & 15, c = 2 * (e & 7);
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) s = fmaf(L[lsk(base + 16 + a, base + m)], Out[(base + m) * kC + base + c], s);
-        X[e] = s;
+        for (int m = 0; m < 16; ++m) {
+            const float l = L[lsk(base + 16 + a, base + m)];
+            const float2 o = *reinterpret_cast<const float2*>(Out + (base + m) * kC + base + c);
+            s0 = fmaf(l, o.x, s0);
+            s1 = fmaf(l, o.y, s1);
+        }
+        *reinterpret_cast<float2*>(X + pr * 256 + a * 16 + c) = make_float2(s0, s1);
     }
     __syncthreads();
-    for (int e = tid; e < 512; e += nth) {
-        const int pr = e >> 8, base = 32 * pr, a = (e >> 4) & 15, c = e & 15;
-        float s = 0.f;
+    for (int e = tid; e < 256; e += nth) {
+        const int pr = e >> 7, base = 32 * pr, a = (e >> 3) & 15, c = 2 * (e & 7);
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) s = fmaf(Out[(base + 16 + a) * kC + base + 16 + m], X[pr * 256 + m * 16 + c], s);
-        Out[(base + 16 + a) * kC + base + c] = -s;
+        for (int m = 0; m < 16; ++m) {
+            const float l = Out[(base + 16 + a) * kC + base + 16 + m];
+            const float2 xv = *reinterpret_cast<const float2*>(X + pr * 256 + m * 16 + c);
+            s0 = fmaf(l, xv.x, s0);
+            s1 = fmaf(l, xv.y, s1);
+        }
+        *reinterpret_cast<float2*>(Out + (base + 16 + a) * kC + base + c) = make_float2(-s0, -s1);
     }
     __syncthreads();
     // 32 -> 64: rows 32..63, columns 0..31; each thread a 1 x 4 strip (4 independent sums)
@@ -156,7 +167,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // item-start scratch (6 x 128 floats)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = tid & 127, half = tid >> 7;
+    const int d0 = 2 * (tid & 63), qt = tid >> 6;  // key channels d0, d0 + 1; chunk rows 16 qt .. +15
     const int HV = p.HV, H = p.H, G = HV / H;
     const int64_t total = p.NT * HV;
     if (tid == 0) {
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     const uint32_t tmem = *tslot;
     if (*(volatile int*)fail) goto cleanup;
     {
-        const ColAddr a64(d, kC), a128(d, 128);  // this thread's column in the 64- and 128-row tiles
+        const ColAddr a64(d0, kC), a128(d0, 128);  // this thread's channel pair in the 64- and 128-row tiles
         auto issue_qk = [&](int64_t r0, int h, uint64_t* b) {
             mbar_expect_tx(b, 2 * TCD);
             for (int x = 0; x < 2; ++x) {
@@ -190,8 +201,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         int64_t r0;
         int c;
         chunk_rows(p, w / HV, r0, c);
-        float G2[32];  // g of channel d, this thread's 32 rows (the next item's during the item's last phase)
-        load_g_quarters<2>(g, r0, c, HV, (int)(w % HV), d, 2 * half, G2);
+        float G2[32];  // g of channels d0 + ch, rows 16 qt + i at [16 ch + i] (the next item's during the last phase)
+        load_g_pair(g, r0, c, HV, (int)(w % HV), d0, qt, G2);
         if (tid < kC) {
             float* sb0 = reinterpret_cast<float*>(sm + IS::MISC);
             sb0[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + (int)(w % HV)]) : 0.f;
@@ -213,37 +224,48 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             if (has_next) chunk_rows(p, wn / HV, r0n, cn);
             const float* sb = reinterpret_cast<const float*>(sm + IS::MISC + 256 * slot);
 
-            quarter_cumsum_log2<2>(G2, d, 2 * half, tmp, G2);
-            // reference row (middle of the chunk, always in rows 0..31) and last valid row
+            pair_cumsum_log2(G2, d0, qt, tmp);
+            // reference row (middle of the chunk) and last valid row
             const int rmid = (c - 1) >> 1;
-            if (half == 0) {
 #pragma unroll
-                for (int x = 0; x < 32; ++x)
-                    if (x == rmid) tmp[512 + d] = G2[x];
+            for (int x = 0; x < 16; ++x) {
+                if (16 * qt + x == rmid) {
+                    tmp[512 + d0] = G2[x];
+                    tmp[512 + d0 + 1] = G2[16 + x];
+                }
+                if (16 * qt + x == c - 1) {
+                    tmp[640 + d0] = G2[x];
+                    tmp[640 + d0 + 1] = G2[16 + x];
+                }
             }
-#pragma unroll
-            for (int x = 0; x < 32; ++x)
-                if (32 * half + x == c - 1) tmp[640 + d] = G2[x];
             __syncthreads();
-            const float ref = tmp[512 + d], gC = tmp[640 + d];
-            if (half == 0) ws.egc[ch * D + d] = exp2f(gC);
+            const float ref0 = tmp[512 + d0], ref1 = tmp[512 + d0 + 1], gC0 = tmp[640 + d0], gC1 = tmp[640 + d0 + 1];
+            if (qt == 0) *reinterpret_cast<float2*>(ws.egc + ch * D + d0) = make_float2(exp2f(gC0), exp2f(gC1));
             if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
-            // decayed factors; in place: q -> scale Q~, k -> K^, v -> beta V
+            // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^, v -> beta V
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-                const int r = 32 * half + x;
+            for (int x = 0; x < 16; ++x) {
+                const int r = 16 * qt + x;
                 const bool in = r < c;
-                const float kv = in ? ld_col(sm + IS::K, a64, r) : 0.f;
-                const float qv = in ? ld_col(sm + IS::Q, a64, r) : 0.f;
-                const float vv = in ? ld_col(sm + IS::V, a64, r) : 0.f;
-                const float b = sb[r], gm = G2[x];
-                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = fast_exp2(gm),
-                            eh = fast_exp2(gC - gm);
                 const uint32_t o = a64.at(r);
-                st_bf16_pair(sm + IS::KQ + a128.at(r), sm + IS::KQ + a128.at(kC + r), kv * ep, qv * ep);
-                st_bf16_pair(sm + IS::KC + o, sm + IS::XK + o, kv * em, b * kv * E);
-                st_bf16_pair(sm + IS::V + o, sm + IS::K + o, b * vv, kv * eh);
-                st_col(sm + IS::Q, a64, r, p.scale * qv * E);
+                const uint32_t k2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::K + o) : 0u;
+                const uint32_t q2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::Q + o) : 0u;
+                const uint32_t v2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::V + o) : 0u;
+                const float k0 = __uint_as_float(k2 << 16), k1 = __uint_as_float(k2 & 0xffff0000u);
+                const float q0 = __uint_as_float(q2 << 16), q1 = __uint_as_float(q2 & 0xffff0000u);
+                const float v0 = __uint_as_float(v2 << 16), v1 = __uint_as_float(v2 & 0xffff0000u);
+                const float b = sb[r], gm0 = G2[x], gm1 = G2[16 + x];
+                const float ep0 = fast_exp2(gm0 - ref0), em0 = fast_exp2(ref0 - gm0), E0 = fast_exp2(gm0),
+                            eh0 = fast_exp2(gC0 - gm0);
+                const float ep1 = fast_exp2(gm1 - ref1), em1 = fast_exp2(ref1 - gm1), E1 = fast_exp2(gm1),
+                            eh1 = fast_exp2(gC1 - gm1);
+                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(k0 * ep0, k1 * ep1);
+                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(q0 * ep0, q1 * ep1);
+                *reinterpret_cast<uint32_t*>(sm + IS::KC + o) = pack2(k0 * em0, k1 * em1);
+                *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(b * k0 * E0, b * k1 * E1);
+                *reinterpret_cast<uint32_t*>(sm + IS::V + o) = pack2(b * v0, b * v1);
+                *reinterpret_cast<uint32_t*>(sm + IS::K + o) = pack2(k0 * eh0, k1 * eh1);
+                *reinterpret_cast<uint32_t*>(sm + IS::Q + o) = pack2(p.scale * q0 * E0, p.scale * q1 * E1);
             }
             fence_async_smem();
             tc_fence_before();
@@ -304,13 +326,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t id = idesc_bf16(128, 64, true, false);
+                // w = INV (beta K~), u = INV (beta V): chunk rows on TMEM lanes (M = 64, N = 128)
+                const uint32_t id = idesc_bf16(64, 128, false, true);
                 const uint32_t ti = smem_u32(sm + IS::TINV);
                 for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_bf16(tmem + 64, desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), desc_kmajor(ti, kC, ks), id,
-                             ks > 0);
+                    mma_bf16(tmem, desc_kmajor(ti, kC, ks), desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), id, ks > 0);
                 for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + IS::V), kC, ks), desc_kmajor(ti, kC, ks), id,
+                    mma_bf16(tmem + 128, desc_kmajor(ti, kC, ks), desc_mnmajor(smem_u32(sm + IS::V), kC, ks), id,
                              ks > 0);
                 mma_commit(&bars[2]);
                 bulk_store(ws.inv + ch * TCC, sm + IS::TINV, TCC);
@@ -319,21 +341,23 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             if (!wait_all(&bars[2], mph, ws.status, 13, fail)) break;
             mph ^= 1;
             if (tid == 0 && has_next) issue_v(r0n, hvn, &bars[slot ^ 1]);  // beta V is consumed
-            if (has_next) load_g_quarters<2>(g, r0n, cn, HV, hvn, d, 2 * half, G2);
+            if (has_next) load_g_pair(g, r0n, cn, HV, hvn, d0, qt, G2);
             tc_fence_after();
-            {  // w^T, u^T: lane = channel 32 * (warp % 4) + lane, 32 chunk rows per warp half
-                const int dd = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+            {  // w, u rows: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+                const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
                 const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
-                float col[32];
-                tmem_ld32(tmem + lb + 64 + c0, col);
-                tmem_ld_wait();
-                const ColAddr ad(dd, kC);
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::WST, ad, c0 + j, col[j], col[j + 1]);
-                tmem_ld32(tmem + lb + 128 + c0, col);
-                tmem_ld_wait();
+                for (int t = 0; t < 4; ++t) {
+                    const int col = 32 * (t & 1) + cb;
+                    float x[32];
+                    tmem_ld32(tmem + lb + 128 * (t >> 1) + col, x);
+                    tmem_ld_wait();
+                    if (lane < 16) {
+                        uint8_t* dst = sm + ((t >> 1) ? IS::UST : IS::WST);
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) st_col_pair(sm + IS::UST, ad, c0 + j, col[j], col[j + 1]);
+                        for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(dst, r, col + c8, kC, x + c8);
+                    }
+                }
             }
             if (tid < kC) reinterpret_cast<float*>(sm + IS::MISC + 256 * (slot ^ 1))[tid] = nbeta;
             tc_fence_before();

@@ -347,5 +347,43 @@ __device__ __forceinline__ void quarter_cumsum_log2(const float (&gv)[16 * NQ], 
     }
 }
 
+// The same canonical order for a thread that owns the key-channel pair d0, d0 + 1
+// (d0 even) over the 16 rows of quarter qt: load_g_pair fetches the gate values into
+// gv[16 * ch + i] (channel d0 + ch, row 16 qt + i; issued early), pair_cumsum_log2
+// turns them into Gamma2 in place. `tot` is 4 x 128 floats of shared scratch;
+// pair_cumsum_log2 contains a __syncthreads().
+__device__ __forceinline__ void load_g_pair(const float* __restrict__ g, int64_t r0, int c, int HV, int hv, int d0,
+                                            int qt, float (&gv)[32]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int r = 16 * qt + i;
+        const float2 x = r < c ? *reinterpret_cast<const float2*>(g + ((r0 + r) * HV + hv) * 128 + d0)
+                               : make_float2(0.f, 0.f);
+        gv[i] = x.x;
+        gv[16 + i] = x.y;
+    }
+}
+__device__ __forceinline__ void pair_cumsum_log2(float (&G2)[32], int d0, int qt, float* tot) {
+    float run[32];
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            acc += G2[16 * ch + i];
+            run[16 * ch + i] = acc;
+        }
+        tot[qt * 128 + d0 + ch] = acc;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+        float off = 0.f;
+        for (int qq = 0; qq < qt; ++qq) off += tot[qq * 128 + d0 + ch];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) G2[16 * ch + i] = (off + run[16 * ch + i]) * 1.4426950408889634f;
+    }
+}
+
 }  // namespace tc
 }  // namespace kda
