@@ -259,10 +259,13 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // Negated-A variant of the __nv_bfloat16 instruction descriptor.
 __host__ __device__ constexpr uint32_t idesc_neg_a(uint32_t id) { return id | (1u << 13); }
 
-// Uniform bounded wait: every thread waits on (bar, parity); if any gives up,
-// *fail becomes nonzero for all after the barrier.
+// Uniform bounded wait on (bar, parity): warp 0 polls the barrier while the other
+// warps park in the CTA barrier (issuing nothing); the barrier then orders the
+// observed completion before every thread's later accesses (callers that read
+// TMEM next add tcgen05.fence::after_thread_sync). If the poll gives up, *fail
+// becomes nonzero for all after the barrier.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* status, int code, int* fail) {
-    if (!mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
+    if (threadIdx.x < 32 && !mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
     __syncthreads();
     return *(volatile int*)fail == 0;
 }
