@@ -47,10 +47,11 @@ struct Layout {
     size_t t_w, t_u, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc;
 };
 
-// The backward of bf16 inputs with K = V = 128 runs on the tensor-core path.
+// bf16 inputs with K = V = 128 run on the tensor-core path (forward and backward).
 bool use_tc(const kda_dims* d, int pass) {
-    // (the state passes put sequences on grid z, which holds at most 65535)
-    return pass == KDA_PASS_BWD && d->dtype == KDA_DTYPE_BF16 && d->K == 128 && d->V == 128 && d->num_seqs <= 65535;
+    // (the state passes put sequences on grid y, which holds at most 65535)
+    return (pass == KDA_PASS_BWD || pass == KDA_PASS_FWD) && d->dtype == KDA_DTYPE_BF16 && d->K == 128 &&
+           d->V == 128 && d->num_seqs <= 65535;
 }
 
 Layout layout(const Prob& p, int pass, bool tc) {
@@ -72,12 +73,16 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_kh = take(CH * TCD);
         L.t_qs = take(CH * TCD);
         L.t_vn = take(CH * TCD);
-        L.t_dvn = take(CH * TCD);
         L.t_aqk = take(CH * TCC);
         L.t_inv = take(CH * TCC);
         L.t_sin = take(CH * TDD);
-        L.t_dso = take(CH * TDD);
         L.t_egc = take(CH * 128 * f);
+        if (pass == KDA_PASS_FWD) {  // the forward needs no gradient regions
+            L.total = off;
+            return L;
+        }
+        L.t_dvn = take(CH * TCD);
+        L.t_dso = take(CH * TDD);
         if (p.HV != p.H) {
             L.dqp = take(R * HV * K * f);
             L.dkp = take(R * HV * K * f);
@@ -140,7 +145,7 @@ TcWs carve_tc(void* base, const Layout& L) {
     char* b = (char*)base;
     TcWs w;
     memset(&w, 0, sizeof(w));
-    auto at = [&](size_t off) { return (uint8_t*)(b + off); };
+    auto at = [&](size_t off) { return off ? (uint8_t*)(b + off) : nullptr; };  // 0: region absent
     w.status = (int*)(b + L.status);
     w.w = at(L.t_w);
     w.u = at(L.t_u);
@@ -278,17 +283,19 @@ extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const v
     if ((size_t)dims->B * dims->T > 0 && !o) return KDA_ERR_INVALID_ARG;
     for (const void* x : {(const void*)o, (const void*)ht, (const void*)states})
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
-    const Layout L = layout(p, KDA_PASS_FWD, false);
-    Ws w = carve(ws, L);
+    const Layout L = layout(p, KDA_PASS_FWD, use_tc(dims, KDA_PASS_FWD));
     cudaStream_t st = (cudaStream_t)stream;
     IO io;
     memset(&io, 0, sizeof(io));
     io.q = q; io.k = k; io.v = v; io.beta = beta; io.g = g; io.h0 = h0;
     io.o = o; io.ht = ht; io.states_out = states;
-    cudaError_t e = cudaMemsetAsync(w.status, 0, kAlign, st);
+    cudaError_t e = cudaMemsetAsync((char*)ws + L.status, 0, kAlign, st);
     if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);
-    e = simt_fwd(p, dims->dtype == KDA_DTYPE_BF16, io, w, st);
+    if (L.tc)
+        e = tc_fwd(p, io, carve_tc(ws, L), st);
+    else
+        e = simt_fwd(p, dims->dtype == KDA_DTYPE_BF16, io, carve(ws, L), st);
     if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
 }
@@ -307,13 +314,13 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
     for (const void* x : {(const void*)d_o, (const void*)dht, (const void*)states, (const void*)dq,
                           (const void*)dk, (const void*)dv, (const void*)dg, (const void*)dbeta, (const void*)dh0})
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
-    if (states) return KDA_ERR_UNSUPPORTED;
     const Layout L = layout(p, KDA_PASS_BWD, use_tc(dims, KDA_PASS_BWD));
+    if (states && !L.tc) return KDA_ERR_UNSUPPORTED;  // saved states are consumed on the tensor-core path
     cudaStream_t st = (cudaStream_t)stream;
     IO io;
     memset(&io, 0, sizeof(io));
     io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht;
-    io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0;
+    io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0; io.states_in = states;
     cudaError_t e = cudaMemsetAsync((char*)ws + L.status, 0, kAlign, st);
     if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);

@@ -14,6 +14,7 @@ struct IO {
     const float *g, *h0, *dht;
     void *o, *dq, *dk, *dv, *dbeta;
     float *ht, *states_out, *dg, *dh0;
+    const float* states_in;  // the forward's saved chunk states (backward), or null
 };
 
 // Workspace carved from the caller's buffer (fp32 unless noted).
@@ -52,8 +53,12 @@ struct TcWs {
 
 // The tensor-core path handles bf16 inputs with K = V = 128.
 bool tc_path_ok(const Prob& p, bool bf16);
+// The tensor-core forward: intra, state pass (ht and the fp32 chunk states
+// when requested), output.
+cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 // Runs the first `stages` stages of the tensor-core backward (1: intra,
-// 2: + state pass, 3: + reverse pass, 4: + gradients).
+// 2: + state pass, or the load of io.states_in, 3: + reverse pass,
+// 4: + gradients).
 cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages);
 // The per-chunk gradient stage (and the grouped-value-head reduction).
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);

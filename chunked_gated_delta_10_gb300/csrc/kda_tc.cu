@@ -393,7 +393,7 @@ struct FwdSm {
 constexpr int kFwdSmem = 1024 + FwdSm::END;
 
 __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
-                                                          TcWs ws) {
+                                                          float* __restrict__ states, TcWs ws) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + FwdSm::S;
@@ -455,6 +455,11 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
+        if (states) {  // the fp32 state entering this chunk, [chunk, HV, K, V]
+            float4* dst = reinterpret_cast<float4*>(states + (ch * D + k) * D + 64 * vh);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        }
         if (!wait_all(&bars[2], ph, ws.status, 21, fail)) break;
         if (tid == 0) {  // delta accumulator = w S (chunk rows on TMEM lanes, M = 64, N = 128)
             tc_fence_after();
@@ -692,6 +697,181 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+// ---------------------------------------------------------------------------
+// tc_state_load: the backward's replacement of tc_state_fwd when the forward's
+// states are given. One CTA per (chunk, value head), 256 threads: S_in (fp32)
+// becomes the bf16 checkpoint tile, and delta = u - w S_in with chunk rows on
+// TMEM lanes; the same arithmetic as tc_state_fwd on the same state values.
+// ---------------------------------------------------------------------------
+struct LoadSm {
+    static constexpr int W = 0, U = TCD, S = 2 * TCD, BARS = S + TDD, END = BARS + 64;
+};
+constexpr int kLoadSmem = 1024 + LoadSm::END;
+
+__global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* __restrict__ states, TcWs ws) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    uint8_t* tS = sm + LoadSm::S;
+    uint8_t* tU = sm + LoadSm::U;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + LoadSm::BARS);  // loads, mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k = tid & 127, vh = tid >> 7;
+    const int64_t ch = (int64_t)blockIdx.x * p.HV + blockIdx.y;
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        *fail = 0;
+        mbar_expect_tx(&bars[0], 2 * TCD);
+        bulk_load(sm + LoadSm::W, ws.w + ch * TCD, TCD, &bars[0]);
+        bulk_load(tU, ws.u + ch * TCD, TCD, &bars[0]);
+    }
+    if (warp == 0) tmem_alloc(tslot, 128);
+    {  // row k, this thread's 64 columns of S_in as bf16
+        const float4* src = reinterpret_cast<const float4*>(states + (ch * D + k) * D + 64 * vh);
+#pragma unroll
+        for (int c8 = 0; c8 < 64; c8 += 8) {
+            const float4 a = src[c8 / 4], b = src[c8 / 4 + 1];
+            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            st_tile_row8(tS, k, 64 * vh + c8, D, x);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (!wait_all(&bars[0], 0, ws.status, 51, fail)) goto cleanup;
+    if (tid == 0) {  // delta accumulator = w S_in (M = 64, N = 128)
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 128, false, true);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + LoadSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
+                     ks > 0);
+        mma_commit(&bars[1]);
+        bulk_store(ws.sin + ch * TDD, tS, TDD);
+        bulk_commit();
+    }
+    if (!wait_all(&bars[1], 0, ws.status, 52, fail)) goto cleanup;
+    tc_fence_after();
+    {  // delta = u - w S_in in place of u: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+        const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
+        const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float acc[32];
+            tmem_ld32(tmem + lq + cb + 32 * h, acc);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) {
+                    float x[8];
+                    ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
+                    st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+                }
+            }
+        }
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(ws.vn + ch * TCD, tU, TCD);
+        bulk_commit();
+    }
+cleanup:
+    if (tid == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+// ---------------------------------------------------------------------------
+// tc_output: the forward output o = scale Q~ S_in + Aqk delta of one (chunk,
+// value head); 128 threads, chunk rows on TMEM lanes (M = 64).
+// ---------------------------------------------------------------------------
+struct OutSm {
+    static constexpr int QS = 0, SIN = TCD, AQK = TCD + TDD, VN = TCD + TDD + TCC, BARS = 2 * TCD + TDD + TCC;
+    static constexpr int END = BARS + 64;
+};
+constexpr int kOutSmem = 1024 + OutSm::END;
+
+__global__ void __launch_bounds__(128, 3) k_tc_output(Prob p, bf16* __restrict__ o, TcWs ws) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OutSm::BARS);  // loads, mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int HV = p.HV, hv = blockIdx.y;
+    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
+    int64_t r0;
+    int c;
+    chunk_rows(p, gc, r0, c);
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        *fail = 0;
+        mbar_expect_tx(&bars[0], 2 * TCD + TDD + TCC);
+        bulk_load(sm + OutSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + OutSm::SIN, ws.sin + ch * TDD, TDD, &bars[0]);
+        bulk_load(sm + OutSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
+        bulk_load(sm + OutSm::VN, ws.vn + ch * TCD, TCD, &bars[0]);
+    }
+    if (warp == 0) tmem_alloc(tslot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (!wait_all(&bars[0], 0, ws.status, 61, fail)) goto cleanup;
+    if (tid == 0) {  // o = (scale Q~) S_in + Aqk delta (M = 64, N = 128)
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 128, false, true);
+        for (int ks = 0; ks < D / 16; ++ks)
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + OutSm::QS), kC, ks), desc_mnmajor(smem_u32(sm + OutSm::SIN), D, ks),
+                     id, ks > 0);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + OutSm::AQK), kC, ks), desc_mnmajor(smem_u32(sm + OutSm::VN), kC, ks),
+                     id, 1);
+        mma_commit(&bars[1]);
+    }
+    if (!wait_all(&bars[1], 0, ws.status, 62, fail)) goto cleanup;
+    tc_fence_after();
+    {  // row r = 16 warp + lane (lane < 16), 128 columns in four groups of 32
+        const int r = 16 * warp + lane;
+        const uint32_t lq = (uint32_t)(32 * warp) << 16;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float x[32];
+            tmem_ld32(tmem + lq + 32 * h, x);
+            tmem_ld_wait();
+            if (lane < 16 && r < c) {
+                bf16* dst = o + ((r0 + r) * HV + hv) * D + 32 * h;
+#pragma unroll
+                for (int u = 0; u < 32; u += 8) {
+                    uint4 vv;
+                    vv.x = pack2(x[u], x[u + 1]);
+                    vv.y = pack2(x[u + 2], x[u + 3]);
+                    vv.z = pack2(x[u + 4], x[u + 5]);
+                    vv.w = pack2(x[u + 6], x[u + 7]);
+                    *reinterpret_cast<uint4*>(dst + u) = vv;
+                }
+            }
+        }
+    }
+cleanup:
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+}
+
+
 template <typename F>
 cudaError_t set_smem(F* f, int bytes) {
     return cudaFuncSetAttribute(reinterpret_cast<const void*>(f), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -701,10 +881,50 @@ cudaError_t set_smem(F* f, int bytes) {
 
 bool tc_path_ok(const Prob& p, bool bf16) { return bf16 && p.K == D && p.V == D; }
 
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages) {
+namespace {
+
+cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
     if ((e = set_smem(k_tc_intra, kIntraSmem)) != cudaSuccess) return e;
+    if (p.NT == 0) return cudaSuccess;
+    const int64_t rows = (int64_t)p.B * p.T;
+    IntraMaps im;
+    memset(&im, 0, sizeof(im));
+    const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
+    if (!make_tmap_bf16_3d(&im.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+        !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
+        !make_tmap_bf16_3d(&im.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC))
+        return cudaErrorInvalidValue;
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t items = p.NT * p.HV;  // persistent: two CTAs per SM, items dealt round-robin
+    const unsigned grid = (unsigned)(items < 2 * (int64_t)nsm ? items : 2 * (int64_t)nsm);
+    k_tc_intra<<<grid, 256, kIntraSmem, st>>>(p, io.g, (const bf16*)io.beta, ws, im);
+    note_launch("tc_intra", st);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
+    cudaError_t e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_output, kOutSmem)) != cudaSuccess) return e;
+    if ((e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
+    k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, io.ht, io.states_out, ws);
+    note_launch("tc_state_fwd", st);
+    if (p.NT > 0) {
+        k_tc_output<<<dim3((unsigned)p.NT, p.HV), 128, kOutSmem, st>>>(p, (bf16*)io.o, ws);
+        note_launch("tc_output", st);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages) {
+    cudaError_t e;
+    if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_ds_rev, kRevSmem)) != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.B * p.T;
     CUtensorMap tm_do;
@@ -712,26 +932,17 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if (rows > 0 && !make_tmap_bf16_3d(&tm_do, io.d_o, D, (uint64_t)p.HV, (uint64_t)rows, (uint64_t)D * 2,
                                        (uint64_t)p.HV * D * 2, 64, 1, kC))
         return cudaErrorInvalidValue;
-    const bf16* beta = (const bf16*)io.beta;
-    if (p.NT > 0 && stages >= 1) {
-        IntraMaps im;
-        memset(&im, 0, sizeof(im));
-        const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
-        if (!make_tmap_bf16_3d(&im.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-            !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-            !make_tmap_bf16_3d(&im.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC))
-            return cudaErrorInvalidValue;
-        int dev = 0, nsm = 0;
-        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-        const int64_t items = p.NT * p.HV;  // persistent: two CTAs per SM, items dealt round-robin
-        const unsigned grid = (unsigned)(items < 2 * (int64_t)nsm ? items : 2 * (int64_t)nsm);
-        k_tc_intra<<<grid, 256, kIntraSmem, st>>>(p, io.g, beta, ws, im);
-        note_launch("tc_intra", st);
-    }
+    if (stages >= 1 && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     if (stages >= 2) {
-        k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, nullptr, ws);
-        note_launch("tc_state_fwd", st);
+        if (io.states_in) {  // the forward's saved states: no sequential recompute
+            if (p.NT > 0) {
+                k_tc_state_load<<<dim3((unsigned)p.NT, p.HV), 256, kLoadSmem, st>>>(p, io.states_in, ws);
+                note_launch("tc_state_load", st);
+            }
+        } else {
+            k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, nullptr, nullptr, ws);
+            note_launch("tc_state_fwd", st);
+        }
     }
     if (stages >= 3) {
         k_tc_ds_rev<<<dim3(p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);

@@ -129,7 +129,10 @@ kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const void* k, con
  *   do: required; dht: nullable (zero).
  *   states: NULL to recompute the forward state pass inside the call (the
  *     default recompute path); or the states saved by kda_chunk_fwd for the
- *     same inputs, which skips the forward state pass.
+ *     same inputs, which replaces the sequential forward state pass by a
+ *     chunk-parallel load (bf16 with K = V = 128 only; KDA_ERR_UNSUPPORTED
+ *     otherwise). With the states of the same build's forward the results
+ *     equal the recompute path's bit for bit.
  *   dh0: nullable; must be NULL when h0 is NULL.
  *   Other arguments as kda_chunk_fwd; ws of at least kda_workspace_bytes(BWD).
  * Errors: as kda_chunk_fwd.

@@ -122,6 +122,64 @@ def test_forward_outputs_and_states(kda, name, dtype):
     assert rel_l2(to64(st), ref["s_in"]) <= tol
 
 
+# Tensor-core forward (bf16, K = V = 128): o, ht and the fp32 chunk states.
+FWD_TC = {
+    "t64": SMALL["t64"],
+    "no_state": SMALL["no_state"],
+    "varlen_gva": dict(B=1, T=0, H=2, HV=4, K=128, V=128, seq_lens=[130, 1, 0, 64, 200]),
+}
+
+
+@pytest.mark.parametrize("name", list(FWD_TC))
+def test_tensor_core_forward(kda, name):
+    inp = kda_inputs.small(seed=35, dtype="bf16", **FWD_TC[name])
+    o, ht, st = gpu_fwd(kda, inp)
+    assert kda.load().kda_launch_name(1) == b"tc_state_fwd"  # the tensor-core path ran
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    tol = _tol(inp)
+    errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
+                states=rel_l2(to64(st), ref["s_in"]))
+    print(name, errs)
+    assert all(e <= tol for e in errs.values()), errs
+
+
+def test_tensor_core_forward_workload(kda):
+    inp = _workload("bf16_b1_t2048_h16_k128")
+    o, ht, st = gpu_fwd(kda, inp)
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
+                states=rel_l2(to64(st), ref["s_in"]))
+    print("bf16_b1_t2048_h16_k128 forward", errs)
+    assert all(e <= _tol(inp) for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("name", ["varlen_gva", "no_state"])
+def test_backward_from_saved_states_is_bitwise_recompute(kda, name):
+    """The backward that loads the forward's chunk states (no sequential state
+    pass) returns exactly what the recompute path returns."""
+    inp = kda_inputs.small(seed=36, dtype="bf16", **FWD_TC[name])
+    _, _, st = gpu_fwd(kda, inp)
+    rec = gpu_bwd(kda, inp)
+    lib = kda.load()
+    names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+    assert b"tc_state_fwd" in names
+    sv = gpu_bwd(kda, inp, states=st)
+    names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+    assert b"tc_state_load" in names and b"tc_state_fwd" not in names, names
+    for key in GRADS:
+        if rec[key] is not None:
+            assert torch.equal(rec[key], sv[key]), key
+    compare_full(inp, sv, oracle.run_inputs(inp))
+
+
+def test_saved_states_off_tensor_core_path_is_unsupported(kda):
+    inp = kda_inputs.small(seed=37, dtype="f32", **SMALL["t65"])
+    _, _, st = gpu_fwd(kda, inp)
+    with pytest.raises(kda.KdaError) as err:
+        gpu_bwd(kda, inp, states=st)
+    assert err.value.code == 2  # KDA_ERR_UNSUPPORTED
+
+
 # ------------------------------------------------------- the five workloads
 
 @functools.lru_cache(maxsize=1)
