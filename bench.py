@@ -6,6 +6,7 @@ bf16 workload B=8, T=4096, H=HV=32, K=V=128, chunk 64 (seeded synthetic
 inputs; see kda_inputs.py). Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--pass bwd|fwd|bwd-states]
 
 * ``value``: device-timed tokens/s (inputs resident in HBM; K steps between
   CUDA events, barrier + synchronize on both sides, max over ranks). The
@@ -20,6 +21,10 @@ inputs; see kda_inputs.py). Prints one JSON line.
 * ``cpu_baseline``: the fp64 oracle on the host cores on a bounded sample of
   the same workload (whole sequences x heads), scaled to tokens/s.
 * ``--impl reference``: the fp64 oracle timed as the reference arm.
+* ``--pass``: ``bwd`` (default, the headline step above); ``fwd`` times one
+  ``kda_chunk_fwd`` call (o and ht) per step; ``bwd-states`` times the
+  backward that consumes the chunk states a forward saved (the states are
+  produced once before the timed region).
 
 Multi-GPU (torchrun): every rank runs the full workload on its own GPU (weak
 scaling, independent batches, no data-path collective); ``value`` is the sum
@@ -46,6 +51,8 @@ import kda_inputs  # noqa: E402
 
 WORKLOAD = "bf16_b8_t4096_h32_k128"
 METRIC = "KDA fwd-recompute+bwd tokens/s on 1 GB300 and % of roofline vs CPU oracle"
+METRICS = {"bwd": METRIC, "fwd": "KDA chunk forward (o, ht) tokens/s on 1 GB300",
+           "bwd-states": "KDA backward from saved chunk states tokens/s on 1 GB300"}
 UNIT = "tokens/s"
 
 # ----------------------------------------------------------------------------
@@ -64,6 +71,20 @@ def step_cost(B, T, H, HV, K, V, in_bytes=2, C=64):
     states = 2 * nck * K * V * 4
     flops = nck * (16 * C * K * V + 9 * C * C * K + 5 * C * C * V + C ** 3)
     return dict(bytes=io_in + io_out + states, flops=flops, io_in=io_in, io_out=io_out, states=states, nck=nck)
+
+
+def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64):
+    """Algorithmic bytes / FLOPs of one step of ``mode`` (see step_cost for the backward)."""
+    s = step_cost(B, T, H, HV, K, V, in_bytes, C)
+    th, tk, nck = B * T * HV, B * T * H, s["nck"]
+    if mode == "fwd":  # q, k, v, g, beta in; o and ht out; the chunk state stays on chip or in bf16 scratch
+        b = tk * K * in_bytes * 2 + th * V * in_bytes + th * K * 4 + th * in_bytes + th * V * in_bytes
+        b += B * HV * K * V * 4
+        f = nck * (6 * C * C * K + 2 * C * C * V + C ** 3 // 3 + 6 * C * K * V + 2 * C * C * V)
+        return dict(s, bytes=b, flops=f)
+    if mode == "bwd-states":  # the saved fp32 states are read once instead of written and read
+        return dict(s, bytes=s["io_in"] + s["io_out"] + s["states"] // 2)
+    return s
 
 
 def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
@@ -105,6 +126,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
     if name == "tc_grads":
         b = nck * (per_in + C * V * in_bytes + 2 * tcd + 2 * tdd + tcc + K * 4) + s["io_out"]
         return "hbm", b, s["flops"]
+    if name == "tc_output":
+        return "hbm", nck * (2 * tcd + tdd + tcc + C * V * in_bytes), nck * (2 * C * K * V + 2 * C * C * V)
+    if name == "tc_state_load":
+        return "hbm", nck * (K * V * 4 + 2 * tcd + tdd + tcd), nck * 2 * C * K * V
     return "hbm", s["bytes"], s["flops"]
 
 
@@ -324,22 +349,44 @@ def gpu_arm(args):
     tokens = B * T
     host = dict(q=inp.q, k=inp.k, v=inp.v, g=inp.g, beta=inp.beta, do=inp.do)
     x = {n: t.to(device).contiguous() for n, t in host.items()}
+    mode = args.mode
+    if mode == "fwd":
+        del host["do"], x["do"]
     dims = kda.make_dims(x["q"], x["v"], inp.scale)
-    wsb = kda.workspace_bytes(dims, kda.PASS_BWD)
+    wsb = kda.workspace_bytes(dims, kda.PASS_FWD if mode == "fwd" else kda.PASS_BWD)
     ws = torch.empty(wsb, dtype=torch.uint8, device=device)
-    out = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
-               dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]), dh0=None)
+    if mode == "fwd":
+        out = dict(o=torch.empty_like(x["v"]), ht=torch.empty(B, HV, K, V, dtype=torch.float32, device=device))
+    else:
+        out = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
+                   dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]))
     stream = torch.cuda.current_stream(device)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    states = None
+    if mode == "bwd-states":  # the forward's saved chunk states, produced once outside the timed region
+        fwb = kda.workspace_bytes(dims, kda.PASS_FWD)
+        fws = torch.empty(fwb, dtype=torch.uint8, device=device)
+        states = torch.empty(dims.num_chunks, HV, K, V, dtype=torch.float32, device=device)
+        o_tmp = torch.empty_like(x["v"])
+        rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(x["q"]), P(x["k"]), P(x["v"]), P(x["g"]), P(x["beta"]),
+                               None, None, None, None, P(o_tmp), None, P(states), P(fws), fwb, sptr)
+        if rc != 0:
+            raise kda.KdaError(rc, "kda_chunk_fwd")
+        del fws, o_tmp
 
     def step(inputs, outs):
-        rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]), P(inputs["g"]),
-                               P(inputs["beta"]), None, None, None, None, P(inputs["do"]), None, None,
-                               P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]), None,
-                               P(ws), wsb, sptr)
+        if mode == "fwd":
+            rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
+                                   P(inputs["g"]), P(inputs["beta"]), None, None, None, None, P(outs["o"]),
+                                   P(outs["ht"]), None, P(ws), wsb, sptr)
+        else:
+            rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
+                                   P(inputs["g"]), P(inputs["beta"]), None, None, None, None, P(inputs["do"]),
+                                   None, P(states), P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]),
+                                   P(outs["dbeta"]), None, P(ws), wsb, sptr)
         if rc != 0:
-            raise kda.KdaError(rc, "kda_chunk_bwd")
+            raise kda.KdaError(rc, "kda_chunk_fwd" if mode == "fwd" else "kda_chunk_bwd")
 
     for _ in range(args.warmup):
         step(x, out)
@@ -388,12 +435,12 @@ def gpu_arm(args):
         ach, pk, unit = aflops / avg / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
     else:
         ach, pk, unit = aflops / avg / 1e12, alu_peak_tflops(clk.get("sm_mhz") or peaks["sm_max_mhz"]), "TFLOP/s"
-    traffic = measured_traffic(dom, step_cost(B, T, H, HV, K, V)["nck"])
+    traffic = measured_traffic(dom, step_cost(B, T, H, HV, K, V)["nck"]) if mode == "bwd" else None
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
                 "traffic": traffic, "peak_source": peak_src if bound != "alu" else "152 SMs x 128 FFMA lanes x SM clock",
                 "avg_launch_ms": avg * 1e3, "share": tot[dom] / sum(tot.values()),
                 "kernels_ms": {n: 1e3 * tot[n] / len(per[n]) for n in names}}
-    sc = step_cost(B, T, H, HV, K, V)
+    sc = pass_cost(mode, B, T, H, HV, K, V)
     step_s = elapsed / args.steps
     path = {"bytes_alg": sc["bytes"], "flops_alg": sc["flops"],
             "hbm_frac": sc["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
@@ -401,7 +448,7 @@ def gpu_arm(args):
 
     # -- end to end through the C ABI from pinned host buffers --
     hin = {n: t.pin_memory() for n, t in host.items()}
-    hout = {n: torch.empty(out[n].shape, dtype=out[n].dtype, pin_memory=True) for n in ("dq", "dk", "dv", "dg", "dbeta")}
+    hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in out.items()}
     h2d = sum(t.numel() * t.element_size() for t in hin.values())
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
     e2e_steps = max(1, min(args.steps, 5))
@@ -419,7 +466,7 @@ def gpu_arm(args):
     torch.cuda.synchronize(device)
     e2e_val, _ = aggregate(tokens * e2e_steps, e0.elapsed_time(e1) / 1e3, world, device)
 
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRICS[mode], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD if not args.batch else f"{WORKLOAD} with B={args.batch}",
@@ -429,7 +476,9 @@ def gpu_arm(args):
             "roofline": roofline, "path": path, "clocks": clk, "gpu_launches": launches * args.steps,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps}}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if mode != "bwd":
+        line["config"]["pass"] = mode
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and mode == "bwd":
         v, used, dt, sample = oracle_sample(inp, 1, 16)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
                                 "seconds": dt}
@@ -448,6 +497,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="mode", default="bwd", choices=list(METRICS),
+                    help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
+                         "bwd-states: backward from saved chunk states")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (smaller cases for profiling; not the benchmark workload)")
     args = ap.parse_args()
