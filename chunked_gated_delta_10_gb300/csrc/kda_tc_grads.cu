@@ -192,6 +192,24 @@ __global__ void __launch_bounds__(512, 1)
         // beta of the next item: loaded now, stored to its shared slot at the end of this item
         const float nbeta =
             (has_next && tid < nx->c) ? __bfloat162float(beta[(nx->r0 + tid) * HV + nx->hv]) : 0.f;
+        if (tid == 0) {  // phase A (needs no gate values: the cumsum below runs while it executes)
+            tc_fence_after();
+            const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
+                           i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
+                         idesc_neg_a(i64n), ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
+                         ks > 0);
+            mma_commit(&bars[2]);
+        }
         // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
         float G2[16];
 #pragma unroll
@@ -212,24 +230,6 @@ __global__ void __launch_bounds__(512, 1)
         // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
         const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
 
-        if (tid == 0) {  // phase A
-            tc_fence_after();
-            const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
-                           i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
-                         idesc_neg_a(i64n), ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
-                         ks > 0);
-            mma_commit(&bars[2]);
-        }
         float rd = 0.f;
 #pragma unroll
         for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
