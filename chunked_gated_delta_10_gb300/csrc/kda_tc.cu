@@ -46,16 +46,22 @@ constexpr int TDD = D * D * 2;         // 128 x 128
 // (I + L)^-1 for a strictly lower triangular 64 x 64 L (fp32, shared), by
 // blocked forward substitution: 16 x 16 diagonal blocks first, then the
 // 2 x 2 block formula [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]] at
-// 32 and 64. Out and scratch X (1024 floats) are shared; 128 threads.
+// 32 and 64. 256 threads. Out (64 x 64) receives the lower block triangle
+// only: its blocks above the diagonal 16 x 16 blocks are never written nor
+// read (the bf16 conversion writes zeros there; see inv_zero_block). Scratch X
+// holds 32 x 36 floats.
 // ---------------------------------------------------------------------------
 // The strictly lower L is stored skewed: element (r, m) at r * 64 + ((m + r) & 63),
-// so a warp writing one row per lane hits 32 different banks.
+// so a warp reading or writing one row per lane hits 32 different banks.
 __device__ __forceinline__ int lsk(int r, int m) { return r * kC + ((m + r) & (kC - 1)); }
 
+// Whether 8 columns c0 .. c0+7 (c0 % 8 == 0) of INV row r lie in a block that tri_inverse64 leaves unwritten.
+__device__ __forceinline__ bool inv_zero_block(int r, int c0) {
+    return (r < 32 && c0 >= 32) || ((r & 31) < 16 && (c0 & 31) >= 16 && (c0 >> 5) == (r >> 5));
+}
+
 __device__ void tri_inverse64(const float* L, float* Out, float* X) {
-    const int tid = threadIdx.x, nth = blockDim.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < kC * kC / 4; i += nth) reinterpret_cast<float4*>(Out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    __syncthreads();
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
         // diagonal 16 x 16 block `warp`, column j = lane, right-looking: once x[m] is
         // known, every later row's partial sum takes its term (independent FMAs).
@@ -75,8 +81,8 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     __syncthreads();
     // 16 -> 32: blocks (1,0) and (3,2). X = L21 D0 (D0 lower triangular, zeros included), then -D1 X.
     // Each thread forms a 1 x 2 strip (256 strips per product).
-    for (int e = tid; e < 256; e += nth) {
-        const int pr = e >> 7, base = 32 * pr, a = (e >> 3) & 15, c = 2 * (e & 7);
+    {
+        const int pr = tid >> 7, base = 32 * pr, a = (tid >> 3) & 15, c = 2 * (tid & 7);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -88,8 +94,8 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
         *reinterpret_cast<float2*>(X + pr * 256 + a * 16 + c) = make_float2(s0, s1);
     }
     __syncthreads();
-    for (int e = tid; e < 256; e += nth) {
-        const int pr = e >> 7, base = 32 * pr, a = (e >> 3) & 15, c = 2 * (e & 7);
+    {
+        const int pr = tid >> 7, base = 32 * pr, a = (tid >> 3) & 15, c = 2 * (tid & 7);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
@@ -101,33 +107,49 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
         *reinterpret_cast<float2*>(Out + (base + 16 + a) * kC + base + c) = make_float2(-s0, -s1);
     }
     __syncthreads();
-    // 32 -> 64: rows 32..63, columns 0..31; each thread a 1 x 4 strip (4 independent sums)
-    for (int e = tid; e < 256; e += nth) {
-        const int a = e >> 3, c0 = (e & 7) * 4;
+    // 32 -> 64, rows 32..63, columns 0..31. X = L[32:64, 0:32] D0 with D0 the (block lower
+    // triangular) top-left 32 x 32 inverse: row a = lane, columns 4 warp .. +3; the columns
+    // of D0's upper-right zero block (16..31 for rows 0..15) only take rows 16..31.
+    {
+        const int a = lane, c0 = 4 * warp;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        auto term = [&](int m) {
             const float l = L[lsk(32 + a, m)];
             const float4 o = *reinterpret_cast<const float4*>(Out + m * kC + c0);
             s0 = fmaf(l, o.x, s0);
             s1 = fmaf(l, o.y, s1);
             s2 = fmaf(l, o.z, s2);
             s3 = fmaf(l, o.w, s3);
+        };
+        if (c0 < 16) {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) term(m);
+        } else {
+#pragma unroll
+            for (int m = 16; m < 32; ++m) term(m);
         }
-        *reinterpret_cast<float4*>(X + a * 32 + c0) = make_float4(s0, s1, s2, s3);
+        *reinterpret_cast<float4*>(X + a * 36 + c0) = make_float4(s0, s1, s2, s3);
     }
     __syncthreads();
-    for (int e = tid; e < 256; e += nth) {
-        const int a = e >> 3, c0 = (e & 7) * 4;
+    // then -D1 X with D1 the bottom-right 32 x 32 inverse: row 32 + a, columns c0 .. c0+3,
+    // a = 4 warp + lane / 8 (rows 0..15 of D1 end at its column 15)
+    {
+        const int a = tid >> 3, c0 = (tid & 7) * 4;
         float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-        for (int m = 0; m < 32; ++m) {
+        auto term = [&](int m) {
             const float l = Out[(32 + a) * kC + 32 + m];
-            const float4 xv = *reinterpret_cast<const float4*>(X + m * 32 + c0);
+            const float4 xv = *reinterpret_cast<const float4*>(X + m * 36 + c0);
             s0 = fmaf(l, xv.x, s0);
             s1 = fmaf(l, xv.y, s1);
             s2 = fmaf(l, xv.z, s2);
             s3 = fmaf(l, xv.w, s3);
+        };
+        if (a < 16) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) term(m);
+        } else {
+#pragma unroll
+            for (int m = 0; m < 32; ++m) term(m);
         }
         *reinterpret_cast<float4*>(Out + (32 + a) * kC + c0) = make_float4(-s0, -s1, -s2, -s3);
     }
@@ -320,7 +342,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
             for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
                 const int r = e >> 3, c0 = (e & 7) * 8;
-                st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
+                if (inv_zero_block(r, c0))
+                    *reinterpret_cast<uint4*>(sm + IS::TINV + tile_off(r, c0, kC)) = make_uint4(0u, 0u, 0u, 0u);
+                else
+                    st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
             }
             fence_async_smem();
             __syncthreads();
