@@ -5,18 +5,21 @@
 // and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
 // (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
 // Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
-// Gamma, Gref = middle row), the kernel evaluates, in five dependent MMA
+// Gamma, Gref = middle row), the kernel evaluates, in three dependent MMA
 // phases (fp32 accumulators in TMEM, columns noted):
 //
 //  A  dQ~^T = S_in dO^T [0,64)     dK^^T = dS_out delta^T [64,128)
 //     dw = -d_delta S_in^T [128,256) (M=64)   dAqk = dO delta^T [256,320)
+//     dXv = INV^T d_delta [320,448)   T = d_delta delta^T [448,512)
 //  B  PR^T = V d_delta^T + K~ dw^T [128,192)  Mkk = Kr Kc^T [192,256)
-//     dQr^T = Kc^T dN^T [256,320)   dXv = INV^T d_delta [320,448)
-//     dXk^T = dw^T INV [448,512)
-//  C  T = dINV INV^T [128,192)     with dINV = (P + R) diag(beta)
-//  D  dAkk = -INV^T T [320,384)
+//     dQr^T = Kc^T dN^T [256,320)   dXk^T = dw^T INV [448,512)
+//     dAkk = -INV^T T [320,384)
 //  E  dKr^T = Kc^T dM^T [128,192)  dKc^T = Qr^T dN + Kr^T dM [192,256)
 //
+// T stands for dINV INV^T with dINV = (P + R) diag(beta) = (d_delta V^T +
+// dw K~^T) diag(beta): since INV diag(beta) V = u, INV diag(beta) K~ = w,
+// dw = -d_delta S_in^T and delta = u - w S_in, it equals d_delta delta^T and
+// needs no dINV product of its own.
 // where dN = scale tril0(dAqk) and dM = diag(beta) tril-1(dAkk). The
 // epilogues give dv = beta dXv and dbeta = sum_j INV[j,r] PR[j,r] +
 // sum_j dAkk[r,j] Mkk[r,j] per chunk row (row-per-thread layout), and per key
@@ -49,7 +52,7 @@ struct GS {
     // after phase A the S_in / dS_out area holds the decayed factor tiles, stored transposed
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
     static constexpr int DW = DSO + TDD;
-    static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, DINV = DM + TCC, TT = DINV + TCC;
+    static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, TT = DM + 2 * TCC;  // DM .. TT: g tile part
     // the g tile (64 x 128 fp32) of a chunk lands on DN .. TT, which the previous chunk no longer needs after phase E
     static constexpr int GT = DN;
     static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048, NXT = BARS + 64;
@@ -208,6 +211,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
                          ks > 0);
+            // T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T + dw w^T, and with
+            // dw = -d_delta S_in^T and delta = u - w S_in this is d_delta delta^T
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem + 448, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
             mma_commit(&bars[2]);
         }
         // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
@@ -262,6 +269,10 @@ __global__ void __launch_bounds__(512, 1)
             for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
             if (rv)
                 for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+            tmem_ld16(tmem + lb + 448 + 16 * cq, x);  // T rows (bf16 operand of phase D)
+            tmem_ld_wait();
+            if (rv)
+                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
             tmem_ld32(tmem + lb + 320 + 32 * cq, x);
             tmem_ld_wait();
             if (rv && rrow < c) {
@@ -313,7 +324,7 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_before();
         fence_async_smem();
         __syncthreads();
-        if (tid == 0) {  // phase B
+        if (tid == 0) {  // phase B, and phase D: dAkk = -INV^T T
             tc_fence_after();
             if (has_next) issue_qk(*nx, nbar);  // q and k are consumed
             const uint32_t i64 = idesc_bf16(64, 64, false, false), i64t = idesc_bf16(64, 64, true, false),
@@ -330,84 +341,45 @@ __global__ void __launch_bounds__(512, 1)
             const uint32_t ixk = idesc_bf16(128, 64, true, true);
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk, ks > 0);
+            const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, true));
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd, ks > 0);
             mma_commit(&bars[2]);
         }
         if (!wait_all(&bars[2], mph, ws.status, 43, fail)) break;
         mph ^= 1;
         if (tid == 0 && has_next) issue_b(*nx, nbar);  // v and d_delta are consumed
         tc_fence_after();
-        {  // epilogue B: dbeta (INV part), dINV columns
+        {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
             const float br = rv ? sbeta[rrow] : 0.f;
-            float x[16];
-            float db = 0.f;
+            float x[16], a[16], m[16];
+            float db = 0.f, db2 = 0.f;
             tmem_ld16(tmem + lb + 128 + 16 * cq, x);
+            tmem_ld16(tmem + lb + 320 + 16 * cq, a);
+            tmem_ld16(tmem + lb + 192 + 16 * cq, m);
             tmem_ld_wait();
             if (rv) {
                 const ColAddr ar(rrow, kC);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) db = fmaf(ld_col(sm + GS::INV, ar, 16 * cq + u), x[u], db);
-#pragma unroll
-                for (int u = 0; u < 16; u += 2)
-                    st_col_pair(sm + GS::DINV, ar, 16 * cq + u, br * x[u], br * x[u + 1]);
-                xdb[cq * 64 + rrow] = db;
             }
-        }
-        tc_fence_before();
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {  // phase C: T = dINV INV^T
-            tc_fence_after();
-            const uint32_t i64 = idesc_bf16(64, 64, false, false);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_kmajor(S(GS::DINV), kC, ks), desc_kmajor(S(GS::INV), kC, ks), i64, ks > 0);
-            mma_commit(&bars[2]);
-        }
-        if (!wait_all(&bars[2], mph, ws.status, 44, fail)) break;
-        mph ^= 1;
-        tc_fence_after();
-        {
-            float x[16];
-            tmem_ld16(tmem + lb + 128 + 16 * cq, x);
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-        }
-        tc_fence_before();
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {  // phase D: dAkk = -INV^T T
-            tc_fence_after();
-            const uint32_t id = idesc_neg_a(idesc_bf16(64, 64, true, true));
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), id, ks > 0);
-            mma_commit(&bars[2]);
-        }
-        if (!wait_all(&bars[2], mph, ws.status, 45, fail)) break;
-        mph ^= 1;
-        if (tid == 0 && has_next) issue_d(*nx, nbar);  // INV is consumed
-        tc_fence_after();
-        {  // epilogue D: dbeta (Akk part), dM row segments
-            const float br = rv ? sbeta[rrow] : 0.f;
-            float a[16], m[16];
-            float db = 0.f;
-            tmem_ld16(tmem + lb + 320 + 16 * cq, a);
-            tmem_ld16(tmem + lb + 192 + 16 * cq, m);
-            tmem_ld_wait();
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 const int j = 16 * cq + u;
                 const bool in = j < rrow && rrow < c;
-                db = in ? fmaf(a[u], m[u], db) : db;
+                db2 = in ? fmaf(a[u], m[u], db2) : db2;
                 a[u] = in ? br * a[u] : 0.f;
             }
             if (rv) {
                 for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DM, rrow, 16 * cq + 8 * u, kC, a + 8 * u);
-                xdb[256 + cq * 64 + rrow] = db;
+                xdb[cq * 64 + rrow] = db;
+                xdb[256 + cq * 64 + rrow] = db2;
             }
         }
         tc_fence_before();
         fence_async_smem();
         __syncthreads();
+        if (tid == 0 && has_next) issue_d(*nx, nbar);  // INV is consumed
         if (tid < kC && tid < c)
             db_out[(r0 + tid) * HV + hv] =
                 __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
