@@ -165,3 +165,23 @@ def test_packed_sequences_equal_separate_runs():
             assert np.array_equal(r[key][0], full[key][0, b:e]), key
         for key in ("ht", "dh0"):
             assert np.array_equal(r[key][0], full[key][n]), key
+
+
+def test_triangle_backward_product_identity():
+    """The chunked oracle's dINV INV^T, with dINV = d_delta (beta V)^T + dw (beta K~)^T, equals
+    d_delta delta^T in every chunk, partial chunks included (u = INV beta V, w = INV beta K~,
+    dw = -d_delta S_in^T, delta = u - w S_in). The gradient kernel forms the product that way."""
+    from oracle.chunked import run_chunked
+
+    inp = kda_inputs.small(seed=41, B=1, T=0, H=1, HV=2, K=8, V=6, dtype="f32", seq_lens=[150, 37])
+    t = lambda x: None if x is None else x.to(torch.float64)
+    ref = run_chunked(t(inp.q), t(inp.k), t(inp.v), t(inp.g), t(inp.beta), inp.scale, t(inp.h0), t(inp.do),
+                      t(inp.dht), inp.cu_seqlens, keep=True)
+    assert len(ref["chunks"]) == 2 * (3 + 1)
+    for key, ch in ref["chunks"].items():
+        dINV = ch["d_delta"] @ ch["Xv"].T + ch["dw"] @ ch["Xk"].T
+        lhs = dINV @ ch["INV"].T
+        rhs = ch["d_delta"] @ ch["delta"].T
+        assert _close(lhs, rhs, 1e-11), key
+        # dropping the dw w^T term (a plausible slip) does not pass: S_in is nonzero (h0 given)
+        assert not _close(ch["d_delta"] @ ch["u"].T, rhs, 1e-6), key
