@@ -63,8 +63,6 @@ struct GS {
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
-__device__ __forceinline__ float bfr(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
 struct GradMaps {
     CUtensorMap q, k, v, d_o, g;
 };
@@ -402,7 +400,10 @@ __global__ void __launch_bounds__(512, 1)
         {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
             float dG[16];
             float dGC = 0.f;
-            const float sc = p.scale;
+            const float sc = p.scale, sce = p.scale * e_ref;
+            // this thread's first output row and the row stride of dq / dk (or of the per-value-head partials)
+            const int HO = G == 1 ? H : HV;
+            const int64_t o0 = ((r0 + 16 * qtr) * HO + (G == 1 ? h : hv)) * D + d, rs = (int64_t)HO * D;
 #pragma unroll
             for (int rb = 0; rb < 2; ++rb) {
                 const uint32_t cb = (uint32_t)(16 * qtr + 8 * rb);
@@ -423,26 +424,30 @@ __global__ void __launch_bounds__(512, 1)
                     const float kv = __uint_as_float(kq[x] << 16), qv = __uint_as_float(kq[x] & 0xffff0000u);
                     const float gm = G2[ii];
                     const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
-                    const float b = sbeta[r];
-                    const float dQt = sc * aQt[x], bX = b * aXk[x];
-                    const float dqv = dQt * E + aQr[x] * ep;
-                    const float dkv = aKh[x] * eh + bX * E + aKr[x] * ep + aKc[x] * em;
-                    const float khk = aKh[x] * kv * eh;
-                    // The factor values of the dGamma pair terms are the bf16 values the MMAs used, so that
-                    // each in-chunk pair's contributions to its two rows cancel in the chunk sum as they do
-                    // exactly.
-                    const float kt_b = bfr(kv * E), qr_b = bfr(qv * ep), kr_b = bfr(kv * ep), kc_b = bfr(kv * em);
-                    const float dgv =
-                        dQt * qv * E - khk + bX * kt_b + aQr[x] * qr_b + aKr[x] * kr_b - aKc[x] * kc_b;
+                    const float bX = sbeta[r] * aXk[x];
+                    // dq = E scale dQ~ + ep dQr;  dk = eh dK^ + E beta dXk + ep dKr + em dKc
+                    const float dqv = ep * fmaf(sce, aQt[x], aQr[x]);
+                    const float dkv = fmaf(ep, fmaf(e_ref, bX, aKr[x]), em * fmaf(e_cr, aKh[x], aKc[x]));
+                    const float khk = aKh[x] * (kv * eh);
+                    // The factor values of the dGamma pair terms are the bf16 values the MMAs used (rounded
+                    // two at a time here as in the factor tiles), so that each in-chunk pair's contributions
+                    // to its two rows cancel in the chunk sum as they do exactly.
+                    const uint32_t p1 = pack2(kv * E, qv * ep), p2 = pack2(kv * ep, kv * em);
+                    const float kt_b = __uint_as_float(p1 << 16), qr_b = __uint_as_float(p1 & 0xffff0000u);
+                    const float kr_b = __uint_as_float(p2 << 16), kc_b = __uint_as_float(p2 & 0xffff0000u);
+                    float dgv = fmaf(sc * aQt[x], qv * E, -khk);
+                    dgv = fmaf(bX, kt_b, dgv);
+                    dgv = fmaf(aQr[x], qr_b, dgv);
+                    dgv = fmaf(aKr[x], kr_b, dgv);
+                    dgv = fmaf(-aKc[x], kc_b, dgv);
                     dG[ii] = in ? dgv : 0.f;
                     if (in) {
                         dGC += khk;
+                        const int64_t o = o0 + ii * rs;
                         if (G == 1) {
-                            const int64_t o = ((r0 + r) * H + h) * D + d;
                             st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o),
                                          reinterpret_cast<uint8_t*>(dk_out + o), dqv, dkv);
                         } else {
-                            const int64_t o = ((r0 + r) * HV + hv) * D + d;
                             ws.dqp[o] = dqv;
                             ws.dkp[o] = dkv;
                         }
