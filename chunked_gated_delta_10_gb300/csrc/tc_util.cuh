@@ -148,12 +148,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
 
 // Descriptor of the 16-deep reduction step `ks` of an operand tile (see the
 // convention at the top). K-major: tile rows = M/N, reduction along columns.
+// The start-address field holds (address >> 4) in 14 bits, and shared-memory
+// addresses stay below 2^18 bytes, so the descriptor of (tile + off) is the
+// tile's descriptor plus off >> 4: one add per K step once the tile's
+// descriptor is formed (offsets are compile-time constants in unrolled loops).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int rows, int ks) {
-    return sdesc(tile + (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32), 16, 1024);
+    return sdesc(tile, 16, 1024) + (uint64_t)(((ks >> 2) * rows * 128 + (ks & 3) * 32) >> 4);
 }
 // MN-major: tile rows = reduction, columns = M/N (blocks of 64 columns).
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int rows, int ks) {
-    return sdesc(tile + (uint32_t)(ks * 16 * 128), (uint32_t)(rows * 128), 1024);
+    return sdesc(tile, (uint32_t)(rows * 128), 1024) + (uint64_t)((ks * 16 * 128) >> 4);
 }
 
 // D[tmem] (+)= A * B^T, one instruction of K = 16 (issued by one thread).
