@@ -454,27 +454,29 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
             }
-            xgc[qtr * 128 + d] = dGC;
-            __syncthreads();
-            const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
-                               ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
-#pragma unroll
-            for (int x = 0; x < 16; ++x)
-                if (16 * qtr + x == c - 1) dG[x] += dGCt;
+            // dg = reverse in-chunk cumsum of dGamma, whose last valid row also takes the Gamma_C terms
+            // dGCt: in-quarter suffix sums and quarter totals first (one exchange), then per row the later
+            // quarters' totals (added in the order 3, 2, 1) and dGCt where row c - 1 lies at or after it.
             float run = 0.f;
 #pragma unroll
             for (int x = 15; x >= 0; --x) {
                 run += dG[x];
                 dG[x] = run;
             }
+            xgc[qtr * 128 + d] = dGC;
             xt1[qtr * 128 + d] = run;
             __syncthreads();
-            float carry = 0.f;  // later quarters' totals, added in the order 3, 2, 1
+            const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
+                               ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
+            const int qc = (c - 1) >> 4, xc = (c - 1) & 15;
+            float carry = 0.f;
             for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
+            if (qc > qtr) carry += dGCt;
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const int r = 16 * qtr + x;
-                if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = dG[x] + carry;
+                const float t = (qc == qtr && x <= xc) ? dG[x] + dGCt : dG[x];
+                if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = t + carry;
             }
         }
         if (tid < kC) reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nbeta;
