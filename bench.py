@@ -127,8 +127,8 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
     if name == "tc_grads":
         b = nck * (per_in + C * V * in_bytes + 2 * tcd + 2 * tdd + tcc + K * 4) + s["io_out"]
         return "hbm", b, s["flops"]
-    if name == "tc_output":
-        return "hbm", nck * (2 * tcd + tdd + tcc + C * V * in_bytes), nck * (2 * C * K * V + 2 * C * C * V)
+    if name == "tc_fwd_out":  # w, K^, Q~s, u, Aqk, e^Gamma_C in; o out (state on chip)
+        return "hbm", nck * (4 * tcd + tcc + K * 4 + C * V * in_bytes), nck * (6 * C * K * V + 2 * C * C * V)
     if name == "tc_state_load":
         return "hbm", nck * (K * V * 4 + 2 * tcd + tdd + tcd), nck * 2 * C * K * V
     return "hbm", s["bytes"], s["flops"]

@@ -72,15 +72,15 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_u = take(CH * TCD);
         L.t_kh = take(CH * TCD);
         L.t_qs = take(CH * TCD);
-        L.t_vn = take(CH * TCD);
         L.t_aqk = take(CH * TCC);
         L.t_inv = take(CH * TCC);
-        L.t_sin = take(CH * TDD);
         L.t_egc = take(CH * 128 * f);
-        if (pass == KDA_PASS_FWD) {  // the forward needs no gradient regions
+        if (pass == KDA_PASS_FWD) {  // the forward keeps the state and delta on chip
             L.total = off;
             return L;
         }
+        L.t_vn = take(CH * TCD);
+        L.t_sin = take(CH * TDD);
         L.t_dvn = take(CH * TCD);
         L.t_dso = take(CH * TDD);
         if (p.HV != p.H) {

@@ -816,86 +816,184 @@ cleanup:
 }
 
 // ---------------------------------------------------------------------------
-// tc_output: the forward output o = scale Q~ S_in + Aqk delta of one (chunk,
-// value head); 128 threads, chunk rows on TMEM lanes (M = 64).
+// tc_fwd_out: the forward's state pass with the output fused in. One CTA per
+// (value head, sequence), 256 threads, thread t owns state row k = t % 128,
+// columns 64 (t / 128) .. +63. Per chunk: delta = u - w S (chunk rows on TMEM
+// lanes, in place of u), then S <- e^(Gamma_C) S + K^^T delta and
+// o = (scale Q~) S + Aqk delta in one MMA group; o leaves as bf16 rows. Inputs
+// are single-buffered in two groups: w is refetched once the delta MMA has
+// consumed it, the rest once the state and output MMAs have.
 // ---------------------------------------------------------------------------
-struct OutSm {
-    static constexpr int QS = 0, SIN = TCD, AQK = TCD + TDD, VN = TCD + TDD + TCC, BARS = 2 * TCD + TDD + TCC;
-    static constexpr int END = BARS + 64;
+struct FoSm {
+    static constexpr int W = 0, KH = TCD, QS = 2 * TCD, U = 3 * TCD, AQK = 4 * TCD, EGC = 4 * TCD + TCC;
+    static constexpr int S = EGC + 1024, BARS = S + TDD, END = BARS + 64;
 };
-constexpr int kOutSmem = 1024 + OutSm::END;
+constexpr int kFoSmem = 1024 + FoSm::END;
 
-__global__ void __launch_bounds__(128, 3) k_tc_output(Prob p, bf16* __restrict__ o, TcWs ws) {
+__global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
+                                                        float* __restrict__ states, bf16* __restrict__ o, TcWs ws) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OutSm::BARS);  // loads, mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
+    uint8_t* tS = sm + FoSm::S;
+    uint8_t* tU = sm + FoSm::U;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FoSm::BARS);  // w, group 2, mma
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, hv = blockIdx.y;
-    const int64_t gc = blockIdx.x, ch = gc * HV + hv;
-    int64_t r0;
-    int c;
-    chunk_rows(p, gc, r0, c);
+    const int k = tid & 127, vh = tid >> 7;
+    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
+    int64_t bos, eos, c0;
+    seq_range(p, n, bos, eos, c0);
+    const int nts = (int)((eos - bos + kC - 1) / kC);
+
     if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
+        for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
         *fail = 0;
-        mbar_expect_tx(&bars[0], 2 * TCD + TDD + TCC);
-        bulk_load(sm + OutSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
-        bulk_load(sm + OutSm::SIN, ws.sin + ch * TDD, TDD, &bars[0]);
-        bulk_load(sm + OutSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
-        bulk_load(sm + OutSm::VN, ws.vn + ch * TCD, TCD, &bars[0]);
     }
-    if (warp == 0) tmem_alloc(tslot, 128);
+    if (warp == 0) tmem_alloc(tslot, 256);
+    float S[64];
+    {
+        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
+    }
+    auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
+    auto issue_w = [&](int it) {
+        mbar_expect_tx(&bars[0], TCD);
+        bulk_load(sm + FoSm::W, ws.w + chunk(it) * TCD, TCD, &bars[0]);
+    };
+    auto issue_g2 = [&](int it) {  // K^, scale Q~, u, Aqk, e^Gamma_C
+        const int64_t ch = chunk(it);
+        mbar_expect_tx(&bars[1], 3 * TCD + TCC + 512);
+        bulk_load(sm + FoSm::KH, ws.kh + ch * TCD, TCD, &bars[1]);
+        bulk_load(sm + FoSm::QS, ws.qs + ch * TCD, TCD, &bars[1]);
+        bulk_load(tU, ws.u + ch * TCD, TCD, &bars[1]);
+        bulk_load(sm + FoSm::AQK, ws.aqk + ch * TCC, TCC, &bars[1]);
+        bulk_load(sm + FoSm::EGC, ws.egc + ch * D, 512, &bars[1]);
+    };
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (!wait_all(&bars[0], 0, ws.status, 61, fail)) goto cleanup;
-    if (tid == 0) {  // o = (scale Q~) S_in + Aqk delta (M = 64, N = 128)
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 128, false, true);
-        for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, desc_kmajor(smem_u32(sm + OutSm::QS), kC, ks), desc_mnmajor(smem_u32(sm + OutSm::SIN), D, ks),
-                     id, ks > 0);
-        for (int ks = 0; ks < kC / 16; ++ks)
-            mma_bf16(tmem, desc_kmajor(smem_u32(sm + OutSm::AQK), kC, ks), desc_mnmajor(smem_u32(sm + OutSm::VN), kC, ks),
-                     id, 1);
-        mma_commit(&bars[1]);
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
+    if (tid == 0 && nts > 0) {
+        issue_w(0);
+        issue_g2(0);
     }
-    if (!wait_all(&bars[1], 0, ws.status, 62, fail)) goto cleanup;
-    tc_fence_after();
-    {  // row r = 16 warp + lane (lane < 16), 128 columns in four groups of 32
-        const int r = 16 * warp + lane;
-        const uint32_t lq = (uint32_t)(32 * warp) << 16;
+    uint32_t mph = 0;
+    for (int it = 0; it < nts; ++it) {
+        const int64_t ch = chunk(it);
+        const uint32_t ph = (uint32_t)it & 1;
+        // bf16 copy of S (row k, this thread's 64 columns): operand of the delta and output MMAs
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            float x[32];
-            tmem_ld32(tmem + lq + 32 * h, x);
-            tmem_ld_wait();
-            if (lane < 16 && r < c) {
-                bf16* dst = o + ((r0 + r) * HV + hv) * D + 32 * h;
+        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
+        fence_async_smem();
+        if (states) {  // the fp32 state entering this chunk, [chunk, HV, K, V]
+            float4* dst = reinterpret_cast<float4*>(states + (ch * D + k) * D + 64 * vh);
 #pragma unroll
-                for (int u = 0; u < 32; u += 8) {
-                    uint4 vv;
-                    vv.x = pack2(x[u], x[u + 1]);
-                    vv.y = pack2(x[u + 2], x[u + 3]);
-                    vv.z = pack2(x[u + 4], x[u + 5]);
-                    vv.w = pack2(x[u + 6], x[u + 7]);
-                    *reinterpret_cast<uint4*>(dst + u) = vv;
+            for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+        }
+        if (!wait_all(&bars[0], ph, ws.status, 71, fail)) break;
+        if (tid == 0) {  // delta accumulator = w S (M = 64, N = 128)
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(64, 128, false, true);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
+                         ks > 0);
+            mma_commit(&bars[2]);
+        }
+        if (!wait_all(&bars[2], mph, ws.status, 72, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && it + 1 < nts) issue_w(it + 1);  // w is consumed
+        if (!wait_all(&bars[1], ph, ws.status, 73, fail)) break;
+        tc_fence_after();
+        const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);  // M = 64 row of this lane, column half
+        {  // delta = u - w S in place of u
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float acc[32];
+                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int c8 = 0; c8 < 32; c8 += 8) {
+                        float x[8];
+                        ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+#pragma unroll
+                        for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
+                        st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+                    }
                 }
             }
         }
+        tc_fence_before();
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // S accumulator = K^^T delta (M = 128, N = 128)
+            const uint32_t is = idesc_bf16(128, 128, true, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + FoSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
+                         is, ks > 0);
+            // o accumulator (in the delta columns) = (scale Q~) S + Aqk delta (M = 64, N = 128)
+            const uint32_t io = idesc_bf16(64, 128, false, true);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::QS), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), io,
+                         ks > 0);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::AQK), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks), io,
+                         1);
+            mma_commit(&bars[2]);
+        }
+        const float e = reinterpret_cast<const float*>(sm + FoSm::EGC)[k];
+        if (!wait_all(&bars[2], mph, ws.status, 74, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && it + 1 < nts) issue_g2(it + 1);  // K^, Q~s, u / delta, Aqk, e^Gamma_C are consumed
+        tc_fence_after();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {  // state update
+            float acc[32];
+            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
+        }
+        {  // o rows (bf16)
+            const int64_t r0 = bos + (int64_t)it * kC;
+            const int c = (int)((eos - r0) < kC ? (eos - r0) : kC);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float x[32];
+                tmem_ld32(tmem + lq + cb + 32 * h, x);
+                tmem_ld_wait();
+                if (lane < 16 && r < c) {
+                    bf16* dst = o + ((r0 + r) * HV + hv) * D + cb + 32 * h;
+#pragma unroll
+                    for (int u = 0; u < 32; u += 8) {
+                        uint4 vv;
+                        vv.x = pack2(x[u], x[u + 1]);
+                        vv.y = pack2(x[u + 2], x[u + 3]);
+                        vv.z = pack2(x[u + 4], x[u + 5]);
+                        vv.w = pack2(x[u + 6], x[u + 7]);
+                        *reinterpret_cast<uint4*>(dst + u) = vv;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
     }
-cleanup:
+    if (ht && *(volatile int*)fail == 0) {
+        float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) dst[j] = S[j];
+    }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem, 256);
 }
-
 
 template <typename F>
 cudaError_t set_smem(F* f, int bytes) {
@@ -934,15 +1032,10 @@ cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream
 
 cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
-    if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
-    if ((e = set_smem(k_tc_output, kOutSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_fwd_out, kFoSmem)) != cudaSuccess) return e;
     if ((e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
-    k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, io.ht, io.states_out, ws);
-    note_launch("tc_state_fwd", st);
-    if (p.NT > 0) {
-        k_tc_output<<<dim3((unsigned)p.NT, p.HV), 128, kOutSmem, st>>>(p, (bf16*)io.o, ws);
-        note_launch("tc_output", st);
-    }
+    k_tc_fwd_out<<<dim3(p.HV, p.N), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws);
+    note_launch("tc_fwd_out", st);
     return cudaGetLastError();
 }
 

@@ -134,7 +134,7 @@ FWD_TC = {
 def test_tensor_core_forward(kda, name):
     inp = kda_inputs.small(seed=35, dtype="bf16", **FWD_TC[name])
     o, ht, st = gpu_fwd(kda, inp)
-    assert kda.load().kda_launch_name(1) == b"tc_state_fwd"  # the tensor-core path ran
+    assert kda.load().kda_launch_name(1) == b"tc_fwd_out"  # the tensor-core path ran
     ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
     tol = _tol(inp)
     errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
