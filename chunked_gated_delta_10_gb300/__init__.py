@@ -166,8 +166,9 @@ def _workspace(dims, which, device, ws):
     return ws
 
 
-def chunk_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_states=True, ws=None):
-    """Chunked KDA forward. Returns (o, ht, states); states is [num_chunks, HV, K, V] fp32 or None."""
+def chunk_fwd(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None, output_states=False, ws=None):
+    """Chunked KDA forward. Returns (o, ht, states); states is [num_chunks, HV, K, V] fp32 when
+    ``output_states`` (the state entering every chunk, for a backward that skips the recompute), else None."""
     lib = load()
     dt = q.dtype
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):

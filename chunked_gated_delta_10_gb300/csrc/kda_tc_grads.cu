@@ -491,23 +491,25 @@ __global__ void __launch_bounds__(512, 1)
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dq, dk of key head h = sum over its G value heads in ascending order.
-__global__ void k_tc_gva_reduce(int64_t rows, int H, int G, const float* __restrict__ dqp,
-                                const float* __restrict__ dkp, bf16* __restrict__ dq, bf16* __restrict__ dk) {
-    const int64_t total = rows * H * D;
+// dq, dk of key head h = sum over its G value heads in ascending order; each thread
+// handles 4 consecutive key channels of one (row, key head).
+__global__ void __launch_bounds__(256) k_tc_gva_reduce(int64_t rows, int H, int G, const float* __restrict__ dqp,
+                                                       const float* __restrict__ dkp, bf16* __restrict__ dq,
+                                                       bf16* __restrict__ dk) {
+    const int64_t total = rows * H * (D / 4);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int dd = (int)(i % D);
-        const int64_t rh = i / D;
-        const int hh = (int)(rh % H);
-        const int64_t r = rh / H;
-        const int64_t base = (r * H * G + (int64_t)hh * G) * D + dd;
-        float aq = 0.f, ak = 0.f;
+        const int d4 = (int)(i & (D / 4 - 1));
+        const int64_t rh = i >> 5;  // row * H + key head (D / 4 = 32 channel groups)
+        const int64_t base = rh * G * D + 4 * d4;  // value heads hh * G .. hh * G + G - 1 of that row
+        float4 aq = make_float4(0.f, 0.f, 0.f, 0.f), ak = aq;
         for (int j = 0; j < G; ++j) {
-            aq += dqp[base + (int64_t)j * D];
-            ak += dkp[base + (int64_t)j * D];
+            const float4 x = *reinterpret_cast<const float4*>(dqp + base + (int64_t)j * D);
+            const float4 y = *reinterpret_cast<const float4*>(dkp + base + (int64_t)j * D);
+            aq.x += x.x; aq.y += x.y; aq.z += x.z; aq.w += x.w;
+            ak.x += y.x; ak.y += y.y; ak.z += y.z; ak.w += y.w;
         }
-        dq[i] = __float2bfloat16_rn(aq);
-        dk[i] = __float2bfloat16_rn(ak);
+        *reinterpret_cast<uint2*>(dq + rh * D + 4 * d4) = make_uint2(pack2(aq.x, aq.y), pack2(aq.z, aq.w));
+        *reinterpret_cast<uint2*>(dk + rh * D + 4 * d4) = make_uint2(pack2(ak.x, ak.y), pack2(ak.z, ak.w));
     }
 }
 
@@ -536,7 +538,8 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
                                                io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
     if (p.HV != p.H) {
-        k_tc_gva_reduce<<<1024, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq, (bf16*)io.dk);
+        k_tc_gva_reduce<<<8 * 152, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq,
+                                                  (bf16*)io.dk);
         note_launch("tc_gva_reduce", st);
     }
     return cudaGetLastError();

@@ -49,7 +49,7 @@ def gpu_bwd(kda, inp, states=None):
 def gpu_fwd(kda, inp):
     x = _cuda(inp)
     o, ht, st = kda.chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], scale=inp.scale, h0=x["h0"],
-                              cu_seqlens=inp.cu_seqlens)
+                              cu_seqlens=inp.cu_seqlens, output_states=True)
     torch.cuda.synchronize()
     return o, ht, st
 
