@@ -44,7 +44,7 @@ struct Layout {
     size_t status, gam, w, u, vn, inv, aqk, sin, dso, dvn, dqt, dkh, dw, dgc, dqp, dkp, total;
     // tensor-core path regions
     bool tc;
-    size_t t_w, t_u, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc;
+    size_t t_w, t_u, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc, t_seg_e, t_seg_p, t_seg_s0;
 };
 
 // bf16 inputs with K = V = 128 run on the tensor-core path (forward and backward).
@@ -83,6 +83,13 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_sin = take(CH * TDD);
         L.t_dvn = take(CH * TCD);
         L.t_dso = take(CH * TDD);
+        const SegPlan sp = seg_plan(p);
+        if (sp.len) {  // segmented state passes: three fp32 K x V matrices per (sequence, head, segment)
+            const size_t segs = (size_t)p.N * HV * sp.M * 128 * 128 * f;
+            L.t_seg_e = take(segs);
+            L.t_seg_p = take(segs);
+            L.t_seg_s0 = take(segs);
+        }
         if (p.HV != p.H) {
             L.dqp = take(R * HV * K * f);
             L.dkp = take(R * HV * K * f);
@@ -158,6 +165,9 @@ TcWs carve_tc(void* base, const Layout& L) {
     w.sin = at(L.t_sin);
     w.dso = at(L.t_dso);
     w.egc = (float*)at(L.t_egc);
+    w.seg_e = (float*)at(L.t_seg_e);
+    w.seg_p = (float*)at(L.t_seg_p);
+    w.seg_s0 = (float*)at(L.t_seg_s0);
     if (L.dqp) {
         w.dqp = (float*)at(L.dqp);
         w.dkp = (float*)at(L.dkp);

@@ -48,8 +48,19 @@ cudaError_t simt_bwd(const Prob& p, bool bf16, const IO& io, const Ws& ws, cudaS
 struct TcWs {
     uint8_t *w, *u, *kh, *qs, *vn, *dvn, *aqk, *inv, *sin, *dso;
     float *egc, *dqp, *dkp;
+    // segmented state passes (long sequences, few sweeps): per (sequence, value head, segment) fp32
+    // K x V end states from a zero start, K x K transitions and start states
+    float *seg_e, *seg_p, *seg_s0;
     int* status;
 };
+
+// Segmented sweeps of the state passes: segment m of a sequence covers chunks
+// [m * len, min((m + 1) * len, chunks)); len = 0 means no segmentation.
+// Chosen from the problem alone (dense batches with few sweeps and long sequences).
+struct SegPlan {
+    int len, M;
+};
+SegPlan seg_plan(const Prob& p);
 
 // The tensor-core path handles bf16 inputs with K = V = 128.
 bool tc_path_ok(const Prob& p, bool bf16);

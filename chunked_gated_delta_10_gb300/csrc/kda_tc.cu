@@ -405,11 +405,26 @@ cleanup:
 }
 
 // ---------------------------------------------------------------------------
-// tc_state_fwd: one CTA per (value head, sequence), 256 threads; thread t owns
-// state row k = t % 128, columns 64 (t / 128) .. +63 in fp32 registers. A bf16
-// copy of S in shared memory feeds the MMAs and is the S_in checkpoint. Chunk
-// inputs: u and e^Gamma_C double-buffered; w and K^ single-buffered, each
-// refetched as soon as its MMA has consumed it. delta overwrites u in place.
+// Segment modes of the state passes (grid z = segment, or 2 x segments for
+// mode kSegEnds: z < M the end state from a zero start, z >= M the transition).
+//   kSegNone   one sweep over the sequence (len = 0), checkpoints written
+//   kSegCkpt   checkpoints of one segment from its start state (seg_s0)
+//   kSegEnds   per segment: the end state from a zero start (seg_e) and the
+//              transition, i.e. the end state from the identity with the
+//              chunk inputs that do not multiply the state set to zero (seg_p)
+// ---------------------------------------------------------------------------
+enum { kSegNone = 0, kSegCkpt = 1, kSegEnds = 2 };
+struct SegArg {
+    int len, M, mode;
+};
+
+// ---------------------------------------------------------------------------
+// tc_state_fwd: one CTA per (value head, sequence[, segment]), 256 threads;
+// thread t owns state row k = t % 128, columns 64 (t / 128) .. +63 in fp32
+// registers. A bf16 copy of S in shared memory feeds the MMAs and is the S_in
+// checkpoint. Chunk inputs: u and e^Gamma_C double-buffered; w and K^
+// single-buffered, each refetched as soon as its MMA has consumed it. delta
+// overwrites u in place.
 // ---------------------------------------------------------------------------
 struct FwdSm {
     static constexpr int W = 0, KH = TCD, U = 2 * TCD, UBUF = TCD + 1024;  // u tile, then e^Gamma_C (512 B)
@@ -417,8 +432,7 @@ struct FwdSm {
 };
 constexpr int kFwdSmem = 1024 + FwdSm::END;
 
-__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
-                                                          float* __restrict__ states, TcWs ws) {
+__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + FwdSm::S;
@@ -432,6 +446,12 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
+    // segment and mode: 0 checkpoints, 1 end state from zero, 2 transition
+    const int m = sg.mode == kSegEnds ? (int)blockIdx.z % sg.M : (int)blockIdx.z;
+    const int mode = sg.mode == kSegEnds ? 1 + (int)blockIdx.z / sg.M : 0;
+    const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
+    if (sg.len && lo >= hi) return;
+    const bool ckpt = mode == 0, with_u = mode != 2;
 
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(&bars[i], 1);
@@ -440,17 +460,21 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     float S[64];
+    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
     {
-        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
+        const float* src = nullptr;
+        if (mode == 0) src = (lo == 0) ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
+                                       : ws.seg_s0 + seg_at;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : (mode == 2 && 64 * vh + j == k ? 1.f : 0.f);
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
     auto issue_u = [&](int it) {
-        uint8_t* b = sm + FwdSm::U + (it & 1) * FwdSm::UBUF;
-        mbar_expect_tx(&bars[it & 1], TCD + 512);
-        bulk_load(b, ws.u + chunk(it) * TCD, TCD, &bars[it & 1]);
-        bulk_load(b + TCD, ws.egc + chunk(it) * D, 512, &bars[it & 1]);
+        const int b = (it - lo) & 1;
+        uint8_t* buf = sm + FwdSm::U + b * FwdSm::UBUF;
+        mbar_expect_tx(&bars[b], (with_u ? TCD : 0) + 512);
+        if (with_u) bulk_load(buf, ws.u + chunk(it) * TCD, TCD, &bars[b]);
+        bulk_load(buf + TCD, ws.egc + chunk(it) * D, 512, &bars[b]);
     };
     auto issue_w = [&](int it) {
         mbar_expect_tx(&bars[2], TCD);
@@ -465,26 +489,22 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;  // this warp's TMEM lane quarter
-    if (tid == 0 && nts > 0) {
-        issue_w(0);
-        issue_kh(0);
-        issue_u(0);
-        if (nts > 1) issue_u(1);
+    if (tid == 0 && lo < hi) {
+        issue_w(lo);
+        issue_kh(lo);
+        issue_u(lo);
+        if (lo + 1 < hi) issue_u(lo + 1);
     }
     uint32_t mph = 0;
-    for (int it = 0; it < nts; ++it) {
+    for (int it = lo; it < hi; ++it) {
         const int64_t ch = chunk(it);
-        const uint32_t ph = (uint32_t)it & 1;  // phase of the single-buffered w and K^ barriers
-        uint8_t* tU = sm + FwdSm::U + (it & 1) * FwdSm::UBUF;
+        const int rel = it - lo;
+        const uint32_t ph = (uint32_t)rel & 1;  // phase of the single-buffered w and K^ barriers
+        uint8_t* tU = sm + FwdSm::U + (rel & 1) * FwdSm::UBUF;
         // bf16 copy of S (row k, this thread's 64 columns) for the MMAs and the S_in checkpoint
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
-        if (states) {  // the fp32 state entering this chunk, [chunk, HV, K, V]
-            float4* dst = reinterpret_cast<float4*>(states + (ch * D + k) * D + 64 * vh);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
-        }
         if (!wait_all(&bars[2], ph, ws.status, 21, fail)) break;
         if (tid == 0) {  // delta accumulator = w S (chunk rows on TMEM lanes, M = 64, N = 128)
             tc_fence_after();
@@ -493,13 +513,15 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
                          ks > 0);
             mma_commit(&bars[4]);
-            bulk_store(ws.sin + ch * TDD, tS, TDD);
-            bulk_commit();
+            if (ckpt) {
+                bulk_store(ws.sin + ch * TDD, tS, TDD);
+                bulk_commit();
+            }
         }
         if (!wait_all(&bars[4], mph, ws.status, 22, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < nts) issue_w(it + 1);  // w is consumed
-        if (!wait_all(&bars[it & 1], (it >> 1) & 1, ws.status, 24, fail)) break;
+        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w is consumed
+        if (!wait_all(&bars[rel & 1], (rel >> 1) & 1, ws.status, 24, fail)) break;
         tc_fence_after();
         {  // delta = u - w S in place of u: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
             const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
@@ -511,8 +533,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 if (lane < 16) {
 #pragma unroll
                     for (int c8 = 0; c8 < 32; c8 += 8) {
-                        float x[8];
-                        ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
+                        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                        if (with_u) ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
 #pragma unroll
                         for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
                         st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
@@ -530,12 +552,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + FwdSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          id, ks > 0);
             mma_commit(&bars[4]);
-            bulk_store(ws.vn + ch * TCD, tU, TCD);
-            bulk_commit();
+            if (ckpt) {
+                bulk_store(ws.vn + ch * TCD, tU, TCD);
+                bulk_commit();
+            }
         }
         if (!wait_all(&bars[4], mph, ws.status, 23, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < nts) issue_kh(it + 1);  // K^ is consumed
+        if (tid == 0 && it + 1 < hi) issue_kh(it + 1);  // K^ is consumed
         tc_fence_after();
         {
             const float e = reinterpret_cast<const float*>(tU + TCD)[k];
@@ -551,10 +575,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
         tc_fence_before();
         if (tid == 0) bulk_wait_read();  // S_in and delta copies have read tS and the u buffer
         __syncthreads();
-        if (tid == 0 && it + 2 < nts) issue_u(it + 2);
+        if (tid == 0 && it + 2 < hi) issue_u(it + 2);
     }
-    if (ht && *(volatile int*)fail == 0) {
-        float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
+    if (mode != 0 && *(volatile int*)fail == 0) {
+        float* dst = (mode == 1 ? ws.seg_e : ws.seg_p) + seg_at;
 #pragma unroll
         for (int j = 0; j < 64; ++j) dst[j] = S[j];
     }
@@ -562,6 +586,54 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// tc_seg_combine: start states of the segments of one (sequence, value head),
+// 16 state columns per CTA, 128 threads (one state row each), fp32:
+// S_start(first) = init (h0 or dht, or zero), S_start(next) = P S_start + E
+// with P the segment's transition and E its end state from zero; forward
+// segments in ascending order, reverse segments in descending order.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_tc_seg_combine(Prob p, SegArg sg, int reverse, const float* __restrict__ init,
+                                                        TcWs ws) {
+    __shared__ float sS[D][17];
+    const int k = threadIdx.x, hv = blockIdx.x, n = blockIdx.y, v0 = 16 * blockIdx.z, HV = p.HV;
+    int64_t bos, eos, c0;
+    seq_range(p, n, bos, eos, c0);
+    const int nts = (int)((eos - bos + kC - 1) / kC);
+    const int nseg = (nts + sg.len - 1) / sg.len;
+    float cur[16];
+    {
+        const float* src = init ? init + (((int64_t)n * HV + hv) * D + k) * D + v0 : nullptr;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) cur[v] = src ? src[v] : 0.f;
+    }
+    const int64_t head = ((int64_t)n * HV + hv) * sg.M;
+    for (int s = 0; s < nseg; ++s) {
+        const int m = reverse ? nseg - 1 - s : s;
+        const int64_t at = (head + m) * D * D;
+        float* st = ws.seg_s0 + at + (int64_t)k * D + v0;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) st[v] = cur[v];
+        if (s + 1 == nseg) break;
+        __syncthreads();
+#pragma unroll
+        for (int v = 0; v < 16; ++v) sS[k][v] = cur[v];
+        __syncthreads();
+        const float* prow = ws.seg_p + at + (int64_t)k * D;
+        const float* erow = ws.seg_e + at + (int64_t)k * D + v0;
+#pragma unroll
+        for (int v = 0; v < 16; ++v) cur[v] = erow[v];
+        for (int j4 = 0; j4 < D; j4 += 4) {
+            const float4 pk = *reinterpret_cast<const float4*>(prow + j4);
+            const float pj[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+#pragma unroll
+                for (int v = 0; v < 16; ++v) cur[v] = fmaf(pj[t], sS[j4 + t][v], cur[v]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -579,7 +651,7 @@ struct RevSm {
 constexpr int kRevSmem = 1024 + RevSm::END;
 
 __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
-                                                       TcWs ws, const __grid_constant__ CUtensorMap tm_do) {
+                                                       TcWs ws, const __grid_constant__ CUtensorMap tm_do, SegArg sg) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + RevSm::S;  // bf16 dS (128 x 128), later dDelta (64 x 128)
@@ -593,6 +665,12 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
+    // segment and mode: 0 checkpoints, 1 end state from zero, 2 transition (dO taken as zero)
+    const int m = sg.mode == kSegEnds ? (int)blockIdx.z % sg.M : (int)blockIdx.z;
+    const int mode = sg.mode == kSegEnds ? 1 + (int)blockIdx.z / sg.M : 0;
+    const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
+    if (sg.len && lo >= hi) return;
+    const bool ckpt = mode == 0, with_do = mode != 2;
 
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
@@ -601,21 +679,26 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     float S[64];
+    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
     {
-        const float* src = dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
+        const float* src = nullptr;
+        if (mode == 0) src = (hi == nts) ? (dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
+                                         : ws.seg_s0 + seg_at;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : (mode == 2 && 64 * vh + j == k ? 1.f : 0.f);
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
     auto issue1 = [&](int it) {  // operands of the first MMA group
         const int64_t ch = chunk(it);
-        mbar_expect_tx(&bars[0], 3 * TCD + TCC);
+        mbar_expect_tx(&bars[0], with_do ? 3 * TCD + TCC : TCD);
         bulk_load(sm + RevSm::KH, ws.kh + ch * TCD, TCD, &bars[0]);
-        bulk_load(sm + RevSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
-        bulk_load(sm + RevSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
-        const int row = (int)(bos + (int64_t)it * kC);
-        tma_load_3d(sm + RevSm::DO, &tm_do, 0, hv, row, &bars[0]);
-        tma_load_3d(sm + RevSm::DO + TCD / 2, &tm_do, 64, hv, row, &bars[0]);
+        if (with_do) {
+            bulk_load(sm + RevSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
+            bulk_load(sm + RevSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
+            const int row = (int)(bos + (int64_t)it * kC);
+            tma_load_3d(sm + RevSm::DO, &tm_do, 0, hv, row, &bars[0]);
+            tma_load_3d(sm + RevSm::DO + TCD / 2, &tm_do, 64, hv, row, &bars[0]);
+        }
     };
     auto issue2 = [&](int it) {  // w (second MMA group) and e^Gamma_C (state update)
         const int64_t ch = chunk(it);
@@ -628,14 +711,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
-    if (tid == 0 && nts > 0) {
-        issue1(nts - 1);
-        issue2(nts - 1);
+    if (tid == 0 && lo < hi) {
+        issue1(hi - 1);
+        issue2(hi - 1);
     }
     uint32_t mph = 0;
-    for (int it = nts - 1; it >= 0; --it) {
+    for (int it = hi - 1; it >= lo; --it) {
         const int64_t ch = chunk(it);
-        const uint32_t ph = (uint32_t)(nts - 1 - it) & 1;
+        const uint32_t ph = (uint32_t)(hi - 1 - it) & 1;
         // bf16 copy of dS (row k, this thread's 64 columns): MMA operand and the dS_out checkpoint
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
@@ -645,26 +728,30 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
             tc_fence_after();
             // dDelta = Aqk^T dO + K^ dS (chunk rows on TMEM lanes, M = 64, N = 128)
             const uint32_t ida = idesc_bf16(64, 128, true, true), idb = idesc_bf16(64, 128, false, true);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem, desc_mnmajor(smem_u32(sm + RevSm::AQK), kC, ks),
-                         desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), ida, ks > 0);
+            if (with_do)
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem, desc_mnmajor(smem_u32(sm + RevSm::AQK), kC, ks),
+                             desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), ida, ks > 0);
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + RevSm::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
-                         1);
+                         with_do || ks > 0);
             // dS accumulator = Q~s^T dO (M = 128, N = 128)
             const uint32_t idc = idesc_bf16(128, 128, true, true);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::QS), kC, ks),
-                         desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), idc, ks > 0);
+            if (with_do)
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::QS), kC, ks),
+                             desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), idc, ks > 0);
             mma_commit(&bars[2]);
-            bulk_store(ws.dso + ch * TDD, tS, TDD);
-            bulk_commit();
+            if (ckpt) {
+                bulk_store(ws.dso + ch * TDD, tS, TDD);
+                bulk_commit();
+            }
         }
         if (!wait_all(&bars[2], mph, ws.status, 32, fail)) break;
         mph ^= 1;
         if (tid == 0) {
-            if (it > 0) issue1(it - 1);  // the first group's operands are consumed
-            bulk_wait_read();            // the dS_out copy has read tS
+            if (it > lo) issue1(it - 1);  // the first group's operands are consumed
+            bulk_wait_read();             // the dS_out copy has read tS
         }
         __syncthreads();
         tc_fence_after();
@@ -689,15 +776,17 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
             const uint32_t id = idesc_neg_a(idesc_bf16(128, 128, true, true));
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::W), kC, ks), desc_mnmajor(smem_u32(tS), kC, ks),
-                         id, 1);
+                         id, with_do || ks > 0);
             mma_commit(&bars[2]);
-            bulk_store(ws.dvn + ch * TCD, tS, TCD);
-            bulk_commit();
+            if (ckpt) {
+                bulk_store(ws.dvn + ch * TCD, tS, TCD);
+                bulk_commit();
+            }
         }
         const float e = reinterpret_cast<const float*>(sm + RevSm::EGC)[k];
         if (!wait_all(&bars[2], mph, ws.status, 33, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it > 0) issue2(it - 1);  // w and e^Gamma_C are consumed
+        if (tid == 0 && it > lo) issue2(it - 1);  // w and e^Gamma_C are consumed
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -711,10 +800,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
         if (tid == 0) bulk_wait_read();  // the dDelta copy has read tS
         __syncthreads();
     }
-    if (dh0 && *(volatile int*)fail == 0) {
-        float* dst = dh0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
+    if (*(volatile int*)fail == 0) {
+        float* dst = mode == 1 ? ws.seg_e + seg_at
+                     : mode == 2 ? ws.seg_p + seg_at
+                     : (dh0 && lo == 0) ? dh0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh
+                                        : nullptr;
+        if (dst)
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[j] = S[j];
+            for (int j = 0; j < 64; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
@@ -1004,6 +1097,19 @@ cudaError_t set_smem(F* f, int bytes) {
 
 bool tc_path_ok(const Prob& p, bool bf16) { return bf16 && p.K == D && p.V == D; }
 
+// Dense batches whose (sequence, value head) sweeps cannot fill the GPU and whose sequences are long
+// run the state passes in segments: about 256 CTAs per pass (two per SM), at least 32 chunks each.
+SegPlan seg_plan(const Prob& p) {
+    SegPlan sp{0, 1};
+    const int64_t sweeps = (int64_t)p.B * p.HV;
+    if (p.cu || p.K != D || p.V != D || sweeps > 64 || p.NTs < 128) return sp;
+    int M = (int)(256 / sweeps);
+    M = M < 2 ? 2 : (M > p.NTs / 32 ? p.NTs / 32 : M);
+    sp.len = (p.NTs + M - 1) / M;
+    sp.M = (p.NTs + sp.len - 1) / sp.len;
+    return sp;
+}
+
 namespace {
 
 cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
@@ -1051,20 +1157,38 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
                                        (uint64_t)p.HV * D * 2, 64, 1, kC))
         return cudaErrorInvalidValue;
     if (stages >= 1 && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
+    const SegPlan sp = seg_plan(p);
+    const SegArg ends{sp.len, sp.M, kSegEnds}, ckpt{sp.len, sp.M, kSegCkpt}, whole{0, 1, kSegNone};
     if (stages >= 2) {
         if (io.states_in) {  // the forward's saved states: no sequential recompute
             if (p.NT > 0) {
                 k_tc_state_load<<<dim3((unsigned)p.NT, p.HV), 256, kLoadSmem, st>>>(p, io.states_in, ws);
                 note_launch("tc_state_load", st);
             }
+        } else if (sp.len) {  // two-level: segment ends and transitions, their chain, then the checkpoints
+            k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends);
+            note_launch("tc_state_fwd_seg", st);
+            k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
+            note_launch("tc_seg_combine", st);
+            k_tc_state_fwd<<<dim3(p.HV, p.N, sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ckpt);
+            note_launch("tc_state_fwd", st);
         } else {
-            k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, nullptr, nullptr, ws);
+            k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, whole);
             note_launch("tc_state_fwd", st);
         }
     }
     if (stages >= 3) {
-        k_tc_ds_rev<<<dim3(p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
-        note_launch("tc_ds_rev", st);
+        if (sp.len) {
+            k_tc_ds_rev<<<dim3(p.HV, p.N, 2 * sp.M), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, ends);
+            note_launch("tc_ds_rev_seg", st);
+            k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 1, io.dht, ws);
+            note_launch("tc_seg_combine", st);
+            k_tc_ds_rev<<<dim3(p.HV, p.N, sp.M), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, ckpt);
+            note_launch("tc_ds_rev", st);
+        } else {
+            k_tc_ds_rev<<<dim3(p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, whole);
+            note_launch("tc_ds_rev", st);
+        }
     }
     if (stages >= 4) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

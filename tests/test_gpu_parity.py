@@ -180,6 +180,17 @@ def test_saved_states_off_tensor_core_path_is_unsupported(kda):
     assert err.value.code == 2  # KDA_ERR_UNSUPPORTED
 
 
+def test_segmented_state_passes_long_sequence(kda):
+    """A dense batch with few (sequence, head) sweeps over long sequences runs both state passes in
+    segments (ends and transitions per segment, their chain, then the checkpoints): full parity."""
+    inp = kda_inputs.small(seed=38, B=1, T=8192 + 37, H=1, HV=2, K=128, V=128, dtype="bf16")
+    out = gpu_bwd(kda, inp)
+    lib = kda.load()
+    names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+    assert b"tc_state_fwd_seg" in names and b"tc_ds_rev_seg" in names, names
+    print("segmented", compare_full(inp, out, oracle.run_inputs(inp)))
+
+
 # ------------------------------------------------------- the five workloads
 
 @functools.lru_cache(maxsize=1)
