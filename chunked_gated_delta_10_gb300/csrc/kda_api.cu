@@ -75,6 +75,13 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_aqk = take(CH * TCC);
         L.t_inv = take(CH * TCC);
         L.t_egc = take(CH * 128 * f);
+        const SegPlan sp = seg_plan(p);
+        if (sp.len) {  // segmented state passes: three fp32 K x V matrices per (sequence, head, segment)
+            const size_t segs = (size_t)p.N * HV * sp.M * 128 * 128 * f;
+            L.t_seg_e = take(segs);
+            L.t_seg_p = take(segs);
+            L.t_seg_s0 = take(segs);
+        }
         if (pass == KDA_PASS_FWD) {  // the forward keeps the state and delta on chip
             L.total = off;
             return L;
@@ -83,13 +90,6 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_sin = take(CH * TDD);
         L.t_dvn = take(CH * TCD);
         L.t_dso = take(CH * TDD);
-        const SegPlan sp = seg_plan(p);
-        if (sp.len) {  // segmented state passes: three fp32 K x V matrices per (sequence, head, segment)
-            const size_t segs = (size_t)p.N * HV * sp.M * 128 * 128 * f;
-            L.t_seg_e = take(segs);
-            L.t_seg_p = take(segs);
-            L.t_seg_s0 = take(segs);
-        }
         if (p.HV != p.H) {
             L.dqp = take(R * HV * K * f);
             L.dkp = take(R * HV * K * f);

@@ -924,7 +924,8 @@ struct FoSm {
 constexpr int kFoSmem = 1024 + FoSm::END;
 
 __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
-                                                        float* __restrict__ states, bf16* __restrict__ o, TcWs ws) {
+                                                        float* __restrict__ states, bf16* __restrict__ o, TcWs ws,
+                                                        SegArg sg) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + FoSm::S;
@@ -939,6 +940,9 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
+    const int m = (int)blockIdx.z;  // segment (kSegCkpt) or the whole sequence (kSegNone)
+    const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
+    if (sg.len && lo >= hi) return;
 
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
@@ -948,7 +952,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     if (warp == 0) tmem_alloc(tslot, 256);
     float S[64];
     {
-        const float* src = h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr;
+        const float* src = lo == 0 ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
+                                   : ws.seg_s0 + (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
 #pragma unroll
         for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
     }
@@ -971,14 +976,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
-    if (tid == 0 && nts > 0) {
-        issue_w(0);
-        issue_g2(0);
+    if (tid == 0 && lo < hi) {
+        issue_w(lo);
+        issue_g2(lo);
     }
     uint32_t mph = 0;
-    for (int it = 0; it < nts; ++it) {
+    for (int it = lo; it < hi; ++it) {
         const int64_t ch = chunk(it);
-        const uint32_t ph = (uint32_t)it & 1;
+        const uint32_t ph = (uint32_t)(it - lo) & 1;
         // bf16 copy of S (row k, this thread's 64 columns): operand of the delta and output MMAs
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
@@ -999,7 +1004,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         }
         if (!wait_all(&bars[2], mph, ws.status, 72, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < nts) issue_w(it + 1);  // w is consumed
+        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w is consumed
         if (!wait_all(&bars[1], ph, ws.status, 73, fail)) break;
         tc_fence_after();
         const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);  // M = 64 row of this lane, column half
@@ -1044,7 +1049,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         const float e = reinterpret_cast<const float*>(sm + FoSm::EGC)[k];
         if (!wait_all(&bars[2], mph, ws.status, 74, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < nts) issue_g2(it + 1);  // K^, Q~s, u / delta, Aqk, e^Gamma_C are consumed
+        if (tid == 0 && it + 1 < hi) issue_g2(it + 1);  // K^, Q~s, u / delta, Aqk, e^Gamma_C are consumed
         tc_fence_after();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {  // state update
@@ -1078,7 +1083,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         }
         tc_fence_before();
     }
-    if (ht && *(volatile int*)fail == 0) {
+    if (ht && hi == nts && *(volatile int*)fail == 0) {
         float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
 #pragma unroll
         for (int j = 0; j < 64; ++j) dst[j] = S[j];
@@ -1139,8 +1144,18 @@ cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream
 cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
     if ((e = set_smem(k_tc_fwd_out, kFoSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
-    k_tc_fwd_out<<<dim3(p.HV, p.N), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws);
+    const SegPlan sp = seg_plan(p);
+    if (sp.len) {  // segment ends and transitions, their chain, then o per segment
+        const SegArg ends{sp.len, sp.M, kSegEnds};
+        k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends);
+        note_launch("tc_state_fwd_seg", st);
+        k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
+        note_launch("tc_seg_combine", st);
+    }
+    k_tc_fwd_out<<<dim3(p.HV, p.N, sp.M), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
+                                                              SegArg{sp.len, sp.M, sp.len ? kSegCkpt : kSegNone});
     note_launch("tc_fwd_out", st);
     return cudaGetLastError();
 }

@@ -191,6 +191,19 @@ def test_segmented_state_passes_long_sequence(kda):
     print("segmented", compare_full(inp, out, oracle.run_inputs(inp)))
 
 
+def test_segmented_forward_long_sequence(kda):
+    inp = kda_inputs.small(seed=39, B=1, T=8192 + 37, H=1, HV=2, K=128, V=128, dtype="bf16")
+    o, ht, st = gpu_fwd(kda, inp)
+    lib = kda.load()
+    names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+    assert b"tc_state_fwd_seg" in names, names
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
+                states=rel_l2(to64(st), ref["s_in"]))
+    print("segmented forward", errs)
+    assert all(e <= _tol(inp) for e in errs.values()), errs
+
+
 # ------------------------------------------------------- the five workloads
 
 @functools.lru_cache(maxsize=1)
