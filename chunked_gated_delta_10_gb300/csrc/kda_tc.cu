@@ -1,25 +1,31 @@
-// Tensor-core (tcgen05) kernels of the chunked KDA backward for bf16 inputs
-// with K = V = 128 and chunks of 64 tokens.
+// Tensor-core (tcgen05) kernels of the chunked KDA forward and backward for
+// bf16 inputs with K = V = 128 and chunks of 64 tokens.
 //
 // Stages (the same steps as the fp32 kernels in kda_simt.cu, regrouped so
 // that every dense product is a tcgen05.mma with bf16 operands and an fp32
 // accumulator in TMEM):
 //
-//   tc_intra      per (chunk, value head): gate cumsum in log2 units, the
-//                 decayed factors Kr = k e^(G-Gref), Qr = q e^(G-Gref),
-//                 Kc = k e^(Gref-G) (Gref = middle row of the chunk), one
-//                 MMA [Kr; Qr] Kc^T giving Akk and Aqk together, the inverse
-//                 INV = (I + Akk)^-1 by blocked forward substitution in fp32,
-//                 then w^T = (beta K~)^T INV^T and u^T = (beta V)^T INV^T.
-//                 Writes w, u, K^, scale*Q~, Aqk, INV and e^(Gamma_C).
-//   tc_state_fwd  per (sequence, value head): the chunk loop delta = u - w S,
-//                 S <- e^(Gamma_C) S + K^^T delta with S in registers (fp32)
-//                 and a bf16 copy in shared memory; writes S_in and delta of
-//                 every chunk.
-//   tc_ds_rev     per (sequence, value head), chunks in reverse:
+//   tc_intra      persistent, per (chunk, value head): gate cumsum in log2
+//                 units, the decayed factors Kr = k e^(G-Gref), Qr =
+//                 q e^(G-Gref), Kc = k e^(Gref-G) (Gref = middle row of the
+//                 chunk), one MMA [Kr; Qr] Kc^T giving Akk and Aqk together,
+//                 the inverse INV = (I + Akk)^-1 by blocked forward
+//                 substitution in fp32, then w = INV (beta K~) and
+//                 u = INV (beta V). Writes w, u, K^, scale*Q~, Aqk, INV and
+//                 e^(Gamma_C).
+//   tc_state_fwd  per (sequence, value head[, segment]): the chunk loop
+//                 delta = u - w S, S <- e^(Gamma_C) S + K^^T delta with S in
+//                 registers (fp32) and a bf16 copy in shared memory; writes
+//                 S_in and delta of every chunk (or, for segmented sweeps,
+//                 the segment's end state and transition).
+//   tc_ds_rev     per (sequence, value head[, segment]), chunks in reverse:
 //                 dDelta = Aqk^T dO + K^ dS,
 //                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
 //                 dDelta and dh0.
+//   tc_seg_combine   chains segment start states (long sequences).
+//   tc_state_load the backward's state pass from the forward's saved states.
+//   tc_fwd_out    the forward: the state pass with o = (scale Q~) S + Aqk
+//                 delta formed in the same MMA group.
 //
 // Intermediates live in the workspace as bf16 tiles in exactly the
 // shared-memory operand layout of tc_util.cuh (row-major, 64-column blocks,

@@ -1,7 +1,8 @@
 // Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
 // K = V = 128, chunks of 64), and the grouped-value-head reduction.
 //
-// One CTA per (chunk, value head), 512 threads. Inputs: q, k, v, dO (TMA),
+// Persistent: one 512-thread CTA per SM walks (chunk, value head) items and
+// prefetches the next item's inputs. Inputs: q, k, v, dO, g (TMA),
 // and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
 // (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
 // Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
@@ -19,8 +20,7 @@
 // T stands for dINV INV^T with dINV = (P + R) diag(beta) = (d_delta V^T +
 // dw K~^T) diag(beta): since INV diag(beta) V = u, INV diag(beta) K~ = w,
 // dw = -d_delta S_in^T and delta = u - w S_in, it equals d_delta delta^T and
-// needs no dINV product of its own.
-// where dN = scale tril0(dAqk) and dM = diag(beta) tril-1(dAkk). The
+// needs no dINV product of its own. Here dN = scale tril0(dAqk) and dM = diag(beta) tril-1(dAkk). The
 // epilogues give dv = beta dXv and dbeta = sum_j INV[j,r] PR[j,r] +
 // sum_j dAkk[r,j] Mkk[r,j] per chunk row (row-per-thread layout), and per key
 // channel (channel-per-thread layout) dq, dk and dGamma, whose reverse
