@@ -138,8 +138,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
 # B=2 case of the benchmark workload and scaled by chunk-heads; reported only while the kernel's
 # source file is unchanged since that capture (sha1 prefix).
 MEASURED_TRAFFIC = {
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "2880f8cbf283",
-                 "bytes_per_chunk_head": (841.629952e6 + 300.759808e6) / 4096},
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "8ee91c909056",
+                 "bytes_per_chunk_head": (841.620992e6 + 300.658176e6) / 4096},
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "16f27449290f",
+                 "bytes_per_chunk_head": (336.209152e6 + 283.242752e6) / 4096},
 }
 
 
@@ -436,7 +438,7 @@ def gpu_arm(args):
         ach, pk, unit = aflops / avg / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
     else:
         ach, pk, unit = aflops / avg / 1e12, alu_peak_tflops(clk.get("sm_mhz") or peaks["sm_max_mhz"]), "TFLOP/s"
-    traffic = measured_traffic(dom, step_cost(B, T, H, HV, K, V)["nck"]) if mode == "bwd" else None
+    traffic = measured_traffic(dom, step_cost(B, T, H, HV, K, V)["nck"])
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
                 "traffic": traffic, "peak_source": peak_src if bound != "alu" else "152 SMs x 128 FFMA lanes x SM clock",
                 "avg_launch_ms": avg * 1e3, "share": tot[dom] / sum(tot.values()),
