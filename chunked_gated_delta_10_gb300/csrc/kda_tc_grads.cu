@@ -55,8 +55,8 @@ struct GS {
     static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, TT = DM + 2 * TCC;  // DM .. TT: g tile part
     // the g tile (64 x 128 fp32) of a chunk lands on DN .. TT, which the previous chunk no longer needs after phase E
     static constexpr int GT = DN;
-    static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048, NXT = BARS + 64;
-    static constexpr int END = NXT + 64;
+    static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048;
+    static constexpr int END = BARS + 128;
     // scratch in the dw tile while that tile is dead: cumsum quarter totals and the reference / last-row gates
     // (chunk start), dbeta partials (epilogues B and D), Gamma_C terms and dg quarter totals (final epilogue)
     static constexpr int XTOT = DW, XRG = DW + 2048, XDB = DW + 4096, XGC = DW + 8192, XT1 = DW + 10240;
@@ -83,41 +83,44 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
     return it;
 }
 
-// Persistent, 512 threads, one CTA per SM. Channel-oriented work: thread (d = tid % 128,
-// quarter = tid / 128) owns key channel d for chunk rows 16 * quarter .. 16 * quarter + 15.
-// Row-oriented work on M = 64 accumulators: row r = 16 * (warp % 4) + lane (lane < 16),
-// column quarter warp / 4. Every cross-thread sum is combined in a fixed order. The
-// inputs of the next item are fetched in five groups, each as soon as the current item's
-// phases have consumed its regions: dO, delta after phase A; q, k after the factor pass;
-// v, d_delta after phase B; INV after phase D; S_in, dS_out, g and e^Gamma_C after phase E.
-__global__ void __launch_bounds__(512, 1)
+// Persistent, one CTA per SM: 512 SIMT threads (warps 0..15) and one producer warp (warp 16).
+// The producer's lane 0 issues every TMA copy and tensor-core MMA; an MMA's issue runs only a
+// couple of instructions ahead of its execution, so the issuing thread is held for about the
+// length of a phase, and in a warp of its own it holds nobody else. The SIMT threads meet on
+// barrier 1 (group_sync<512>). Barriers between the two: inputs of an item (by item parity),
+// phase A / B / E MMAs complete, operands of phase B / phase E written, and the accumulators
+// of the final epilogue read (TMEM free): phase A of the next item then runs while the SIMT
+// threads finish the current one.
+// Channel-oriented work: thread (d = tid % 128, quarter = tid / 128) owns key channel d for chunk
+// rows 16 * quarter .. 16 * quarter + 15. Row-oriented work on M = 64 accumulators: row r =
+// 16 * (warp % 4) + lane (lane < 16), column quarter warp / 4. Every cross-thread sum is
+// combined in a fixed order. The inputs of the next item are fetched in five groups, each as
+// soon as the current item's phases have consumed its regions: dO, delta after phase A; q, k
+// after the factor pass; v, d_delta after phase B; INV after epilogue B/D; S_in, dS_out, g and
+// e^Gamma_C after phase E.
+constexpr int kSimt = 512, kProducerWarp = kSimt / 32, kGradsThreads = kSimt + 32;
+
+__global__ void __launch_bounds__(kGradsThreads, 1)
     k_tc_grads(Prob p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out, bf16* __restrict__ dk_out,
                bf16* __restrict__ dv_out, float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws,
                const __grid_constant__ GradMaps maps) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
-    float* xtot = reinterpret_cast<float*>(sm + GS::XTOT);
-    float* xrg = reinterpret_cast<float*>(sm + GS::XRG);
-    float* xrd = reinterpret_cast<float*>(sm + GS::XRD);
-    float* xgc = reinterpret_cast<float*>(sm + GS::XGC);
-    float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
-    float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
-    const float* gt = reinterpret_cast<const float*>(sm + GS::GT);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);  // [0, 1] inputs (by item parity), [2] mma
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
-    int* fail = reinterpret_cast<int*>(tslot + 1);
-    Item* nx = reinterpret_cast<Item*>(sm + GS::NXT);  // the next item of this CTA (written by thread 0)
+    // [0, 1] inputs (by item parity); [2] phase A, [3] phase B, [4] phase E complete; operands
+    // written: [8] of phase B's first part, [5] of its second part, [6] of phase E; [7] accumulators read
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 9);
+    int* fail = reinterpret_cast<int*>(tslot + 1);  // written by SIMT warp 0 only
     auto S = [&](int off) { return smem_u32(sm + off); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = tid & 127, qtr = tid >> 7, q4 = warp & 3, cq = warp >> 2;
     const int HV = p.HV, H = p.H, G = HV / H;
     const int64_t total = p.NT * HV;
 
     if (tid == 0) {
         mbar_init(&bars[0], 5);
         mbar_init(&bars[1], 5);
-        mbar_init(&bars[2], 1);
+        for (int x = 2; x < 9; ++x) mbar_init(&bars[x], x == 7 ? kSimt / 32 : 1);
         fence_mbar_init();
         *fail = 0;
     }
@@ -126,365 +129,430 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
-    const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
-    const bool rv = lane < 16;
 
-    // the five input groups of an item into input barrier `b` (issued by thread 0)
-    auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta
-        mbar_expect_tx(b, 2 * TCD);
-        tma_load_3d(sm + GS::DO, &maps.d_o, 0, n.hv, (int)n.r0, b);
-        tma_load_3d(sm + GS::DO + TCD / 2, &maps.d_o, 64, n.hv, (int)n.r0, b);
-        bulk_load(sm + GS::DL, ws.vn + n.ch * TCD, TCD, b);
-    };
-    auto issue_qk = [&](const Item& n, uint64_t* b) {
-        mbar_expect_tx(b, 2 * TCD);
-        for (int x = 0; x < 2; ++x) {
-            tma_load_3d(sm + GS::Q + x * (TCD / 2), &maps.q, 64 * x, n.h, (int)n.r0, b);
-            tma_load_3d(sm + GS::K + x * (TCD / 2), &maps.k, 64 * x, n.h, (int)n.r0, b);
-        }
-    };
-    auto issue_b = [&](const Item& n, uint64_t* b) {  // v, d_delta
-        mbar_expect_tx(b, 2 * TCD);
-        tma_load_3d(sm + GS::V, &maps.v, 0, n.hv, (int)n.r0, b);
-        tma_load_3d(sm + GS::V + TCD / 2, &maps.v, 64, n.hv, (int)n.r0, b);
-        bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD, b);
-    };
-    auto issue_d = [&](const Item& n, uint64_t* b) {  // INV
-        mbar_expect_tx(b, TCC);
-        bulk_load(sm + GS::INV, ws.inv + n.ch * TCC, TCC, b);
-    };
-    auto issue_e = [&](const Item& n, uint64_t* b, int slot) {  // S_in, dS_out, g, e^Gamma_C
-        mbar_expect_tx(b, 2 * TDD + kC * D * 4 + 512);
-        bulk_load(sm + GS::SIN, ws.sin + n.ch * TDD, TDD, b);
-        bulk_load(sm + GS::DSO, ws.dso + n.ch * TDD, TDD, b);
-        tma_load_3d(sm + GS::GT, &maps.g, 0, n.hv, (int)n.r0, b);
-        bulk_load(sm + GS::EGC + 512 * slot, ws.egc + n.ch * D, 512, b);
-    };
-
-    int64_t w = blockIdx.x;
-    Item cur = make_item(p, w < total ? w : 0, w < total);
-    const ColAddr ad(d, kC);  // this thread's column in the 64-row q / k tiles
-    if (tid < kC) {
-        float* sb = reinterpret_cast<float*>(sm + GS::BETA);
-        sb[tid] = (w < total && tid < cur.c) ? __bfloat162float(beta[(cur.r0 + tid) * HV + cur.hv]) : 0.f;
-    }
-    if (tid == 0 && w < total) {
-        issue_a(cur, &bars[0]);
-        issue_qk(cur, &bars[0]);
-        issue_b(cur, &bars[0]);
-        issue_d(cur, &bars[0]);
-        issue_e(cur, &bars[0], 0);
-    }
-    uint32_t mph = 0;
-    for (int i = 0; w < total; ++i, w += gridDim.x) {
-        const int slot = i & 1;
-        if (tid == 0) {
-            const int64_t wn = w + gridDim.x;
-            *nx = make_item(p, wn < total ? wn : w, wn < total);
-        }
-        uint64_t* nbar = &bars[slot ^ 1];
-        const float* sbeta = reinterpret_cast<const float*>(sm + GS::BETA + 256 * slot);
-        const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
-        const int64_t r0 = cur.r0;
-        const int c = cur.c, hv = cur.hv, h = cur.h;
-        if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 41, fail)) break;
-        const bool has_next = nx->valid != 0;
-        // beta of the next item: loaded now, stored to its shared slot at the end of this item
-        const float nbeta =
-            (has_next && tid < nx->c) ? __bfloat162float(beta[(nx->r0 + tid) * HV + nx->hv]) : 0.f;
-        if (tid == 0) {  // phase A (needs no gate values: the cumsum below runs while it executes)
-            tc_fence_after();
-            const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
-                           i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks), i128, ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks), i128, ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
-                         idesc_neg_a(i64n), ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
-                         ks > 0);
-            // T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T + dw w^T, and with
-            // dw = -d_delta S_in^T and delta = u - w S_in this is d_delta delta^T
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 448, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::DL), kC, ks), i64, ks > 0);
-            mma_commit(&bars[2]);
-        }
-        // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
-        float G2[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-            const int r = 16 * qtr + x;
-            G2[x] = r < c ? gt[r * D + d] : 0.f;
-        }
-        quarter_cumsum_log2<1>(G2, d, qtr, xtot, G2);
-        const int rmid = (c - 1) >> 1;
-#pragma unroll
-        for (int x = 0; x < 16; ++x) {
-            if (16 * qtr + x == rmid) xrg[d] = G2[x];
-            if (16 * qtr + x == c - 1) xrg[128 + d] = G2[x];
-        }
-        __syncthreads();
-        const float ref = xrg[d], gC = xrg[128 + d];
-        // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
-        // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
-        const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
-
-        float rd = 0.f;
-#pragma unroll
-        for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
-            const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
-            const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
-            const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
-                rd = fmaf(fa.x, fb.x, rd);
-                rd = fmaf(fa.y, fb.y, rd);
+    if (warp == kProducerWarp) {
+        if (lane == 0) {  // the producer thread; lanes 1 .. 31 wait at the warp barrier below
+            auto pwait = [&](uint64_t* b, uint32_t parity, int code) { return mbar_wait(b, parity, ws.status, code); };
+            // the five input groups of an item into input barrier `b`
+            auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta
+                mbar_expect_tx(b, 2 * TCD);
+                tma_load_3d(sm + GS::DO, &maps.d_o, 0, n.hv, (int)n.r0, b);
+                tma_load_3d(sm + GS::DO + TCD / 2, &maps.d_o, 64, n.hv, (int)n.r0, b);
+                bulk_load(sm + GS::DL, ws.vn + n.ch * TCD, TCD, b);
+            };
+            auto issue_qk = [&](const Item& n, uint64_t* b) {
+                mbar_expect_tx(b, 2 * TCD);
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(sm + GS::Q + x * (TCD / 2), &maps.q, 64 * x, n.h, (int)n.r0, b);
+                    tma_load_3d(sm + GS::K + x * (TCD / 2), &maps.k, 64 * x, n.h, (int)n.r0, b);
+                }
+            };
+            auto issue_b = [&](const Item& n, uint64_t* b) {  // v, d_delta
+                mbar_expect_tx(b, 2 * TCD);
+                tma_load_3d(sm + GS::V, &maps.v, 0, n.hv, (int)n.r0, b);
+                tma_load_3d(sm + GS::V + TCD / 2, &maps.v, 64, n.hv, (int)n.r0, b);
+                bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD, b);
+            };
+            auto issue_d = [&](const Item& n, uint64_t* b) {  // INV
+                mbar_expect_tx(b, TCC);
+                bulk_load(sm + GS::INV, ws.inv + n.ch * TCC, TCC, b);
+            };
+            auto issue_e = [&](const Item& n, uint64_t* b, int slot) {  // S_in, dS_out, g, e^Gamma_C
+                mbar_expect_tx(b, 2 * TDD + kC * D * 4 + 512);
+                bulk_load(sm + GS::SIN, ws.sin + n.ch * TDD, TDD, b);
+                bulk_load(sm + GS::DSO, ws.dso + n.ch * TDD, TDD, b);
+                tma_load_3d(sm + GS::GT, &maps.g, 0, n.hv, (int)n.r0, b);
+                bulk_load(sm + GS::EGC + 512 * slot, ws.egc + n.ch * D, 512, b);
+            };
+            int64_t w = blockIdx.x;
+            {
+                const Item first = make_item(p, w, true);
+                issue_a(first, &bars[0]);
+                issue_qk(first, &bars[0]);
+                issue_b(first, &bars[0]);
+                issue_d(first, &bars[0]);
+                issue_e(first, &bars[0], 0);
             }
+            int i = 0;
+            bool pending = false;  // copies of the next item issued and not yet waited for
+            for (; w < total; ++i, w += gridDim.x) {
+                const int slot = i & 1;
+                const uint32_t par = (uint32_t)i & 1;
+                const int64_t wn = w + gridDim.x;
+                const bool has_next = wn < total;
+                const Item nx = make_item(p, has_next ? wn : w, has_next);
+                uint64_t* nbar = &bars[slot ^ 1];
+                pending = false;
+                if (!pwait(&bars[slot], (uint32_t)(i >> 1) & 1, 51)) break;
+                if (i > 0 && !pwait(&bars[7], par ^ 1, 52)) break;  // the last item's accumulators are read
+                {  // phase A
+                    tc_fence_after();
+                    const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
+                                   i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks),
+                                 i128, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks),
+                                 i128, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
+                                 idesc_neg_a(i64n), ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks),
+                                 i64, ks > 0);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
+                                 ks > 0);
+                    // T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T + dw w^T, and with
+                    // dw = -d_delta S_in^T and delta = u - w S_in this is d_delta delta^T
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 448, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::DL), kC, ks),
+                                 i64, ks > 0);
+                    mma_commit(&bars[2]);
+                }
+                if (!pwait(&bars[2], par, 53)) break;
+                if (has_next) issue_a(nx, nbar);  // dO and delta are consumed
+                pending = has_next;
+                if (!pwait(&bars[8], par, 54)) break;  // dw, dN, T written
+                {  // phase B, first part (operands from epilogue A): PR^T = V d_delta^T,
+                           // dAkk = -INV^T T (phase D), dXk^T = dw^T INV
+                    tc_fence_after();
+                    const uint32_t i64 = idesc_bf16(64, 64, false, false);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks),
+                                 i64, ks > 0);
+                    const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, true));
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd,
+                                 ks > 0);
+                    const uint32_t ixk = idesc_bf16(128, 64, true, true);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk,
+                                 ks > 0);
+                }
+                if (!pwait(&bars[5], par, 58)) break;  // factor tiles written
+                {  // phase B, second part (factor tiles): PR^T += K~ dw^T, Mkk = Kr Kc^T, dQr^T = Kc^T dN^T
+                    tc_fence_after();
+                    if (has_next) issue_qk(nx, nbar);  // q and k are consumed
+                    const uint32_t i64t = idesc_bf16(64, 64, true, false), i64tt = idesc_bf16(64, 64, true, true);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt,
+                                 ks > 0);
+                    const uint32_t imk = idesc_bf16(128, 64, false, false);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks),
+                                 imk, ks > 0);
+                    mma_commit(&bars[3]);
+                }
+                if (!pwait(&bars[3], par, 55)) break;
+                if (has_next) issue_b(nx, nbar);  // v and d_delta are consumed
+                if (!pwait(&bars[6], par, 56)) break;  // dM written, INV read
+                {  // phase E
+                    tc_fence_after();
+                    if (has_next) issue_d(nx, nbar);  // INV is consumed
+                    const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks),
+                                 im, ks > 0);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+                    mma_commit(&bars[4]);
+                }
+                if (!pwait(&bars[4], par, 57)) break;
+                if (has_next) issue_e(nx, nbar, slot ^ 1);  // factor tiles, dN, dM, T are consumed
+                pending = false;
+            }
+            // after a failed wait: let copies already issued land before the block exits (bounded)
+            if (pending) mbar_wait(&bars[(i & 1) ^ 1], (uint32_t)((i + 1) >> 1) & 1, nullptr, 0, 2000000);
         }
-        xrd[qtr * 128 + d] = rd;
-        if (!wait_all(&bars[2], mph, ws.status, 42, fail)) break;
-        mph ^= 1;
-        if (tid == 0 && has_next) issue_a(*nx, nbar);  // dO and delta are consumed
-        tc_fence_after();
-        {  // epilogue A: dw row segment (32 columns), dN row segment (16 columns), dv row segment (32 columns)
-            const float br = rv ? sbeta[rrow] : 0.f;
-            float x[32];
-            tmem_ld32(tmem + lb + 128 + 32 * cq, x);
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 4; ++u) st_tile_row8(sm + GS::DW, rrow, 32 * cq + 8 * u, kC, x + 8 * u);
-            tmem_ld16(tmem + lb + 256 + 16 * cq, x);
-            tmem_ld_wait();
+        __syncwarp();
+    } else {
+        float* xtot = reinterpret_cast<float*>(sm + GS::XTOT);
+        float* xrg = reinterpret_cast<float*>(sm + GS::XRG);
+        float* xrd = reinterpret_cast<float*>(sm + GS::XRD);
+        float* xgc = reinterpret_cast<float*>(sm + GS::XGC);
+        float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
+        float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
+        const float* gt = reinterpret_cast<const float*>(sm + GS::GT);
+        const int d = tid & 127, qtr = tid >> 7, q4 = warp & 3, cq = warp >> 2;
+        const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
+        const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
+        const bool rv = lane < 16;
+        int64_t w = blockIdx.x;
+        if (tid < kC) {
+            const Item first = make_item(p, w, true);
+            float* sb = reinterpret_cast<float*>(sm + GS::BETA);
+            sb[tid] = tid < first.c ? __bfloat162float(beta[(first.r0 + tid) * HV + first.hv]) : 0.f;
+        }
+        for (int i = 0; w < total; ++i, w += gridDim.x) {
+            const int slot = i & 1;
+            const uint32_t par = (uint32_t)i & 1;
+            const Item cur = make_item(p, w, true);
+            const int64_t wn = w + gridDim.x;
+            const float* sbeta = reinterpret_cast<const float*>(sm + GS::BETA + 256 * slot);
+            const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
+            const int64_t r0 = cur.r0;
+            const int c = cur.c, hv = cur.hv, h = cur.h;
+            if (!wait_group<kSimt>(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 41, fail)) break;
+            // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
+            float G2[16];
 #pragma unroll
-            for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
-            if (rv)
-                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-            tmem_ld16(tmem + lb + 448 + 16 * cq, x);  // T rows (bf16 operand of phase D)
-            tmem_ld_wait();
-            if (rv)
-                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-            tmem_ld32(tmem + lb + 320 + 32 * cq, x);
-            tmem_ld_wait();
-            if (rv && rrow < c) {
-                bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D + 32 * cq;
+            for (int x = 0; x < 16; ++x) {
+                const int r = 16 * qtr + x;
+                G2[x] = r < c ? gt[r * D + d] : 0.f;
+            }
+            quarter_cumsum_log2<1, kSimt>(G2, d, qtr, xtot, G2);
+            const int rmid = (c - 1) >> 1;
 #pragma unroll
-                for (int u = 0; u < 32; u += 8) {
-                    uint4 vv;
-                    vv.x = pack2(br * x[u], br * x[u + 1]);
-                    vv.y = pack2(br * x[u + 2], br * x[u + 3]);
-                    vv.z = pack2(br * x[u + 4], br * x[u + 5]);
-                    vv.w = pack2(br * x[u + 6], br * x[u + 7]);
-                    *reinterpret_cast<uint4*>(dvrow + u) = vv;
+            for (int x = 0; x < 16; ++x) {
+                if (16 * qtr + x == rmid) xrg[d] = G2[x];
+                if (16 * qtr + x == c - 1) xrg[128 + d] = G2[x];
+            }
+            group_sync<kSimt>();
+            const float ref = xrg[d], gC = xrg[128 + d];
+            // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
+            // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
+            const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
+
+            float rd = 0.f;
+#pragma unroll
+            for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
+                const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
+                const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
+                const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+                const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
+                    rd = fmaf(fa.x, fb.x, rd);
+                    rd = fmaf(fa.y, fb.y, rd);
                 }
             }
-        }
-        tc_fence_before();
-        __syncthreads();  // every warp has read dXv before its columns take the q, k stash
-        tc_fence_after();
-        // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
-        // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). The raw
-        // (k, q) pairs go to TMEM columns 384 + 16 quarter .. +15 for the final epilogue.
-#pragma unroll
-        for (int h8 = 0; h8 < 2; ++h8) {
-            float kr[8], kc[8], qr[8], kt[8];
-            uint32_t kq[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                const int r = 16 * qtr + 8 * h8 + x;
-                const bool in = r < c;
-                const uint32_t kbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
-                const uint32_t qbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
-                kq[x] = kbits | (qbits << 16);
-                const float kv = __uint_as_float(kbits << 16), qv = __uint_as_float(qbits << 16);
-                const float gm = G2[8 * h8 + x];
-                const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
-                kr[x] = kv * ep;
-                kc[x] = kv * em;
-                qr[x] = qv * ep;
-                kt[x] = kv * E;
-            }
-            const int c0 = 16 * qtr + 8 * h8;
-            st_tile_row8(sm + GS::KR, d, c0, D, kr);
-            st_tile_row8(sm + GS::KC, d, c0, D, kc);
-            st_tile_row8(sm + GS::QR, d, c0, D, qr);
-            st_tile_row8(sm + GS::KT, d, c0, D, kt);
-            tmem_st8(tmem + lb + 384 + (uint32_t)c0, kq);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {  // phase B, and phase D: dAkk = -INV^T T
+            xrd[qtr * 128 + d] = rd;
+            if (!wait_group<kSimt>(&bars[2], par, ws.status, 42, fail)) break;
             tc_fence_after();
-            if (has_next) issue_qk(*nx, nbar);  // q and k are consumed
-            const uint32_t i64 = idesc_bf16(64, 64, false, false), i64t = idesc_bf16(64, 64, true, false),
-                           i64tt = idesc_bf16(64, 64, true, true);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks), i64, ks > 0);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
-            for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt, ks > 0);
-            const uint32_t imk = idesc_bf16(128, 64, false, false);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk, ks > 0);
-            const uint32_t ixk = idesc_bf16(128, 64, true, true);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk, ks > 0);
-            const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, true));
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd, ks > 0);
-            mma_commit(&bars[2]);
-        }
-        if (!wait_all(&bars[2], mph, ws.status, 43, fail)) break;
-        mph ^= 1;
-        if (tid == 0 && has_next) issue_b(*nx, nbar);  // v and d_delta are consumed
-        tc_fence_after();
-        {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
-            const float br = rv ? sbeta[rrow] : 0.f;
-            float x[16], a[16], m[16];
-            float db = 0.f, db2 = 0.f;
-            tmem_ld16(tmem + lb + 128 + 16 * cq, x);
-            tmem_ld16(tmem + lb + 320 + 16 * cq, a);
-            tmem_ld16(tmem + lb + 192 + 16 * cq, m);
-            tmem_ld_wait();
-            if (rv) {
-                const ColAddr ar(rrow, kC);
+            {  // epilogue A: dw row segment (32 columns), dN row segment (16 columns), dv row segment (32 columns)
+                const float br = rv ? sbeta[rrow] : 0.f;
+                float x[16];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) db = fmaf(ld_col(sm + GS::INV, ar, 16 * cq + u), x[u], db);
-            }
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int j = 16 * cq + u;
-                const bool in = j < rrow && rrow < c;
-                db2 = in ? fmaf(a[u], m[u], db2) : db2;
-                a[u] = in ? br * a[u] : 0.f;
-            }
-            if (rv) {
-                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DM, rrow, 16 * cq + 8 * u, kC, a + 8 * u);
-                xdb[cq * 64 + rrow] = db;
-                xdb[256 + cq * 64 + rrow] = db2;
-            }
-        }
-        tc_fence_before();
-        fence_async_smem();
-        __syncthreads();
-        if (tid == 0 && has_next) issue_d(*nx, nbar);  // INV is consumed
-        if (tid < kC && tid < c)
-            db_out[(r0 + tid) * HV + hv] =
-                __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
-                                    ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
-        if (tid == 0) {  // phase E
-            tc_fence_after();
-            const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks), im, ks > 0);
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
-            mma_commit(&bars[2]);
-        }
-        if (!wait_all(&bars[2], mph, ws.status, 46, fail)) break;
-        mph ^= 1;
-        if (tid == 0 && has_next) issue_e(*nx, nbar, slot ^ 1);  // factor tiles, dN, dM, dINV, T are consumed
-        tc_fence_after();
-        {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
-            float dG[16];
-            float dGC = 0.f;
-            const float sc = p.scale, sce = p.scale * e_ref;
-            // this thread's first output row and the row stride of dq / dk (or of the per-value-head partials)
-            const int HO = G == 1 ? H : HV;
-            const int64_t o0 = ((r0 + 16 * qtr) * HO + (G == 1 ? h : hv)) * D + d, rs = (int64_t)HO * D;
-#pragma unroll
-            for (int rb = 0; rb < 2; ++rb) {
-                const uint32_t cb = (uint32_t)(16 * qtr + 8 * rb);
-                float aQt[8], aKh[8], aKr[8], aKc[8], aQr[8], aXk[8];
-                uint32_t kq[8];
-                tmem_ld8(tmem + lb + 0 + cb, aQt);
-                tmem_ld8(tmem + lb + 64 + cb, aKh);
-                tmem_ld8(tmem + lb + 128 + cb, aKr);
-                tmem_ld8(tmem + lb + 192 + cb, aKc);
-                tmem_ld8(tmem + lb + 256 + cb, aQr);
-                tmem_ld8(tmem + lb + 448 + cb, aXk);
-                tmem_ld8u(tmem + lb + 384 + cb, kq);
+                for (int hh = 0; hh < 2; ++hh) {
+                    tmem_ld16(tmem + lb + 128 + 32 * cq + 16 * hh, x);
+                    tmem_ld_wait();
+                    if (rv)
+                        for (int u = 0; u < 2; ++u)
+                            st_tile_row8(sm + GS::DW, rrow, 32 * cq + 16 * hh + 8 * u, kC, x + 8 * u);
+                }
+                tmem_ld16(tmem + lb + 256 + 16 * cq, x);
                 tmem_ld_wait();
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    const int ii = 8 * rb + x, r = 16 * qtr + ii;
-                    const bool in = r < c;
-                    const float kv = __uint_as_float(kq[x] << 16), qv = __uint_as_float(kq[x] & 0xffff0000u);
-                    const float gm = G2[ii];
-                    const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
-                    const float bX = sbeta[r] * aXk[x];
-                    // dq = E scale dQ~ + ep dQr;  dk = eh dK^ + E beta dXk + ep dKr + em dKc
-                    const float dqv = ep * fmaf(sce, aQt[x], aQr[x]);
-                    const float dkv = fmaf(ep, fmaf(e_ref, bX, aKr[x]), em * fmaf(e_cr, aKh[x], aKc[x]));
-                    const float khk = aKh[x] * (kv * eh);
-                    // The factor values of the dGamma pair terms are the bf16 values the MMAs used (rounded
-                    // two at a time here as in the factor tiles), so that each in-chunk pair's contributions
-                    // to its two rows cancel in the chunk sum as they do exactly.
-                    const uint32_t p1 = pack2(kv * E, qv * ep), p2 = pack2(kv * ep, kv * em);
-                    const float kt_b = __uint_as_float(p1 << 16), qr_b = __uint_as_float(p1 & 0xffff0000u);
-                    const float kr_b = __uint_as_float(p2 << 16), kc_b = __uint_as_float(p2 & 0xffff0000u);
-                    float dgv = fmaf(sc * aQt[x], qv * E, -khk);
-                    dgv = fmaf(bX, kt_b, dgv);
-                    dgv = fmaf(aQr[x], qr_b, dgv);
-                    dgv = fmaf(aKr[x], kr_b, dgv);
-                    dgv = fmaf(-aKc[x], kc_b, dgv);
-                    dG[ii] = in ? dgv : 0.f;
-                    if (in) {
-                        dGC += khk;
-                        const int64_t o = o0 + ii * rs;
-                        if (G == 1) {
-                            st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o),
-                                         reinterpret_cast<uint8_t*>(dk_out + o), dqv, dkv);
-                        } else {
-                            ws.dqp[o] = dqv;
-                            ws.dkp[o] = dkv;
+                for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
+                if (rv)
+                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+                tmem_ld16(tmem + lb + 448 + 16 * cq, x);  // T rows (bf16 operand of phase D)
+                tmem_ld_wait();
+                if (rv)
+                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    tmem_ld16(tmem + lb + 320 + 32 * cq + 16 * hh, x);
+                    tmem_ld_wait();
+                    if (rv && rrow < c) {
+                        bf16* dvrow = dv_out + ((r0 + rrow) * HV + hv) * D + 32 * cq + 16 * hh;
+#pragma unroll
+                        for (int u = 0; u < 16; u += 8) {
+                            uint4 vv;
+                            vv.x = pack2(br * x[u], br * x[u + 1]);
+                            vv.y = pack2(br * x[u + 2], br * x[u + 3]);
+                            vv.z = pack2(br * x[u + 4], br * x[u + 5]);
+                            vv.w = pack2(br * x[u + 6], br * x[u + 7]);
+                            *reinterpret_cast<uint4*>(dvrow + u) = vv;
                         }
                     }
                 }
             }
-            // dg = reverse in-chunk cumsum of dGamma, whose last valid row also takes the Gamma_C terms
-            // dGCt: in-quarter suffix sums and quarter totals first (one exchange), then per row the later
-            // quarters' totals (added in the order 3, 2, 1) and dGCt where row c - 1 lies at or after it.
-            float run = 0.f;
+            tc_fence_before();
+            fence_async_smem();
+            group_sync<kSimt>();  // every warp has read dXv before its columns take the q, k stash
+            if (tid == 0) mbar_arrive(&bars[8]);  // operands of phase B's first part are in place
+            tc_fence_after();
+            // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
+            // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). The raw
+            // (k, q) pairs go to TMEM columns 384 + 16 quarter .. +15 for the final epilogue.
+            const ColAddr ad(d, kC);  // this thread's column in the 64-row q / k tiles
 #pragma unroll
-            for (int x = 15; x >= 0; --x) {
-                run += dG[x];
-                dG[x] = run;
-            }
-            xgc[qtr * 128 + d] = dGC;
-            xt1[qtr * 128 + d] = run;
-            __syncthreads();
-            const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
-                               ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
-            const int qc = (c - 1) >> 4, xc = (c - 1) & 15;
-            float carry = 0.f;
-            for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
-            if (qc > qtr) carry += dGCt;
+            for (int h8 = 0; h8 < 2; ++h8) {
+                float kr[8], kc[8], qr[8], kt[8];
+                uint32_t kq[8];
 #pragma unroll
-            for (int x = 0; x < 16; ++x) {
-                const int r = 16 * qtr + x;
-                const float t = (qc == qtr && x <= xc) ? dG[x] + dGCt : dG[x];
-                if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = t + carry;
+                for (int x = 0; x < 8; ++x) {
+                    const int r = 16 * qtr + 8 * h8 + x;
+                    const bool in = r < c;
+                    const uint32_t kbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
+                    const uint32_t qbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
+                    kq[x] = kbits | (qbits << 16);
+                    const float kv = __uint_as_float(kbits << 16), qv = __uint_as_float(qbits << 16);
+                    const float gm = G2[8 * h8 + x];
+                    const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
+                    kr[x] = kv * ep;
+                    kc[x] = kv * em;
+                    qr[x] = qv * ep;
+                    kt[x] = kv * E;
+                }
+                const int c0 = 16 * qtr + 8 * h8;
+                st_tile_row8(sm + GS::KR, d, c0, D, kr);
+                st_tile_row8(sm + GS::KC, d, c0, D, kc);
+                st_tile_row8(sm + GS::QR, d, c0, D, qr);
+                st_tile_row8(sm + GS::KT, d, c0, D, kt);
+                tmem_st8(tmem + lb + 384 + (uint32_t)c0, kq);
             }
+            tmem_st_wait();
+            tc_fence_before();
+            fence_async_smem();
+            group_sync<kSimt>();
+            if (tid == 0) mbar_arrive(&bars[5]);  // operands of phase B are in place
+            if (tid < kC) {  // beta of the next item to its shared slot, while phase B runs
+                float nb = 0.f;
+                if (wn < total) {
+                    const Item nx = make_item(p, wn, true);
+                    if (tid < nx.c) nb = __bfloat162float(beta[(nx.r0 + tid) * HV + nx.hv]);
+                }
+                reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nb;
+            }
+            if (!wait_group<kSimt>(&bars[3], par, ws.status, 43, fail)) break;
+            tc_fence_after();
+            {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
+                const float br = rv ? sbeta[rrow] : 0.f;
+                float db = 0.f, db2 = 0.f;
+                const ColAddr ar(rrow, kC);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {  // eight columns at a time (register budget)
+                    const int j0 = 16 * cq + 8 * hh;
+                    float x[8], a[8], m[8];
+                    tmem_ld8(tmem + lb + 128 + j0, x);
+                    tmem_ld8(tmem + lb + 320 + j0, a);
+                    tmem_ld8(tmem + lb + 192 + j0, m);
+                    tmem_ld_wait();
+                    if (rv) {
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) db = fmaf(ld_col(sm + GS::INV, ar, j0 + u), x[u], db);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const bool in = j0 + u < rrow && rrow < c;
+                        db2 = in ? fmaf(a[u], m[u], db2) : db2;
+                        a[u] = in ? br * a[u] : 0.f;
+                    }
+                    if (rv) st_tile_row8(sm + GS::DM, rrow, j0, kC, a);
+                }
+                if (rv) {
+                    xdb[cq * 64 + rrow] = db;
+                    xdb[256 + cq * 64 + rrow] = db2;
+                }
+            }
+            tc_fence_before();
+            fence_async_smem();
+            group_sync<kSimt>();
+            if (tid == 0) mbar_arrive(&bars[6]);  // dM is in place and INV has been read
+            if (tid < kC && tid < c)
+                db_out[(r0 + tid) * HV + hv] =
+                    __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
+                                        ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
+            if (!wait_group<kSimt>(&bars[4], par, ws.status, 46, fail)) break;
+            tc_fence_after();
+            {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
+                float dG[16];
+                float dGC = 0.f;
+                const float sc = p.scale, sce = p.scale * e_ref;
+                // this thread's first output row and the row stride of dq / dk (or of the per-value-head partials)
+                const int HO = G == 1 ? H : HV;
+                const int64_t o0 = ((r0 + 16 * qtr) * HO + (G == 1 ? h : hv)) * D + d, rs = (int64_t)HO * D;
+#pragma unroll
+                for (int rb = 0; rb < 4; ++rb) {  // four rows at a time (register budget)
+                    const uint32_t cb = (uint32_t)(16 * qtr + 4 * rb);
+                    float aQt[4], aKh[4], aKr[4], aKc[4], aQr[4], aXk[4];
+                    uint32_t kq[4];
+                    tmem_ld4(tmem + lb + 0 + cb, aQt);
+                    tmem_ld4(tmem + lb + 64 + cb, aKh);
+                    tmem_ld4(tmem + lb + 128 + cb, aKr);
+                    tmem_ld4(tmem + lb + 192 + cb, aKc);
+                    tmem_ld4(tmem + lb + 256 + cb, aQr);
+                    tmem_ld4(tmem + lb + 448 + cb, aXk);
+                    tmem_ld4u(tmem + lb + 384 + cb, kq);
+                    tmem_ld_wait();
+                    if (rb == 3) {  // every accumulator of this item has been read: TMEM is free
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars[7]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int ii = 4 * rb + x, r = 16 * qtr + ii;
+                        const bool in = r < c;
+                        const float kv = __uint_as_float(kq[x] << 16), qv = __uint_as_float(kq[x] & 0xffff0000u);
+                        const float gm = G2[ii];
+                        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
+                        const float bX = sbeta[r] * aXk[x];
+                        // dq = E scale dQ~ + ep dQr;  dk = eh dK^ + E beta dXk + ep dKr + em dKc
+                        const float dqv = ep * fmaf(sce, aQt[x], aQr[x]);
+                        const float dkv = fmaf(ep, fmaf(e_ref, bX, aKr[x]), em * fmaf(e_cr, aKh[x], aKc[x]));
+                        const float khk = aKh[x] * (kv * eh);
+                        // The factor values of the dGamma pair terms are the bf16 values the MMAs used (rounded
+                        // two at a time here as in the factor tiles), so that each in-chunk pair's contributions
+                        // to its two rows cancel in the chunk sum as they do exactly.
+                        const uint32_t p1 = pack2(kv * E, qv * ep), p2 = pack2(kv * ep, kv * em);
+                        const float kt_b = __uint_as_float(p1 << 16), qr_b = __uint_as_float(p1 & 0xffff0000u);
+                        const float kr_b = __uint_as_float(p2 << 16), kc_b = __uint_as_float(p2 & 0xffff0000u);
+                        float dgv = fmaf(sc * aQt[x], qv * E, -khk);
+                        dgv = fmaf(bX, kt_b, dgv);
+                        dgv = fmaf(aQr[x], qr_b, dgv);
+                        dgv = fmaf(aKr[x], kr_b, dgv);
+                        dgv = fmaf(-aKc[x], kc_b, dgv);
+                        dG[ii] = in ? dgv : 0.f;
+                        if (in) {
+                            dGC += khk;
+                            const int64_t o = o0 + ii * rs;
+                            if (G == 1) {
+                                st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o),
+                                             reinterpret_cast<uint8_t*>(dk_out + o), dqv, dkv);
+                            } else {
+                                ws.dqp[o] = dqv;
+                                ws.dkp[o] = dkv;
+                            }
+                        }
+                    }
+                }
+                // dg = reverse in-chunk cumsum of dGamma, whose last valid row also takes the Gamma_C terms
+                // dGCt: in-quarter suffix sums and quarter totals first (one exchange), then per row the later
+                // quarters' totals (added in the order 3, 2, 1) and dGCt where row c - 1 lies at or after it.
+                float run = 0.f;
+#pragma unroll
+                for (int x = 15; x >= 0; --x) {
+                    run += dG[x];
+                    dG[x] = run;
+                }
+                xgc[qtr * 128 + d] = dGC;
+                xt1[qtr * 128 + d] = run;
+                group_sync<kSimt>();
+                const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
+                                   ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
+                const int qc = (c - 1) >> 4, xc = (c - 1) & 15;
+                float carry = 0.f;
+                for (int qq = 3; qq > qtr; --qq) carry += xt1[qq * 128 + d];
+                if (qc > qtr) carry += dGCt;
+#pragma unroll
+                for (int x = 0; x < 16; ++x) {
+                    const int r = 16 * qtr + x;
+                    const float t = (qc == qtr && x <= xc) ? dG[x] + dGCt : dG[x];
+                    if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = t + carry;
+                }
+            }
+            group_sync<kSimt>();  // the next item's scratch is reused from here
         }
-        if (tid < kC) reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nbeta;
-        const Item nc = *nx;
-        tc_fence_before();
-        __syncthreads();  // the next item's scratch and TMEM accumulators are reused from here
-        tc_fence_after();
-        cur = nc;
     }
     tc_fence_before();
     __syncthreads();
@@ -534,8 +602,8 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     const int64_t items = p.NT * p.HV;  // persistent: one CTA per SM, items dealt round-robin
     const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-    k_tc_grads<<<grid, 512, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv,
-                                               io.dg, (bf16*)io.dbeta, ws, m);
+    k_tc_grads<<<grid, kGradsThreads, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk,
+                                                        (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
     if (p.HV != p.H) {
         k_tc_gva_reduce<<<8 * 152, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq,

@@ -108,6 +108,21 @@ __device__ __forceinline__ void tmem_ld8u(uint32_t taddr, uint32_t* r) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                  : "r"(taddr));
 }
+// As tmem_ld32 with 4 consecutive columns.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float* v) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+// As tmem_ld4, raw 32-bit values.
+__device__ __forceinline__ void tmem_ld4u(uint32_t taddr, uint32_t* r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 // Store 8 consecutive 32-bit columns of this thread's lane (same addressing as tmem_ld32);
 // tmem_st_wait() completes the warp's outstanding stores.
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
@@ -263,6 +278,13 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // Negated-A variant of the __nv_bfloat16 instruction descriptor.
 __host__ __device__ constexpr uint32_t idesc_neg_a(uint32_t id) { return id | (1u << 13); }
 
+// Barrier 1 over threads 0 .. N-1 of the block (a multiple of 32): the group of
+// warps that shares a phase while other warps of the block run on their own.
+template <int N>
+__device__ __forceinline__ void group_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
+
 // Uniform bounded wait on (bar, parity): warp 0 polls the barrier while the other
 // warps park in the CTA barrier (issuing nothing); the barrier then orders the
 // observed completion before every thread's later accesses (callers that read
@@ -271,6 +293,15 @@ __host__ __device__ constexpr uint32_t idesc_neg_a(uint32_t id) { return id | (1
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* status, int code, int* fail) {
     if (threadIdx.x < 32 && !mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
     __syncthreads();
+    return *(volatile int*)fail == 0;
+}
+// The same for the group of threads 0 .. N-1 (group_sync); *fail must be written
+// by no thread outside the group, so that every thread of the group reads the
+// same value after the barrier.
+template <int N>
+__device__ __forceinline__ bool wait_group(uint64_t* bar, uint32_t parity, int* status, int code, int* fail) {
+    if (threadIdx.x < 32 && !mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
+    group_sync<N>();
     return *(volatile int*)fail == 0;
 }
 
@@ -318,7 +349,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // load_g_quarters fetches its g values (issued early, ahead of other
 // copies, since the cumsum heads each kernel's critical path) and
 // quarter_cumsum_log2 forms G2; `tot` is 4 x 128 floats of shared scratch.
-// quarter_cumsum_log2 contains a __syncthreads().
+// quarter_cumsum_log2 contains a barrier: __syncthreads(), or with kGroup > 0
+// named barrier 1 over the first kGroup threads of the block (group_sync).
 template <int NQ>
 __device__ __forceinline__ void load_g_quarters(const float* __restrict__ g, int64_t r0, int c, int HV, int hv, int d,
                                                 int q0, float (&gv)[16 * NQ]) {
@@ -330,7 +362,7 @@ __device__ __forceinline__ void load_g_quarters(const float* __restrict__ g, int
             gv[16 * qi + i] = r < c ? g[((r0 + r) * HV + hv) * 128 + d] : 0.f;
         }
 }
-template <int NQ>
+template <int NQ, int kGroup = 0>
 __device__ __forceinline__ void quarter_cumsum_log2(const float (&gv)[16 * NQ], int d, int q0, float* tot,
                                                     float (&G2)[16 * NQ]) {
     float run[16 * NQ];
@@ -344,7 +376,10 @@ __device__ __forceinline__ void quarter_cumsum_log2(const float (&gv)[16 * NQ], 
         }
         tot[(q0 + qi) * 128 + d] = acc;
     }
-    __syncthreads();
+    if constexpr (kGroup > 0)
+        group_sync<kGroup>();
+    else
+        __syncthreads();
 #pragma unroll
     for (int qi = 0; qi < NQ; ++qi) {
         float off = 0.f;
