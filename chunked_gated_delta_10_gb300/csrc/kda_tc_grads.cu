@@ -1,21 +1,20 @@
 // Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
 // K = V = 128, chunks of 64), and the grouped-value-head reduction.
 //
-// Persistent: one 512-thread CTA per SM walks (chunk, value head) items and
-// prefetches the next item's inputs. Inputs: q, k, v, dO, g (TMA),
+// Persistent: one CTA per SM (512 SIMT threads and a producer warp) walks
+// (chunk, value head) items and prefetches the next item's inputs. Inputs: q, k, v, dO, g (TMA),
 // and from the earlier stages delta, d_delta, S_in, dS_out, INV, e^Gamma_C
 // (bulk copies of bf16 tiles). With Kr = k e^(G-Gref), Kc = k e^(Gref-G),
 // Qr = q e^(G-Gref), K~ = k e^G, Q~ = q e^G, K^ = k e^(G_C-G) (natural-log
 // Gamma, Gref = middle row), the kernel evaluates, in three dependent MMA
 // phases (fp32 accumulators in TMEM, columns noted):
 //
-//  A  dQ~^T = S_in dO^T [0,64)     dK^^T = dS_out delta^T [64,128)
-//     dw = -d_delta S_in^T [128,256) (M=64)   dAqk = dO delta^T [256,320)
-//     dXv = INV^T d_delta [320,448)   T = d_delta delta^T [448,512)
-//  B  PR^T = V d_delta^T + K~ dw^T [128,192)  Mkk = Kr Kc^T [192,256)
-//     dQr^T = Kc^T dN^T [256,320)   dXk^T = dw^T INV [448,512)
-//     dAkk = -INV^T T [320,384)
-//  E  dKr^T = Kc^T dM^T [128,192)  dKc^T = Qr^T dN + Kr^T dM [192,256)
+//  A  [dQ~^T | -dw^T] = S_in [dO; d_delta]^T [0,128)   dAqk = dO delta^T [128,192)
+//     T = d_delta delta^T [192,256)   dK^^T = dS_out delta^T [256,320)
+//     dXv = INV^T d_delta [320,448)   (raw q, k of the final epilogue [448,512))
+//  B  PR^T = V d_delta^T + K~ dw^T [64,128)   dAkk = -INV^T T [128,192)
+//     dXk^T = dw^T INV [192,256)   Mkk = Kr Kc^T [320,384)   dQr^T = Kc^T dN^T [384,448)
+//  E  dKr^T = Kc^T dM^T [64,128)   dKc^T = Qr^T dN + Kr^T dM [128,192)
 //
 // T stands for dINV INV^T with dINV = (P + R) diag(beta) = (d_delta V^T +
 // dw K~^T) diag(beta): since INV diag(beta) V = u, INV diag(beta) K~ = w,
@@ -47,7 +46,9 @@ constexpr int TCD = kC * D * 2, TCC = kC * kC * 2, TDD = D * D * 2;
 
 // Shared-memory map (offsets from a 1024-aligned base).
 struct GS {
-    static constexpr int Q = 0, K = TCD, V = 2 * TCD, DO = 3 * TCD, DL = 4 * TCD, DDL = 5 * TCD;
+    // dO and d_delta interleave by 64-column half (dO h0, d_delta h0, dO h1, d_delta h1; half stride 2 * 8 KB),
+    // so that together they are one 128-row operand [dO; d_delta]
+    static constexpr int Q = 0, K = TCD, V = 2 * TCD, DO = 3 * TCD, DDL = 3 * TCD + TCD / 2, DL = 5 * TCD;
     static constexpr int SIN = 6 * TCD, DSO = SIN + TDD;
     // after phase A the S_in / dS_out area holds the decayed factor tiles, stored transposed
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta
                 mbar_expect_tx(b, 2 * TCD);
                 tma_load_3d(sm + GS::DO, &maps.d_o, 0, n.hv, (int)n.r0, b);
-                tma_load_3d(sm + GS::DO + TCD / 2, &maps.d_o, 64, n.hv, (int)n.r0, b);
+                tma_load_3d(sm + GS::DO + TCD, &maps.d_o, 64, n.hv, (int)n.r0, b);
                 bulk_load(sm + GS::DL, ws.vn + n.ch * TCD, TCD, b);
             };
             auto issue_qk = [&](const Item& n, uint64_t* b) {
@@ -151,7 +152,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 mbar_expect_tx(b, 2 * TCD);
                 tma_load_3d(sm + GS::V, &maps.v, 0, n.hv, (int)n.r0, b);
                 tma_load_3d(sm + GS::V + TCD / 2, &maps.v, 64, n.hv, (int)n.r0, b);
-                bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD, b);
+                bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD / 2, b);
+                bulk_load(sm + GS::DDL + TCD, ws.dvn + n.ch * TCD + TCD / 2, TCD / 2, b);
             };
             auto issue_d = [&](const Item& n, uint64_t* b) {  // INV
                 mbar_expect_tx(b, TCC);
@@ -174,7 +176,6 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 issue_e(first, &bars[0], 0);
             }
             int i = 0;
-            bool pending = false;  // copies of the next item issued and not yet waited for
             for (; w < total; ++i, w += gridDim.x) {
                 const int slot = i & 1;
                 const uint32_t par = (uint32_t)i & 1;
@@ -182,69 +183,67 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 const bool has_next = wn < total;
                 const Item nx = make_item(p, has_next ? wn : w, has_next);
                 uint64_t* nbar = &bars[slot ^ 1];
-                pending = false;
+                if (i > 0) {  // the last item's accumulators and q, k tiles are read: this item's q, k
+                    if (!pwait(&bars[7], par ^ 1, 52)) break;
+                    issue_qk(make_item(p, w, true), &bars[slot]);
+                }
                 if (!pwait(&bars[slot], (uint32_t)(i >> 1) & 1, 51)) break;
-                if (i > 0 && !pwait(&bars[7], par ^ 1, 52)) break;  // the last item's accumulators are read
                 {  // phase A
                     tc_fence_after();
-                    const uint32_t i128 = idesc_bf16(128, 64, false, false), i64n = idesc_bf16(64, 128, false, false),
+                    const uint32_t i128w = idesc_bf16(128, 128, false, false), i128 = idesc_bf16(128, 64, false, false),
                                    i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
+                    // [dQ~^T | S_in d_delta^T = -dw^T] = S_in [dO; d_delta]^T: one N = 128 product
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), kC, ks),
+                        mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), 2 * kC, ks),
+                                 i128w, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 256, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks),
                                  i128, ks > 0);
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 64, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks),
-                                 i128, ks > 0);
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::SIN), D, ks),
-                                 idesc_neg_a(i64n), ks > 0);
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 256, desc_kmajor(S(GS::DO), kC, ks), desc_kmajor(S(GS::DL), kC, ks),
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::DO), 2 * kC, ks), desc_kmajor(S(GS::DL), kC, ks),
                                  i64, ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), kC, ks), ixv,
-                                 ks > 0);
+                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), 2 * kC, ks),
+                                 ixv, ks > 0);
                     // T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T + dw w^T, and with
                     // dw = -d_delta S_in^T and delta = u - w S_in this is d_delta delta^T
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 448, desc_kmajor(S(GS::DDL), kC, ks), desc_kmajor(S(GS::DL), kC, ks),
+                        mma_bf16(tmem + 192, desc_kmajor(S(GS::DDL), 2 * kC, ks), desc_kmajor(S(GS::DL), kC, ks),
                                  i64, ks > 0);
                     mma_commit(&bars[2]);
                 }
                 if (!pwait(&bars[2], par, 53)) break;
                 if (has_next) issue_a(nx, nbar);  // dO and delta are consumed
-                pending = has_next;
                 if (!pwait(&bars[8], par, 54)) break;  // dw, dN, T written
                 {  // phase B, first part (operands from epilogue A): PR^T = V d_delta^T,
-                           // dAkk = -INV^T T (phase D), dXk^T = dw^T INV
+                   // dAkk = -INV^T T (phase D), dXk^T = dw^T INV
                     tc_fence_after();
                     const uint32_t i64 = idesc_bf16(64, 64, false, false);
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), kC, ks),
-                                 i64, ks > 0);
+                        mma_bf16(tmem + 64, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), 2 * kC, ks), i64,
+                                 ks > 0);
                     const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, true));
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd,
+                        mma_bf16(tmem + 128, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd,
                                  ks > 0);
-                    const uint32_t ixk = idesc_bf16(128, 64, true, true);
+                    const uint32_t ixk = idesc_bf16(128, 64, false, true);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 448, desc_mnmajor(S(GS::DW), kC, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk,
+                        mma_bf16(tmem + 192, desc_kmajor(S(GS::DW), D, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk,
                                  ks > 0);
                 }
                 if (!pwait(&bars[5], par, 58)) break;  // factor tiles written
                 {  // phase B, second part (factor tiles): PR^T += K~ dw^T, Mkk = Kr Kc^T, dQr^T = Kc^T dN^T
                     tc_fence_after();
-                    if (has_next) issue_qk(nx, nbar);  // q and k are consumed
-                    const uint32_t i64t = idesc_bf16(64, 64, true, false), i64tt = idesc_bf16(64, 64, true, true);
+                    const uint32_t i64tt = idesc_bf16(64, 64, true, true);
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_mnmajor(S(GS::KT), D, ks), desc_kmajor(S(GS::DW), kC, ks), i64t, 1);
+                        mma_bf16(tmem + 64, desc_mnmajor(S(GS::KT), D, ks), desc_mnmajor(S(GS::DW), D, ks), i64tt, 1);
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 192, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt,
+                        mma_bf16(tmem + 320, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt,
                                  ks > 0);
                     const uint32_t imk = idesc_bf16(128, 64, false, false);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 256, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks),
-                                 imk, ks > 0);
+                        mma_bf16(tmem + 384, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk,
+                                 ks > 0);
                     mma_commit(&bars[3]);
                 }
                 if (!pwait(&bars[3], par, 55)) break;
@@ -255,20 +254,22 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     if (has_next) issue_d(nx, nbar);  // INV is consumed
                     const uint32_t ik = idesc_bf16(128, 64, false, false), im = idesc_bf16(128, 64, false, true);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
+                        mma_bf16(tmem + 64, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 192, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks),
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks),
                                  im, ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 192, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
                     mma_commit(&bars[4]);
                 }
                 if (!pwait(&bars[4], par, 57)) break;
                 if (has_next) issue_e(nx, nbar, slot ^ 1);  // factor tiles, dN, dM, T are consumed
-                pending = false;
             }
-            // after a failed wait: let copies already issued land before the block exits (bounded)
-            if (pending) mbar_wait(&bars[(i & 1) ^ 1], (uint32_t)((i + 1) >> 1) & 1, nullptr, 0, 2000000);
+            if (w < total) {  // a wait gave up: let copies already issued land before the block exits
+                const long long t0 = clock64();
+                while (clock64() - t0 < 2000000) {
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -339,21 +340,20 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             {  // epilogue A: dw row segment (32 columns), dN row segment (16 columns), dv row segment (32 columns)
                 const float br = rv ? sbeta[rrow] : 0.f;
                 float x[16];
+                // dw^T for key channel d (this thread's TMEM lane), chunk rows 16 * cq .. +15: the negated
+                // S_in d_delta^T columns, to the transposed dw tile (row = key channel)
+                tmem_ld16(tmem + lb + 64 + 16 * cq, x);
+                tmem_ld_wait();
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    tmem_ld16(tmem + lb + 128 + 32 * cq + 16 * hh, x);
-                    tmem_ld_wait();
-                    if (rv)
-                        for (int u = 0; u < 2; ++u)
-                            st_tile_row8(sm + GS::DW, rrow, 32 * cq + 16 * hh + 8 * u, kC, x + 8 * u);
-                }
-                tmem_ld16(tmem + lb + 256 + 16 * cq, x);
+                for (int u = 0; u < 16; ++u) x[u] = -x[u];
+                for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DW, d, 16 * cq + 8 * u, D, x + 8 * u);
+                tmem_ld16(tmem + lb + 128 + 16 * cq, x);
                 tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
                 if (rv)
                     for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-                tmem_ld16(tmem + lb + 448 + 16 * cq, x);  // T rows (bf16 operand of phase D)
+                tmem_ld16(tmem + lb + 192 + 16 * cq, x);  // T rows (bf16 operand of phase D)
                 tmem_ld_wait();
                 if (rv)
                     for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
@@ -377,26 +377,26 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             }
             tc_fence_before();
             fence_async_smem();
-            group_sync<kSimt>();  // every warp has read dXv before its columns take the q, k stash
+            group_sync<kSimt>();  // epilogue A's tiles are written and its accumulators read
             if (tid == 0) mbar_arrive(&bars[8]);  // operands of phase B's first part are in place
             tc_fence_after();
             // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
-            // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). The raw
-            // (k, q) pairs go to TMEM columns 384 + 16 quarter .. +15 for the final epilogue.
+            // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). Gamma2 goes
+            // to TMEM columns 448 + 16 quarter .. +15 for the final epilogue, which reads q and k again.
             const ColAddr ad(d, kC);  // this thread's column in the 64-row q / k tiles
 #pragma unroll
             for (int h8 = 0; h8 < 2; ++h8) {
                 float kr[8], kc[8], qr[8], kt[8];
-                uint32_t kq[8];
+                uint32_t g2b[8];
 #pragma unroll
                 for (int x = 0; x < 8; ++x) {
                     const int r = 16 * qtr + 8 * h8 + x;
                     const bool in = r < c;
                     const uint32_t kbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
                     const uint32_t qbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
-                    kq[x] = kbits | (qbits << 16);
                     const float kv = __uint_as_float(kbits << 16), qv = __uint_as_float(qbits << 16);
                     const float gm = G2[8 * h8 + x];
+                    g2b[x] = __float_as_uint(gm);
                     const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
                     kr[x] = kv * ep;
                     kc[x] = kv * em;
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 st_tile_row8(sm + GS::KC, d, c0, D, kc);
                 st_tile_row8(sm + GS::QR, d, c0, D, qr);
                 st_tile_row8(sm + GS::KT, d, c0, D, kt);
-                tmem_st8(tmem + lb + 384 + (uint32_t)c0, kq);
+                tmem_st8(tmem + lb + 448 + (uint32_t)c0, g2b);
             }
             tmem_st_wait();
             tc_fence_before();
@@ -433,9 +433,9 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 for (int hh = 0; hh < 2; ++hh) {  // eight columns at a time (register budget)
                     const int j0 = 16 * cq + 8 * hh;
                     float x[8], a[8], m[8];
-                    tmem_ld8(tmem + lb + 128 + j0, x);
-                    tmem_ld8(tmem + lb + 320 + j0, a);
-                    tmem_ld8(tmem + lb + 192 + j0, m);
+                    tmem_ld8(tmem + lb + 64 + j0, x);
+                    tmem_ld8(tmem + lb + 128 + j0, a);
+                    tmem_ld8(tmem + lb + 320 + j0, m);
                     tmem_ld_wait();
                     if (rv) {
 #pragma unroll
@@ -471,20 +471,29 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 // this thread's first output row and the row stride of dq / dk (or of the per-value-head partials)
                 const int HO = G == 1 ? H : HV;
                 const int64_t o0 = ((r0 + 16 * qtr) * HO + (G == 1 ? h : hv)) * D + d, rs = (int64_t)HO * D;
+                // this thread's column in the 64-row q / k tiles: byte offset of (r, d) = qk0 + 128 r + (dd2 ^ 16 (r % 8))
+                const uint32_t qk0 = (uint32_t)((d >> 6) * kC * 128), dd2 = (uint32_t)((d & 63) * 2);
 #pragma unroll
                 for (int rb = 0; rb < 4; ++rb) {  // four rows at a time (register budget)
                     const uint32_t cb = (uint32_t)(16 * qtr + 4 * rb);
                     float aQt[4], aKh[4], aKr[4], aKc[4], aQr[4], aXk[4];
-                    uint32_t kq[4];
+                    uint32_t g2u[4], kb[4], qb[4];
                     tmem_ld4(tmem + lb + 0 + cb, aQt);
-                    tmem_ld4(tmem + lb + 64 + cb, aKh);
-                    tmem_ld4(tmem + lb + 128 + cb, aKr);
-                    tmem_ld4(tmem + lb + 192 + cb, aKc);
-                    tmem_ld4(tmem + lb + 256 + cb, aQr);
-                    tmem_ld4(tmem + lb + 448 + cb, aXk);
-                    tmem_ld4u(tmem + lb + 384 + cb, kq);
+                    tmem_ld4(tmem + lb + 256 + cb, aKh);
+                    tmem_ld4(tmem + lb + 64 + cb, aKr);
+                    tmem_ld4(tmem + lb + 128 + cb, aKc);
+                    tmem_ld4(tmem + lb + 384 + cb, aQr);
+                    tmem_ld4(tmem + lb + 192 + cb, aXk);
+                    tmem_ld4u(tmem + lb + 448 + cb, g2u);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {  // raw k, q of this thread's channel (rows >= c read as zero)
+                        const int r = 16 * qtr + 4 * rb + x;
+                        const uint32_t o = qk0 + (uint32_t)r * 128u + (dd2 ^ (uint32_t)((r & 7) << 4));
+                        kb[x] = r < c ? *reinterpret_cast<const uint16_t*>(sm + GS::K + o) : 0u;
+                        qb[x] = r < c ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + o) : 0u;
+                    }
                     tmem_ld_wait();
-                    if (rb == 3) {  // every accumulator of this item has been read: TMEM is free
+                    if (rb == 3) {  // the accumulators and the q, k tiles of this item have been read
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&bars[7]);
@@ -493,8 +502,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     for (int x = 0; x < 4; ++x) {
                         const int ii = 4 * rb + x, r = 16 * qtr + ii;
                         const bool in = r < c;
-                        const float kv = __uint_as_float(kq[x] << 16), qv = __uint_as_float(kq[x] & 0xffff0000u);
-                        const float gm = G2[ii];
+                        const float kv = __uint_as_float(kb[x] << 16), qv = __uint_as_float(qb[x] << 16);
+                        const float gm = __uint_as_float(g2u[x]);
                         const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
                         const float bX = sbeta[r] * aXk[x];
                         // dq = E scale dQ~ + ep dQr;  dk = eh dK^ + E beta dXk + ep dKr + em dKc
