@@ -9,12 +9,13 @@
 // Gamma, Gref = middle row), the kernel evaluates, in three dependent MMA
 // phases (fp32 accumulators in TMEM, columns noted):
 //
-//  A  [dQ~^T | -dw^T] = S_in [dO; d_delta]^T [0,128)   dAqk = dO delta^T [128,192)
-//     T = d_delta delta^T [192,256)   dK^^T = dS_out delta^T [256,320)
-//     dXv = INV^T d_delta [320,448)   (raw q, k of the final epilogue [448,512))
-//  B  PR^T = V d_delta^T + K~ dw^T [64,128)   dAkk = -INV^T T [128,192)
-//     dXk^T = dw^T INV [192,256)   Mkk = Kr Kc^T [320,384)   dQr^T = Kc^T dN^T [384,448)
-//  E  dKr^T = Kc^T dM^T [64,128)   dKc^T = Qr^T dN + Kr^T dM [128,192)
+//  A  [dQ~^T | -dw^T] = S_in [dO; d_delta]^T [0,128)
+//     [V; delta] [dO; d_delta]^T [128,256): V d_delta^T (rows 0..63, columns 192..255),
+//        dAqk^T = delta dO^T and T^T = delta d_delta^T (rows 64..127)
+//     dK^^T = dS_out delta^T [256,320)   dXv = INV^T d_delta [320,448)   (Gamma2 [448,512))
+//  B  PR^T = V d_delta^T + K~ dw^T [192,256)   dAkk = -INV^T T [64,128)
+//     dXk^T = dw^T INV [128,192)   Mkk = Kr Kc^T [320,384)   dQr^T = Kc^T dN^T [384,448)
+//  E  dKr^T = Kc^T dM^T [64,128)   dKc^T = Qr^T dN + Kr^T dM [320,384)
 //
 // T stands for dINV INV^T with dINV = (P + R) diag(beta) = (d_delta V^T +
 // dw K~^T) diag(beta): since INV diag(beta) V = u, INV diag(beta) K~ = w,
@@ -46,9 +47,9 @@ constexpr int TCD = kC * D * 2, TCC = kC * kC * 2, TDD = D * D * 2;
 
 // Shared-memory map (offsets from a 1024-aligned base).
 struct GS {
-    // dO and d_delta interleave by 64-column half (dO h0, d_delta h0, dO h1, d_delta h1; half stride 2 * 8 KB),
-    // so that together they are one 128-row operand [dO; d_delta]
-    static constexpr int Q = 0, K = TCD, V = 2 * TCD, DO = 3 * TCD, DDL = 3 * TCD + TCD / 2, DL = 5 * TCD;
+    // v and delta, and dO and d_delta, interleave by 64-column half (v h0, delta h0, v h1, delta h1; half
+    // stride 2 * 8 KB), so that each pair is one 128-row operand: [V; delta] and [dO; d_delta]
+    static constexpr int Q = 0, K = TCD, V = 2 * TCD, DL = 2 * TCD + TCD / 2, DO = 4 * TCD, DDL = 4 * TCD + TCD / 2;
     static constexpr int SIN = 6 * TCD, DSO = SIN + TDD;
     // after phase A the S_in / dS_out area holds the decayed factor tiles, stored transposed
     static constexpr int KR = SIN, KC = SIN + TCD, QR = SIN + 2 * TCD, KT = SIN + 3 * TCD;
@@ -95,10 +96,10 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
 // Channel-oriented work: thread (d = tid % 128, quarter = tid / 128) owns key channel d for chunk
 // rows 16 * quarter .. 16 * quarter + 15. Row-oriented work on M = 64 accumulators: row r =
 // 16 * (warp % 4) + lane (lane < 16), column quarter warp / 4. Every cross-thread sum is
-// combined in a fixed order. The inputs of the next item are fetched in five groups, each as
-// soon as the current item's phases have consumed its regions: dO, delta after phase A; q, k
-// after the factor pass; v, d_delta after phase B; INV after epilogue B/D; S_in, dS_out, g and
-// e^Gamma_C after phase E.
+// combined in a fixed order. The inputs of the next item are fetched in four groups, each as
+// soon as the current item has consumed its regions: dO, delta, v and d_delta after phase A;
+// INV after epilogue B/D; S_in, dS_out, g and e^Gamma_C after phase E; q and k once the final
+// epilogue has read them.
 constexpr int kSimt = 512, kProducerWarp = kSimt / 32, kGradsThreads = kSimt + 32;
 
 __global__ void __launch_bounds__(kGradsThreads, 1)
@@ -119,8 +120,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     const int64_t total = p.NT * HV;
 
     if (tid == 0) {
-        mbar_init(&bars[0], 5);
-        mbar_init(&bars[1], 5);
+        mbar_init(&bars[0], 4);  // four input groups per item
+        mbar_init(&bars[1], 4);
         for (int x = 2; x < 9; ++x) mbar_init(&bars[x], x == 7 ? kSimt / 32 : 1);
         fence_mbar_init();
         *fail = 0;
@@ -135,11 +136,14 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
         if (lane == 0) {  // the producer thread; lanes 1 .. 31 wait at the warp barrier below
             auto pwait = [&](uint64_t* b, uint32_t parity, int code) { return mbar_wait(b, parity, ws.status, code); };
             // the five input groups of an item into input barrier `b`
-            auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta
-                mbar_expect_tx(b, 2 * TCD);
-                tma_load_3d(sm + GS::DO, &maps.d_o, 0, n.hv, (int)n.r0, b);
-                tma_load_3d(sm + GS::DO + TCD, &maps.d_o, 64, n.hv, (int)n.r0, b);
-                bulk_load(sm + GS::DL, ws.vn + n.ch * TCD, TCD, b);
+            auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta, v, d_delta
+                mbar_expect_tx(b, 4 * TCD);
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d(sm + GS::DO + x * TCD, &maps.d_o, 64 * x, n.hv, (int)n.r0, b);
+                    tma_load_3d(sm + GS::V + x * TCD, &maps.v, 64 * x, n.hv, (int)n.r0, b);
+                    bulk_load(sm + GS::DL + x * TCD, ws.vn + n.ch * TCD + x * (TCD / 2), TCD / 2, b);
+                    bulk_load(sm + GS::DDL + x * TCD, ws.dvn + n.ch * TCD + x * (TCD / 2), TCD / 2, b);
+                }
             };
             auto issue_qk = [&](const Item& n, uint64_t* b) {
                 mbar_expect_tx(b, 2 * TCD);
@@ -147,13 +151,6 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     tma_load_3d(sm + GS::Q + x * (TCD / 2), &maps.q, 64 * x, n.h, (int)n.r0, b);
                     tma_load_3d(sm + GS::K + x * (TCD / 2), &maps.k, 64 * x, n.h, (int)n.r0, b);
                 }
-            };
-            auto issue_b = [&](const Item& n, uint64_t* b) {  // v, d_delta
-                mbar_expect_tx(b, 2 * TCD);
-                tma_load_3d(sm + GS::V, &maps.v, 0, n.hv, (int)n.r0, b);
-                tma_load_3d(sm + GS::V + TCD / 2, &maps.v, 64, n.hv, (int)n.r0, b);
-                bulk_load(sm + GS::DDL, ws.dvn + n.ch * TCD, TCD / 2, b);
-                bulk_load(sm + GS::DDL + TCD, ws.dvn + n.ch * TCD + TCD / 2, TCD / 2, b);
             };
             auto issue_d = [&](const Item& n, uint64_t* b) {  // INV
                 mbar_expect_tx(b, TCC);
@@ -171,7 +168,6 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 const Item first = make_item(p, w, true);
                 issue_a(first, &bars[0]);
                 issue_qk(first, &bars[0]);
-                issue_b(first, &bars[0]);
                 issue_d(first, &bars[0]);
                 issue_e(first, &bars[0], 0);
             }
@@ -191,63 +187,58 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 {  // phase A
                     tc_fence_after();
                     const uint32_t i128w = idesc_bf16(128, 128, false, false), i128 = idesc_bf16(128, 64, false, false),
-                                   i64 = idesc_bf16(64, 64, false, false), ixv = idesc_bf16(64, 128, true, true);
-                    // [dQ~^T | S_in d_delta^T = -dw^T] = S_in [dO; d_delta]^T: one N = 128 product
+                                   ixv = idesc_bf16(64, 128, true, true);
+                    // [dQ~^T | S_in d_delta^T = -dw^T] = S_in [dO; d_delta]^T
                     for (int ks = 0; ks < D / 16; ++ks)
                         mma_bf16(tmem + 0, desc_kmajor(S(GS::SIN), D, ks), desc_kmajor(S(GS::DO), 2 * kC, ks),
                                  i128w, ks > 0);
+                    // [V; delta] [dO; d_delta]^T: rows 0..63 give V d_delta^T (PR^T's first term) in columns
+                    // 192..255; rows 64..127 give dAqk^T = delta dO^T in columns 128..191 and T^T = delta d_delta^T
+                    // there after, where T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T +
+                    // dw w^T, which with dw = -d_delta S_in^T and delta = u - w S_in is d_delta delta^T
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 256, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), kC, ks),
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::V), 2 * kC, ks), desc_kmajor(S(GS::DO), 2 * kC, ks),
+                                 i128w, ks > 0);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16(tmem + 256, desc_kmajor(S(GS::DSO), D, ks), desc_kmajor(S(GS::DL), 2 * kC, ks),
                                  i128, ks > 0);
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::DO), 2 * kC, ks), desc_kmajor(S(GS::DL), kC, ks),
-                                 i64, ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_bf16(tmem + 320, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::DDL), 2 * kC, ks),
                                  ixv, ks > 0);
-                    // T = dINV INV^T = (d_delta V^T + dw K~^T) diag(beta) INV^T = d_delta u^T + dw w^T, and with
-                    // dw = -d_delta S_in^T and delta = u - w S_in this is d_delta delta^T
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 192, desc_kmajor(S(GS::DDL), 2 * kC, ks), desc_kmajor(S(GS::DL), kC, ks),
-                                 i64, ks > 0);
                     mma_commit(&bars[2]);
                 }
                 if (!pwait(&bars[2], par, 53)) break;
-                if (has_next) issue_a(nx, nbar);  // dO and delta are consumed
-                if (!pwait(&bars[8], par, 54)) break;  // dw, dN, T written
-                {  // phase B, first part (operands from epilogue A): PR^T = V d_delta^T,
-                   // dAkk = -INV^T T (phase D), dXk^T = dw^T INV
+                if (has_next) issue_a(nx, nbar);  // dO, delta, v and d_delta are consumed
+                if (!pwait(&bars[8], par, 54)) break;  // dw, dN^T, T^T written
+                {  // phase B, first part (operands from epilogue A): dAkk = -INV^T T (phase D), dXk^T = dw^T INV
                     tc_fence_after();
-                    const uint32_t i64 = idesc_bf16(64, 64, false, false);
-                    for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 64, desc_kmajor(S(GS::V), kC, ks), desc_kmajor(S(GS::DDL), 2 * kC, ks), i64,
-                                 ks > 0);
-                    const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, true));
+                    const uint32_t idd = idesc_neg_a(idesc_bf16(64, 64, true, false));
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_mnmajor(S(GS::INV), kC, ks), desc_mnmajor(S(GS::TT), kC, ks), idd,
+                        mma_bf16(tmem + 64, desc_mnmajor(S(GS::INV), kC, ks), desc_kmajor(S(GS::TT), kC, ks), idd,
                                  ks > 0);
                     const uint32_t ixk = idesc_bf16(128, 64, false, true);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 192, desc_kmajor(S(GS::DW), D, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk,
+                        mma_bf16(tmem + 128, desc_kmajor(S(GS::DW), D, ks), desc_mnmajor(S(GS::INV), kC, ks), ixk,
                                  ks > 0);
                 }
                 if (!pwait(&bars[5], par, 58)) break;  // factor tiles written
                 {  // phase B, second part (factor tiles): PR^T += K~ dw^T, Mkk = Kr Kc^T, dQr^T = Kc^T dN^T
                     tc_fence_after();
-                    const uint32_t i64tt = idesc_bf16(64, 64, true, true);
+                    // PR^T's rows are lanes 0..63 of an M = 128 accumulator: K~ dw^T accumulates as an M = 128
+                    // product whose rows 64..127 (from the 16 KB after the K~ tile) land on T^T, already read
+                    const uint32_t ipr = idesc_bf16(128, 64, true, true), i64tt = idesc_bf16(64, 64, true, true);
                     for (int ks = 0; ks < D / 16; ++ks)
-                        mma_bf16(tmem + 64, desc_mnmajor(S(GS::KT), D, ks), desc_mnmajor(S(GS::DW), D, ks), i64tt, 1);
+                        mma_bf16(tmem + 192, desc_mnmajor(S(GS::KT), D, ks), desc_mnmajor(S(GS::DW), D, ks), ipr, 1);
                     for (int ks = 0; ks < D / 16; ++ks)
                         mma_bf16(tmem + 320, desc_mnmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::KC), D, ks), i64tt,
                                  ks > 0);
-                    const uint32_t imk = idesc_bf16(128, 64, false, false);
+                    const uint32_t imk = idesc_bf16(128, 64, false, true);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 384, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DN), kC, ks), imk,
+                        mma_bf16(tmem + 384, desc_kmajor(S(GS::KC), D, ks), desc_mnmajor(S(GS::DN), kC, ks), imk,
                                  ks > 0);
                     mma_commit(&bars[3]);
                 }
                 if (!pwait(&bars[3], par, 55)) break;
-                if (has_next) issue_b(nx, nbar);  // v and d_delta are consumed
                 if (!pwait(&bars[6], par, 56)) break;  // dM written, INV read
                 {  // phase E
                     tc_fence_after();
@@ -256,10 +247,10 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_bf16(tmem + 64, desc_kmajor(S(GS::KC), D, ks), desc_kmajor(S(GS::DM), kC, ks), ik, ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::QR), D, ks), desc_mnmajor(S(GS::DN), kC, ks),
-                                 im, ks > 0);
+                        mma_bf16(tmem + 320, desc_kmajor(S(GS::QR), D, ks), desc_kmajor(S(GS::DN), kC, ks), ik,
+                                 ks > 0);
                     for (int ks = 0; ks < kC / 16; ++ks)
-                        mma_bf16(tmem + 128, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
+                        mma_bf16(tmem + 320, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
                     mma_commit(&bars[4]);
                 }
                 if (!pwait(&bars[4], par, 57)) break;
@@ -337,7 +328,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             xrd[qtr * 128 + d] = rd;
             if (!wait_group<kSimt>(&bars[2], par, ws.status, 42, fail)) break;
             tc_fence_after();
-            {  // epilogue A: dw row segment (32 columns), dN row segment (16 columns), dv row segment (32 columns)
+            {  // epilogue A: dw^T, dN^T and T^T row segments (16 columns), dv row segments (32 columns)
                 const float br = rv ? sbeta[rrow] : 0.f;
                 float x[16];
                 // dw^T for key channel d (this thread's TMEM lane), chunk rows 16 * cq .. +15: the negated
@@ -347,16 +338,20 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
 #pragma unroll
                 for (int u = 0; u < 16; ++u) x[u] = -x[u];
                 for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DW, d, 16 * cq + 8 * u, D, x + 8 * u);
-                tmem_ld16(tmem + lb + 128 + 16 * cq, x);
-                tmem_ld_wait();
+                if (q4 >= 2) {  // lanes 64..127 of [V; delta] [dO; d_delta]^T: row i of dAqk^T and of T^T
+                    const int ii = 32 * (q4 - 2) + lane;
+                    tmem_ld16(tmem + lb + 128 + 16 * cq, x);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) x[u] = (16 * cq + u <= rrow && rrow < c) ? p.scale * x[u] : 0.f;
-                if (rv)
-                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
-                tmem_ld16(tmem + lb + 192 + 16 * cq, x);  // T rows (bf16 operand of phase D)
-                tmem_ld_wait();
-                if (rv)
-                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, rrow, 16 * cq + 8 * u, kC, x + 8 * u);
+                    for (int u = 0; u < 16; ++u) {  // dN^T[i][r] = scale dAqk[r][i] for i <= r < c
+                        const int r = 16 * cq + u;
+                        x[u] = (ii <= r && r < c) ? p.scale * x[u] : 0.f;
+                    }
+                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, ii, 16 * cq + 8 * u, kC, x + 8 * u);
+                    tmem_ld16(tmem + lb + 192 + 16 * cq, x);  // T^T (bf16 operand of phase D)
+                    tmem_ld_wait();
+                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, ii, 16 * cq + 8 * u, kC, x + 8 * u);
+                }
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     tmem_ld16(tmem + lb + 320 + 32 * cq + 16 * hh, x);
@@ -426,21 +421,32 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             if (!wait_group<kSimt>(&bars[3], par, ws.status, 43, fail)) break;
             tc_fence_after();
             {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
+                if (q4 < 2) {  // INV part from PR^T row j (lanes 0..63 of an M = 128 accumulator), 16 columns
+                    const int j = 32 * q4 + lane;
+                    float x[16];
+                    tmem_ld16(tmem + lb + 192 + 16 * cq, x);
+                    tmem_ld_wait();
+                    // INV[r][j], r = 16 cq + u: byte offset 128 r + (2 j ^ 16 (r % 8)) in the 64-row INV tile
+                    const uint8_t* invc = sm + GS::INV + 16 * cq * 128;
+                    const uint32_t j2 = (uint32_t)(2 * j);
+                    float db = 0.f;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) {
+                        const uint32_t o = (uint32_t)(u * 128) + (j2 ^ (uint32_t)((u & 7) << 4));
+                        const float iv = __uint_as_float((uint32_t)*reinterpret_cast<const uint16_t*>(invc + o) << 16);
+                        db = fmaf(iv, x[u], db);
+                    }
+                    xdb[cq * 64 + j] = db;
+                }
                 const float br = rv ? sbeta[rrow] : 0.f;
-                float db = 0.f, db2 = 0.f;
-                const ColAddr ar(rrow, kC);
+                float db2 = 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {  // eight columns at a time (register budget)
                     const int j0 = 16 * cq + 8 * hh;
-                    float x[8], a[8], m[8];
-                    tmem_ld8(tmem + lb + 64 + j0, x);
-                    tmem_ld8(tmem + lb + 128 + j0, a);
+                    float a[8], m[8];
+                    tmem_ld8(tmem + lb + 64 + j0, a);
                     tmem_ld8(tmem + lb + 320 + j0, m);
                     tmem_ld_wait();
-                    if (rv) {
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) db = fmaf(ld_col(sm + GS::INV, ar, j0 + u), x[u], db);
-                    }
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const bool in = j0 + u < rrow && rrow < c;
@@ -449,10 +455,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     }
                     if (rv) st_tile_row8(sm + GS::DM, rrow, j0, kC, a);
                 }
-                if (rv) {
-                    xdb[cq * 64 + rrow] = db;
-                    xdb[256 + cq * 64 + rrow] = db2;
-                }
+                if (rv) xdb[256 + cq * 64 + rrow] = db2;
             }
             tc_fence_before();
             fence_async_smem();
@@ -481,9 +484,9 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     tmem_ld4(tmem + lb + 0 + cb, aQt);
                     tmem_ld4(tmem + lb + 256 + cb, aKh);
                     tmem_ld4(tmem + lb + 64 + cb, aKr);
-                    tmem_ld4(tmem + lb + 128 + cb, aKc);
+                    tmem_ld4(tmem + lb + 320 + cb, aKc);
                     tmem_ld4(tmem + lb + 384 + cb, aQr);
-                    tmem_ld4(tmem + lb + 192 + cb, aXk);
+                    tmem_ld4(tmem + lb + 128 + cb, aXk);
                     tmem_ld4u(tmem + lb + 448 + cb, g2u);
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {  // raw k, q of this thread's channel (rows >= c read as zero)
