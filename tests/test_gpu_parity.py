@@ -258,6 +258,22 @@ def test_rerun_is_bitwise_identical(kda):
         assert torch.equal(a[key], b[key]), key
 
 
+def test_rerun_is_bitwise_identical_benchmark_workload(kda):
+    """The benchmark workload (16,384 chunk-heads, about 108 per persistent CTA, so every CTA runs its
+    prefetch pipeline and its producer / SIMT hand-offs many times): two backward runs and two
+    forward runs agree bit for bit."""
+    inp = _workload("bf16_b8_t4096_h32_k128")
+    a = gpu_bwd(kda, inp)
+    b = gpu_bwd(kda, inp)
+    for key in GRADS:
+        if a[key] is not None:
+            assert torch.equal(a[key], b[key]), key
+    del a, b
+    o1, ht1, _ = gpu_fwd(kda, inp)
+    o2, ht2, _ = gpu_fwd(kda, inp)
+    assert torch.equal(o1, o2) and torch.equal(ht1, ht2)
+
+
 def test_packed_equals_separate_sequences_bitwise(kda):
     lens = [100, 1, 64, 257]
     inp = kda_inputs.small(seed=34, B=1, T=0, H=2, HV=2, K=128, V=128, dtype="bf16", seq_lens=lens)
