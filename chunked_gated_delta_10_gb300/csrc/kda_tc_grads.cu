@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     if (warp == kProducerWarp) {
         if (lane == 0) {  // the producer thread; lanes 1 .. 31 wait at the warp barrier below
             auto pwait = [&](uint64_t* b, uint32_t parity, int code) { return mbar_wait(b, parity, ws.status, code); };
-            // the five input groups of an item into input barrier `b`
+            // the four input groups of an item into input barrier `b`
             auto issue_a = [&](const Item& n, uint64_t* b) {  // dO, delta, v, d_delta
                 mbar_expect_tx(b, 4 * TCD);
                 for (int x = 0; x < 2; ++x) {
