@@ -8,6 +8,7 @@ compared on whole independent units (one sequence x one key head and its value
 heads), which the oracle computes exactly, at the sizes and launch
 configuration the benchmark times.
 """
+import dataclasses
 import functools
 
 import numpy as np
@@ -246,6 +247,39 @@ def test_workload_bf16_t65536_gva_sampled(kda):
     inp = _workload("bf16_b1_t65536_h16_hv32_k128")
     out = gpu_bwd(kda, inp)
     print("bf16_b1_t65536_h16_hv32_k128", compare_unit(inp, out, 0, 9))
+
+
+# ------------------------------------------------------------ degenerate inputs
+
+DEGENERATE = {
+    "fp32_k64": dict(B=1, T=0, H=2, HV=2, K=64, V=64, seq_lens=[70, 1, 33], dtype="f32"),
+    "bf16_k128": dict(B=1, T=0, H=2, HV=4, K=128, V=128, seq_lens=[130, 5, 64], dtype="bf16"),
+}
+
+
+@pytest.mark.parametrize("name", list(DEGENERATE))
+def test_zero_cotangents_give_exactly_zero_gradients(kda, name):
+    """do = 0 and dht = 0: every gradient is exactly zero (an exactly zero reference
+    requires an exactly zero result)."""
+    inp = kda_inputs.small(seed=41, **DEGENERATE[name])
+    inp = dataclasses.replace(inp, do=torch.zeros_like(inp.do), dht=torch.zeros_like(inp.dht))
+    out = gpu_bwd(kda, inp)
+    for key in GRADS:
+        assert torch.count_nonzero(out[key]) == 0, key
+
+
+@pytest.mark.parametrize("name", list(DEGENERATE))
+@pytest.mark.parametrize("case", ["beta_zero", "gate_zero"])
+def test_degenerate_gates_match_the_oracle(kda, name, case):
+    """beta = 0 (no delta-rule write: the state only decays) and g = 0 (no decay)."""
+    inp = kda_inputs.small(seed=42, **DEGENERATE[name])
+    if case == "beta_zero":
+        inp = dataclasses.replace(inp, beta=torch.zeros_like(inp.beta))
+    else:
+        inp = dataclasses.replace(inp, g=torch.zeros_like(inp.g))
+    out = gpu_bwd(kda, inp)
+    errs = compare_full(inp, out, oracle.run_inputs(inp))
+    print(name, case, errs)
 
 
 # ------------------------------------------------------------ invariances
