@@ -6,12 +6,15 @@ bf16 workload B=8, T=4096, H=HV=32, K=V=128, chunk 64 (seeded synthetic
 inputs; see kda_inputs.py). Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--pass bwd|fwd|bwd-states]
+                    [--pass bwd|fwd|bwd-states] [--workload NAME]
 
 * ``value``: device-timed tokens/s (inputs resident in HBM; K steps between
   CUDA events, barrier + synchronize on both sides, max over ranks). The
   per-step working set (~10 GB) is far larger than the 129 MB L2, so no flush
-  is needed between steps.
+  is needed between steps. The library also records one CUDA event after
+  each of its kernel launches inside the timed region (its per-kernel timing
+  hook); ``step_ms`` gives the median, minimum, maximum and standard
+  deviation of the per-step spans those events bracket.
 * ``e2e``: the same metric through the C ABI from pinned host buffers: every
   step copies its inputs host->device, runs the call, and copies every
   gradient back; with two device buffer sets the copies of neighbouring steps
@@ -28,6 +31,11 @@ inputs; see kda_inputs.py). Prints one JSON line.
   ``kda_chunk_fwd`` call (o and ht) per step; ``bwd-states`` times the
   backward that consumes the chunk states a forward saved (the states are
   produced once before the timed region).
+* ``--workload``: one of the four bf16 workloads of kda_inputs.py (default
+  the B=8 T=4096 H=HV=32 benchmark); the others (B=1 T=2048 H=16 with h0 and
+  dht; 16 packed sequences of U[1,4096] tokens with h0; B=1 T=65536 with 16
+  key heads over 32 value heads, h0 and dht) run with their initial states,
+  final-state gradients and packed-sequence tables as drawn.
 
 Multi-GPU (torchrun): every rank runs the full workload on its own GPU (weak
 scaling, independent batches, no data-path collective); ``value`` is the sum
@@ -65,20 +73,25 @@ UNIT = "tokens/s"
 # ----------------------------------------------------------------------------
 
 
-def step_cost(B, T, H, HV, K, V, in_bytes=2, C=64):
+def step_cost(B, T, H, HV, K, V, in_bytes=2, C=64, nck=None, seq_states=0):
+    """Algorithmic bytes / FLOPs of one backward step. ``nck``: chunk-heads when the sequences are packed
+    (default B * ceil(T / C) * HV); ``seq_states``: fp32 [N, HV, K, V] tensors the step reads or writes
+    besides the chunk states (h0, dht, dh0), given as their total element count."""
     th = B * T * HV  # token-heads
     tk = B * T * H
-    nck = B * ((T + C - 1) // C) * HV
+    if nck is None:
+        nck = B * ((T + C - 1) // C) * HV
     io_in = tk * K * in_bytes * 2 + th * V * in_bytes * 2 + th * K * 4 + th * in_bytes
     io_out = tk * K * in_bytes * 2 + th * V * in_bytes + th * K * 4 + th * in_bytes
+    io_in += seq_states * 4
     states = 2 * nck * K * V * 4
     flops = nck * (16 * C * K * V + 9 * C * C * K + 5 * C * C * V + C ** 3)
     return dict(bytes=io_in + io_out + states, flops=flops, io_in=io_in, io_out=io_out, states=states, nck=nck)
 
 
-def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64):
+def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None, seq_states=0):
     """Algorithmic bytes / FLOPs of one step of ``mode`` (see step_cost for the backward)."""
-    s = step_cost(B, T, H, HV, K, V, in_bytes, C)
+    s = step_cost(B, T, H, HV, K, V, in_bytes, C, nck, seq_states)
     th, tk, nck = B * T * HV, B * T * H, s["nck"]
     if mode == "fwd":  # q, k, v, g, beta in; o and ht out; the chunk state stays on chip or in bf16 scratch
         b = tk * K * in_bytes * 2 + th * V * in_bytes + th * K * 4 + th * in_bytes + th * V * in_bytes
@@ -90,9 +103,9 @@ def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64):
     return s
 
 
-def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64):
+def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
     """(bound, algorithmic bytes, algorithmic flops) of one launch of kernel ``name``."""
-    s = step_cost(B, T, H, HV, K, V, in_bytes, C)
+    s = step_cost(B, T, H, HV, K, V, in_bytes, C, nck)
     nck = s["nck"]
     th = B * T * HV
     tk = B * T * H
@@ -300,26 +313,61 @@ def oracle_sample(inp, n_seqs, n_heads):
     return token_heads / H / dt, used, dt, f"{n_seqs} sequence(s) x {n_heads} of {H} key heads x {T} tokens"
 
 
+def workload_config(inp, world, extra=None):
+    """The ``config`` object of a JSON line (the same keys on both arms)."""
+    B, T, H, K = inp.q.shape
+    HV = inp.v.shape[2]
+    cfg = {"workload": inp.spec.name, "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
+           "head_dim": K, "chunk": 64, "parallelism": f"dp{world}" if world > 1 else "single",
+           "l2": "inputs larger than L2 (several GB touched per step), no flush"}
+    if inp.cu_seqlens is not None:
+        cfg["packed_sequences"] = inp.num_seqs
+    cfg.update(extra or {})
+    return cfg
+
+
+def oracle_sample_any(inp):
+    """The bounded CPU sample of a workload: 16 key heads of the first sequence (its first 4096 tokens)."""
+    if inp.cu_seqlens is None and inp.T <= 4096:
+        return oracle_sample(inp, 1, min(16, inp.q.shape[2]))
+    import oracle
+
+    b, e = inp.seq_bounds[0]
+    L = min(e - b, 4096)
+    H, HV = inp.q.shape[2], inp.v.shape[2]
+    G = HV // H
+    nh = min(16, H)
+    hs, vs = slice(0, nh), slice(0, nh * G)
+    rows = lambda x, s: x.reshape(-1, *x.shape[2:])[b:b + L, s].unsqueeze(0).contiguous()
+    st = lambda x: None if x is None else x[0:1, vs].contiguous()
+    oracle.build()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    used = min(cores, nh)
+    t0 = time.perf_counter()
+    oracle.run(rows(inp.q, hs), rows(inp.k, hs), rows(inp.v, vs), rows(inp.g, vs), rows(inp.beta, vs), inp.scale,
+               st(inp.h0), rows(inp.do, vs), st(inp.dht), nthreads=used)
+    dt = time.perf_counter() - t0
+    return L * nh / H / dt, used, dt, f"first {L} tokens of sequence 0 x {nh} of {H} key heads"
+
+
 def reference_arm(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return
-    inp = kda_inputs.workload(WORKLOAD)
-    n_seqs, n_heads = 1, 16
+    inp = kda_inputs.workload(args.workload)
     vals = []
     for _ in range(args.warmup):
-        oracle_sample(inp, n_seqs, n_heads)
+        oracle_sample_any(inp)
     used = 0
     sample = ""
     for _ in range(args.steps):
-        v, used, dt, sample = oracle_sample(inp, n_seqs, n_heads)
+        v, used, dt, sample = oracle_sample_any(inp)
         vals.append(v)
     value = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 8, "seq_len": 4096, "heads": 32, "head_dim": 128,
-                       "chunk": 64},
+            "config": workload_config(inp, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -343,7 +391,7 @@ def gpu_arm(args):
     kda.build()
     lib = kda.load()
 
-    spec = kda_inputs.WORKLOADS[WORKLOAD]
+    spec = kda_inputs.WORKLOADS[args.workload]
     if args.batch:
         import dataclasses
 
@@ -351,20 +399,29 @@ def gpu_arm(args):
     inp = kda_inputs.make(spec)
     B, T, H, K = inp.q.shape
     HV, V = inp.v.shape[2], inp.v.shape[3]
+    N = inp.num_seqs
     tokens = B * T
-    host = dict(q=inp.q, k=inp.k, v=inp.v, g=inp.g, beta=inp.beta, do=inp.do)
-    x = {n: t.to(device).contiguous() for n, t in host.items()}
     mode = args.mode
-    if mode == "fwd":
-        del host["do"], x["do"]
-    dims = kda.make_dims(x["q"], x["v"], inp.scale)
+    host = dict(q=inp.q, k=inp.k, v=inp.v, g=inp.g, beta=inp.beta)
+    if inp.h0 is not None:
+        host["h0"] = inp.h0
+    if mode != "fwd":
+        host["do"] = inp.do
+        if inp.dht is not None:
+            host["dht"] = inp.dht
+    x = {n: t.to(device).contiguous() for n, t in host.items()}
+    vl = kda._Varlen(inp.cu_seqlens, device)
+    dims = kda.make_dims(x["q"], x["v"], inp.scale, inp.cu_seqlens)
+    nck = int(dims.num_chunks) * HV
     wsb = kda.workspace_bytes(dims, kda.PASS_FWD if mode == "fwd" else kda.PASS_BWD)
     ws = torch.empty(wsb, dtype=torch.uint8, device=device)
     if mode == "fwd":
-        out = dict(o=torch.empty_like(x["v"]), ht=torch.empty(B, HV, K, V, dtype=torch.float32, device=device))
+        out = dict(o=torch.empty_like(x["v"]), ht=torch.empty(N, HV, K, V, dtype=torch.float32, device=device))
     else:
         out = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
                    dg=torch.empty_like(x["g"]), dbeta=torch.empty_like(x["beta"]))
+        if "h0" in x:
+            out["dh0"] = torch.empty_like(x["h0"])
     stream = torch.cuda.current_stream(device)
     sptr = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
@@ -375,7 +432,8 @@ def gpu_arm(args):
         states = torch.empty(dims.num_chunks, HV, K, V, dtype=torch.float32, device=device)
         o_tmp = torch.empty_like(x["v"])
         rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(x["q"]), P(x["k"]), P(x["v"]), P(x["g"]), P(x["beta"]),
-                               None, None, None, None, P(o_tmp), None, P(states), P(fws), fwb, sptr)
+                               P(x.get("h0")), P(vl.cu), P(vl.idx), P(vl.off), P(o_tmp), None, P(states), P(fws),
+                               fwb, sptr)
         if rc != 0:
             raise kda.KdaError(rc, "kda_chunk_fwd")
         del fws, o_tmp
@@ -383,13 +441,14 @@ def gpu_arm(args):
     def step(inputs, outs):
         if mode == "fwd":
             rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
-                                   P(inputs["g"]), P(inputs["beta"]), None, None, None, None, P(outs["o"]),
-                                   P(outs["ht"]), None, P(ws), wsb, sptr)
+                                   P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
+                                   P(vl.off), P(outs["o"]), P(outs["ht"]), None, P(ws), wsb, sptr)
         else:
             rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
-                                   P(inputs["g"]), P(inputs["beta"]), None, None, None, None, P(inputs["do"]),
-                                   None, P(states), P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]),
-                                   P(outs["dbeta"]), None, P(ws), wsb, sptr)
+                                   P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
+                                   P(vl.off), P(inputs["do"]), P(inputs.get("dht")), P(states), P(outs["dq"]),
+                                   P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]),
+                                   P(outs.get("dh0")), P(ws), wsb, sptr)
         if rc != 0:
             raise kda.KdaError(rc, "kda_chunk_fwd" if mode == "fwd" else "kda_chunk_bwd")
 
@@ -429,23 +488,28 @@ def gpu_arm(args):
     for evs in ev_sets:
         for i, n in enumerate(names):
             per[n].append(evs[i].elapsed_time(evs[i + 1]) / 1e3)
+    spans = [evs[0].elapsed_time(evs[-1]) for evs in ev_sets]  # ms, first to last launch of each step
+    step_ms = {"mean": statistics.fmean(spans), "median": statistics.median(spans), "min": min(spans),
+               "max": max(spans), "stdev": statistics.pstdev(spans), "n": len(spans)}
     tot = {n: sum(v) for n, v in per.items()}
     dom = max(tot, key=tot.get)
     avg = tot[dom] / len(per[dom])
     peaks, peak_src = load_peaks()
-    bound, abytes, aflops = kernel_cost(dom, B, T, H, HV, K, V)
+    bound, abytes, aflops = kernel_cost(dom, B, T, H, HV, K, V, nck=nck)
     if bound == "hbm":
         ach, pk, unit = abytes / avg / 1e9, peaks["hbm_gbs"], "GB/s"
     elif bound == "tensor":
         ach, pk, unit = aflops / avg / 1e12, peaks["bf16_tflops_sustained"], "TFLOP/s"
     else:
         ach, pk, unit = aflops / avg / 1e12, alu_peak_tflops(clk.get("sm_mhz") or peaks["sm_max_mhz"]), "TFLOP/s"
-    traffic = measured_traffic(dom, step_cost(B, T, H, HV, K, V)["nck"])
+    traffic = measured_traffic(dom, nck) if args.workload == WORKLOAD else None
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": pk, "unit": unit, "frac": ach / pk,
                 "traffic": traffic, "peak_source": peak_src if bound != "alu" else "152 SMs x 128 FFMA lanes x SM clock",
                 "avg_launch_ms": avg * 1e3, "share": tot[dom] / sum(tot.values()),
                 "kernels_ms": {n: 1e3 * tot[n] / len(per[n]) for n in names}}
-    sc = pass_cost(mode, B, T, H, HV, K, V)
+    seq_states = N * HV * K * V * ((1 if "h0" in x else 0) + (0 if mode == "fwd" else
+                                                             (1 if "dht" in x else 0) + (1 if "h0" in x else 0)))
+    sc = pass_cost(mode, B, T, H, HV, K, V, nck=nck, seq_states=seq_states)
     step_s = elapsed / args.steps
     path = {"bytes_alg": sc["bytes"], "flops_alg": sc["flops"],
             "hbm_frac": sc["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
@@ -492,20 +556,24 @@ def gpu_arm(args):
     torch.cuda.synchronize(device)
     e2e_val, _ = aggregate(tokens * e2e_steps, e0.elapsed_time(e1) / 1e3, world, device)
 
+    extra = {}
+    if args.batch:
+        extra["workload"] = f"{spec.name} with B={args.batch}"
+    if mode != "bwd":
+        extra["pass"] = mode
     line = {"metric": METRICS[mode], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD if not args.batch else f"{WORKLOAD} with B={args.batch}",
-                       "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
-                       "head_dim": K, "chunk": 64, "parallelism": f"dp{world}" if world > 1 else "single",
-                       "l2": "inputs larger than L2 (about 10 GB touched per step), no flush"},
-            "roofline": roofline, "path": path, "clocks": clk, "gpu_launches": launches * args.steps,
+            "config": workload_config(inp, world, extra),
+            "timing": "value and ms_per_step: mean over the K back-to-back steps between two CUDA events; the "
+                      "library records one CUDA event after each of its launches inside that region (per-kernel "
+                      "times); step_ms: per-step spans from those events",
+            "step_ms": step_ms, "roofline": roofline, "path": path, "clocks": clk,
+            "gpu_launches": launches * args.steps,
             "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps}}
-    if mode != "bwd":
-        line["config"]["pass"] = mode
     if rank == 0 and world == 1 and not args.no_cpu_baseline and mode == "bwd":
-        v, used, dt, sample = oracle_sample(inp, 1, 16)
+        v, used, dt, sample = oracle_sample_any(inp)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample,
                                 "seconds": dt}
     if rank == 0:
@@ -526,6 +594,9 @@ def main():
     ap.add_argument("--pass", dest="mode", default="bwd", choices=list(METRICS),
                     help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
                          "bwd-states: backward from saved chunk states")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[n for n in kda_inputs.WORKLOAD_ORDER if kda_inputs.WORKLOADS[n].dtype == "bf16"],
+                    help="the workload of the JSON line (default: the B=8 T=4096 H=HV=32 benchmark)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (smaller cases for profiling; not the benchmark workload)")
     args = ap.parse_args()

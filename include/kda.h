@@ -163,14 +163,23 @@ kda_status kda_device_status(const void* ws, kda_stream_t stream);
  * memory on every GPU that loads it, until the process exits. It allocates
  * nothing; the caller still passes every input and output, as for
  * kda_chunk_bwd.
- *   - The first call on a device looks up that array's device address (a
- *     one-time set-up with the device current); make that first call before
- *     any stream capture.
- *   - Every call shares the one array. Calls whose execution overlaps on the
- *     GPU (several streams or host threads) race on it: serialise them.
- *   - Errors: those of kda_chunk_bwd; KDA_ERR_WORKSPACE when the problem needs
- *     more than KDA_NOALLOC_SCRATCH_BYTES (kda_workspace_bytes(dims,
- *     KDA_PASS_BWD) > KDA_NOALLOC_SCRATCH_BYTES), returned before any launch.
+ *   - Set-up: the array's device address is looked up once per device, with
+ *     that device current, by kda_noalloc_prepare (or by the first call on
+ *     the device if prepare was not called). With CUDA's lazy module loading
+ *     that first look-up also loads the module and commits the 64 MiB array,
+ *     so it needs that much free device memory: call kda_noalloc_prepare in
+ *     the caller's set-up phase, before any execute phase or stream capture.
+ *   - The address stays valid for the life of the device's context; after a
+ *     device reset (cudaDeviceReset), call kda_noalloc_prepare again.
+ *   - Every call shares the one array and it keeps the last call's contents
+ *     (each call clears the status word it needs at zero). Calls whose
+ *     execution overlaps on the GPU (several streams or host threads) race
+ *     on it: serialise them.
+ *   - Errors: those of kda_chunk_bwd, returned before any launch, plus
+ *     KDA_ERR_WORKSPACE when the problem needs more than
+ *     KDA_NOALLOC_SCRATCH_BYTES (kda_workspace_bytes(dims, KDA_PASS_BWD) >
+ *     KDA_NOALLOC_SCRATCH_BYTES). A bounded device wait that gives up is
+ *     reported by kda_noalloc_device_status, not by the call itself.
  * This entry point has no counterpart in the paper; it is a deployment aid.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
@@ -179,6 +188,16 @@ kda_status kda_chunk_bwd_noalloc(const kda_dims* dims, const void* q, const void
                                  const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
                                  const float* dht, void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0,
                                  kda_stream_t stream);
+
+/* Set-up of kda_chunk_bwd_noalloc on the current device: loads the module and
+ * looks up (again) the scratch array's device address. Allocates nothing
+ * beyond the module's own static array. KDA_ERR_CUDA if the look-up fails. */
+kda_status kda_noalloc_prepare(void);
+
+/* kda_device_status for kda_chunk_bwd_noalloc: synchronises `stream`, then
+ * reads the status word the last call on the current device left in the
+ * shared scratch (KDA_OK, or KDA_ERR_DEVICE_TIMEOUT if a bounded wait gave up). */
+kda_status kda_noalloc_device_status(kda_stream_t stream);
 
 /*
  * Per-kernel timing hook (for benchmarks and profiling; off by default).

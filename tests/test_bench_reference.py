@@ -22,6 +22,10 @@ def test_reference_arm_prints_one_complete_json_line():
     assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 0
     assert d["higher_is_better"] is True and d["vs_baseline"] is None
     assert d["config"]["workload"] == "bf16_b8_t4096_h32_k128"
+    # the same config keys as the GPU arm's line (both come from bench.workload_config)
+    for key in ("global_batch", "seq_len", "heads", "value_heads", "head_dim", "chunk", "parallelism", "l2"):
+        assert key in d["config"], key
+    assert d["config"]["value_heads"] == 32 and d["config"]["parallelism"] == "single"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     e2e = d["e2e"]

@@ -3,10 +3,9 @@ oracle on the same seeded inputs.
 
 Tolerances (per-tensor relative L2, oracle rounded to the output dtype):
 5e-3 for bf16 inputs (bf16 tensor-core operands, fp32 accumulation) and 1e-4
-for fp32 inputs. Small cases are compared in full; the full-size workloads are
-compared on whole independent units (one sequence x one key head and its value
-heads), which the oracle computes exactly, at the sizes and launch
-configuration the benchmark times.
+for fp32 inputs. Every case, the full-size workloads included, is compared
+element by element over whole tensors (the oracle runs on all host cores), at
+the sizes and in the launch configuration the benchmark times.
 """
 import dataclasses
 import functools
@@ -59,35 +58,27 @@ def _tol(inp):
     return TOL[inp.spec.dtype]
 
 
-def _check(name, got, ref64, out_dtype, tol, errs):
-    e = rel_l2(to64(got), round_like(ref64, out_dtype))
-    errs[name] = e
-    assert e <= tol, (name, e, tol)
+def _check(name, got, ref64, out_dtype, errs):
+    errs[name] = rel_l2(to64(got), round_like(ref64, out_dtype))
+
+
+def _report(name, errs):
+    """One greppable line per workload: the whole-tensor errors behind the error table."""
+    import json
+    print("PARITY " + json.dumps({"workload": name, **{k: float(v) for k, v in errs.items()}}))
 
 
 def compare_full(inp, out, ref):
+    """Whole-tensor relative L2 of every gradient against the oracle (rounded to the output dtype);
+    every tensor is measured before any is asserted, so a failure shows all of them."""
     dt, tol, errs = inp.torch_dtype, _tol(inp), {}
     for key in ("dq", "dk", "dv", "dbeta"):
-        _check(key, out[key], ref[key], dt, tol, errs)
-    _check("dg", out["dg"], ref["dg"], torch.float32, tol, errs)
+        _check(key, out[key], ref[key], dt, errs)
+    _check("dg", out["dg"], ref["dg"], torch.float32, errs)
     if inp.h0 is not None:
-        _check("dh0", out["dh0"], ref["dh0"], torch.float32, tol, errs)
+        _check("dh0", out["dh0"], ref["dh0"], torch.float32, errs)
+    assert all(e <= tol for e in errs.values()), (errs, tol)
     return errs
-
-
-def compare_unit(inp, out, n, h):
-    """Compare one (sequence n, key head h) unit against the oracle."""
-    ref = oracle.run_unit(inp, n, h)
-    b, e = inp.seq_bounds[n]
-    H, HV = inp.q.shape[2], inp.v.shape[2]
-    G = HV // H
-    rows = lambda t, hs: t.reshape(-1, *t.shape[2:])[b:e, hs].unsqueeze(0)
-    sl = dict(dq=rows(out["dq"], slice(h, h + 1)), dk=rows(out["dk"], slice(h, h + 1)),
-              dv=rows(out["dv"], slice(h * G, h * G + G)), dg=rows(out["dg"], slice(h * G, h * G + G)),
-              dbeta=rows(out["dbeta"], slice(h * G, h * G + G)))
-    if inp.h0 is not None:
-        sl["dh0"] = out["dh0"][n:n + 1, h * G:h * G + G]
-    return compare_full(inp, sl, ref)
 
 
 # ---------------------------------------------------------------- small cases
@@ -150,7 +141,7 @@ def test_tensor_core_forward_workload(kda):
     ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
     errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
                 states=rel_l2(to64(st), ref["s_in"]))
-    print("bf16_b1_t2048_h16_k128 forward", errs)
+    _report("bf16_b1_t2048_h16_k128 forward", errs)
     assert all(e <= _tol(inp) for e in errs.values()), errs
 
 
@@ -216,37 +207,72 @@ def test_workload_fp32_b1_t256_full(kda):
     inp = _workload("fp32_b1_t256_h2_k64")
     out = gpu_bwd(kda, inp)
     errs = compare_full(inp, out, oracle.run_inputs(inp))
-    print("fp32_b1_t256_h2_k64", errs)
+    _report("fp32_b1_t256_h2_k64", errs)
 
 
 def test_workload_bf16_b1_t2048_full(kda):
     inp = _workload("bf16_b1_t2048_h16_k128")
     out = gpu_bwd(kda, inp)
     errs = compare_full(inp, out, oracle.run_inputs(inp))
-    print("bf16_b1_t2048_h16_k128", errs)
+    _report("bf16_b1_t2048_h16_k128", errs)
 
 
-def test_workload_bf16_b8_t4096_sampled(kda):
-    inp = _workload("bf16_b8_t4096_h32_k128")
+def _full_backward(kda, name):
+    inp = _workload(name)
     out = gpu_bwd(kda, inp)
-    for n, h in [(0, 0), (7, 31), (3, 17)]:
-        print("bf16_b8_t4096_h32_k128", n, h, compare_unit(inp, out, n, h))
+    got = {k: (None if v is None else v.cpu()) for k, v in out.items()}
+    del out
+    torch.cuda.empty_cache()
+    errs = compare_full(inp, got, oracle.run_inputs(inp))
+    _report(name, errs)
+    return errs
 
 
-def test_workload_bf16_varlen_sampled(kda):
-    inp = _workload("bf16_varlen16_h32_k128")
-    out = gpu_bwd(kda, inp)
-    lens = [e - b for b, e in inp.seq_bounds]
-    picks = [int(np.argmin(lens)), int(np.argmax(lens)), 5]
-    for n, h in zip(picks, [3, 30, 11]):
-        print("bf16_varlen16_h32_k128", n, lens[n], h, compare_unit(inp, out, n, h))
+def test_workload_bf16_b8_t4096_full(kda):
+    """The benchmark workload (B=8 T=4096 H=HV=32), every element of every gradient."""
+    _full_backward(kda, "bf16_b8_t4096_h32_k128")
+
+
+def test_workload_bf16_varlen_full(kda):
+    """16 packed sequences of U[1,4096] tokens, every element of every gradient and of dh0."""
+    _full_backward(kda, "bf16_varlen16_h32_k128")
 
 
 @pytest.mark.slow
-def test_workload_bf16_t65536_gva_sampled(kda):
-    inp = _workload("bf16_b1_t65536_h16_hv32_k128")
+def test_workload_bf16_t65536_gva_full(kda):
+    """B=1 T=65536 with 16 key heads over 32 value heads (segmented state passes and the grouped
+    dq/dk sum), every element of every gradient and of dh0."""
+    _full_backward(kda, "bf16_b1_t65536_h16_hv32_k128")
+
+
+@pytest.mark.parametrize("name", ["bf16_b8_t4096_h32_k128", "bf16_varlen16_h32_k128",
+                                  "bf16_b1_t65536_h16_hv32_k128"])
+def test_workload_forward_full(kda, name):
+    """Forward o, ht and the fp32 chunk states on the large workloads, whole tensors."""
+    inp = _workload(name)
+    o, ht, st = gpu_fwd(kda, inp)
+    o, ht, st = o.cpu(), ht.cpu(), st.cpu()
+    torch.cuda.empty_cache()
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
+                states=rel_l2(to64(st), ref["s_in"]))
+    _report(name + " forward", errs)
+    assert all(e <= _tol(inp) for e in errs.values()), errs
+
+
+@pytest.mark.parametrize("seed", [11, 12, 13, 14, 15])
+def test_workload_bf16_b1_t2048_seeds(kda, seed):
+    """The B=1 T=2048 H=16 workload drawn from five more seeds: the bf16 error level is not a
+    property of one draw."""
+    inp = kda_inputs.make(dataclasses.replace(kda_inputs.WORKLOADS["bf16_b1_t2048_h16_k128"], seed=seed))
     out = gpu_bwd(kda, inp)
-    print("bf16_b1_t65536_h16_hv32_k128", compare_unit(inp, out, 0, 9))
+    errs = compare_full(inp, out, oracle.run_inputs(inp))
+    o, ht, st = gpu_fwd(kda, inp)
+    ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
+    errs.update(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
+                states=rel_l2(to64(st), ref["s_in"]))
+    _report(f"bf16_b1_t2048_h16_k128 seed {seed}", errs)
+    assert all(e <= _tol(inp) for e in errs.values()), errs
 
 
 # ------------------------------------------------------------ degenerate inputs

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import kda_inputs
-from tests.util import TOL, rel_l2, to64
+from tests.util import to64
 
 NOALLOC_BYTES = 64 * 1024 * 1024
 
@@ -27,6 +27,10 @@ def _lib():
     P = ctypes.c_void_p
     lib.kda_chunk_bwd_noalloc.restype = ctypes.c_int
     lib.kda_chunk_bwd_noalloc.argtypes = [ctypes.POINTER(kda.Dims)] + [P] * 17 + [P]
+    lib.kda_noalloc_prepare.restype = ctypes.c_int
+    lib.kda_noalloc_prepare.argtypes = []
+    lib.kda_noalloc_device_status.restype = ctypes.c_int
+    lib.kda_noalloc_device_status.argtypes = [P]
     return kda, lib
 
 
@@ -43,7 +47,8 @@ def _noalloc_bwd(kda, lib, inp, x):
                                    p(out["dq"]), p(out["dk"]), p(out["dv"]), p(out["dg"]), p(out["dbeta"]),
                                    p(out["dh0"]), kda._stream())
     assert rc == 0, kda.STATUS.get(rc, rc)
-    torch.cuda.synchronize()
+    # the bounded device waits of this call left no time-out in the shared scratch's status word
+    assert lib.kda_noalloc_device_status(kda._stream()) == 0
     return out
 
 
@@ -55,7 +60,12 @@ def _cuda(inp):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
+    """Both entry points launch the same deterministic kernels, so their results must agree bit for bit.
+    The larger case runs first, so the second call reads a scratch that still holds the first call's
+    contents: a stale-scratch read would show as a mismatch."""
     kda, lib = _lib()
+    torch.cuda.init()
+    assert lib.kda_noalloc_prepare() == 0  # the set-up phase: module load and address look-up
     cases = [
         kda_inputs.small(seed=41, B=1, T=0, H=2, HV=4, K=128, V=128, dtype="bf16", seq_lens=[150, 3, 64]),
         kda_inputs.small(seed=42, B=2, T=97, H=1, HV=1, K=64, V=64, dtype="f32", dht=False),
@@ -69,8 +79,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
         for key in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
             if ref[key] is None:
                 continue
-            err = rel_l2(to64(got[key]), to64(ref[key]))
-            assert err <= TOL[inp.spec.dtype], (key, err)
+            assert torch.equal(got[key], ref[key]), key
             assert np.isfinite(to64(got[key])).all(), key
 
 
