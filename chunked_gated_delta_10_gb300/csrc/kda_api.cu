@@ -44,7 +44,7 @@ struct Layout {
     size_t status, gam, w, u, vn, inv, aqk, sin, dso, dvn, dqt, dkh, dw, dgc, dqp, dkp, total;
     // tensor-core path regions
     bool tc;
-    size_t t_w, t_u, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc, t_seg_e, t_seg_p, t_seg_s0;
+    size_t t_w, t_invb, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc, t_seg_e, t_seg_p, t_seg_s0;
 };
 
 // bf16 inputs with K = V = 128 run on the tensor-core path (forward and backward).
@@ -69,11 +69,11 @@ Layout layout(const Prob& p, int pass, bool tc) {
     if (tc) {
         const size_t CH = NT * HV, TCD = (size_t)kC * 128 * 2, TCC = (size_t)kC * kC * 2, TDD = 128 * 128 * 2;
         L.t_w = take(CH * TCD);
-        L.t_u = take(CH * TCD);
         L.t_kh = take(CH * TCD);
         L.t_qs = take(CH * TCD);
         L.t_aqk = take(CH * TCC);
         L.t_inv = take(CH * TCC);
+        L.t_invb = take(CH * TCC);
         L.t_egc = take(CH * 128 * f);
         const SegPlan sp = seg_plan(p);
         if (sp.len) {  // segmented state passes: three fp32 K x V matrices per (sequence, head, segment)
@@ -155,7 +155,7 @@ TcWs carve_tc(void* base, const Layout& L) {
     auto at = [&](size_t off) { return off ? (uint8_t*)(b + off) : nullptr; };  // 0: region absent
     w.status = (int*)(b + L.status);
     w.w = at(L.t_w);
-    w.u = at(L.t_u);
+    w.invb = at(L.t_invb);
     w.kh = at(L.t_kh);
     w.qs = at(L.t_qs);
     w.vn = at(L.t_vn);
@@ -373,7 +373,7 @@ extern "C" kda_status kda_debug_ws_region(const kda_dims* dims, int32_t pass, co
     const struct {
         const char* n;
         size_t off;
-    } tab[] = {{"w", L.t_w}, {"u", L.t_u}, {"kh", L.t_kh}, {"qs", L.t_qs}, {"vn", L.t_vn}, {"dvn", L.t_dvn},
+    } tab[] = {{"w", L.t_w}, {"invb", L.t_invb}, {"kh", L.t_kh}, {"qs", L.t_qs}, {"vn", L.t_vn}, {"dvn", L.t_dvn},
                {"aqk", L.t_aqk}, {"inv", L.t_inv}, {"sin", L.t_sin}, {"dso", L.t_dso}, {"egc", L.t_egc}};
     if (!L.tc) return KDA_ERR_UNSUPPORTED;
     for (size_t i = 0; i < sizeof(tab) / sizeof(tab[0]); ++i)

@@ -41,12 +41,12 @@ cudaError_t simt_bwd(const Prob& p, bool bf16, const IO& io, const Ws& ws, cudaS
 
 // Workspace of the tensor-core path (bf16, K = V = 128). Per chunk-head
 // ch = chunk * HV + hv, bf16 tiles in the operand layout of tc_util.cuh:
-//   w, u, kh (K^), qs (scale Q~), vn (delta), dvn (d_delta): 64 x 128 (16 KB)
-//   aqk, inv: 64 x 64 (8 KB);  sin, dso: 128 x 128 (32 KB)
+//   w, kh (K^), qs (scale Q~), vn (delta), dvn (d_delta): 64 x 128 (16 KB)
+//   aqk, inv, invb (INV diag(beta)): 64 x 64 (8 KB);  sin, dso: 128 x 128 (32 KB)
 //   egc: 128 fp32 (e^Gamma_C per key channel)
 // dqp, dkp: fp32 [R, HV, K] per-value-head dq/dk before the group sum.
 struct TcWs {
-    uint8_t *w, *u, *kh, *qs, *vn, *dvn, *aqk, *inv, *sin, *dso;
+    uint8_t *w, *invb, *kh, *qs, *vn, *dvn, *aqk, *inv, *sin, *dso;
     float *egc, *dqp, *dkp;
     // segmented state passes (long sequences, few sweeps): per (sequence, value head, segment) fp32
     // K x V end states from a zero start, K x K transitions and start states

@@ -10,14 +10,17 @@
 //                 q e^(G-Gref), Kc = k e^(Gref-G) (Gref = middle row of the
 //                 chunk), one MMA [Kr; Qr] Kc^T giving Akk and Aqk together,
 //                 the inverse INV = (I + Akk)^-1 by blocked forward
-//                 substitution in fp32, then w = INV (beta K~) and
-//                 u = INV (beta V). Writes w, u, K^, scale*Q~, Aqk, INV and
-//                 e^(Gamma_C).
+//                 substitution in fp32, then INVb = INV diag(beta) and
+//                 w = INVb K~. Writes w, K^, scale*Q~, Aqk, INV, INVb and
+//                 e^(Gamma_C). u = INVb V is never formed on its own: the
+//                 state passes take it into delta's accumulator (below), so
+//                 it is not rounded to bf16 and makes no round trip.
 //   tc_state_fwd  per (sequence, value head[, segment]): the chunk loop
-//                 delta = u - w S, S <- e^(Gamma_C) S + K^^T delta with S in
-//                 registers (fp32) and a bf16 copy in shared memory; writes
-//                 S_in and delta of every chunk (or, for segmented sweeps,
-//                 the segment's end state and transition).
+//                 delta = INVb V - w S (one accumulator),
+//                 S <- e^(Gamma_C) S + K^^T delta with S in registers (fp32)
+//                 and a bf16 copy in shared memory; writes S_in and delta of
+//                 every chunk (or, for segmented sweeps, the segment's end
+//                 state and transition).
 //   tc_ds_rev     per (sequence, value head[, segment]), chunks in reverse:
 //                 dDelta = Aqk^T dO + K^ dS,
 //                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
@@ -165,22 +168,22 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 // ---------------------------------------------------------------------------
 // tc_intra: persistent, two 256-thread CTAs per SM (two threads per key channel:
 // rows 0..31 and 32..63), each walking its (chunk, value head) items round-robin.
-// Inputs staged by TMA and transformed in place (q -> scale Q~, k -> K^,
-// v -> beta V). The next item's q and k are fetched once the K^ / Q~ copies have
-// read their tiles, its v once the second MMA has consumed beta V, and its g
-// (registers) and beta while the current item finishes. 112 KB of shared memory.
+// Inputs staged by TMA and transformed in place (q -> scale Q~, k -> K^). The
+// next item's q and k are fetched once the K^ / Q~ copies have read their tiles,
+// and its g (registers) and beta while the current item finishes. 112 KB of
+// shared memory.
 // ---------------------------------------------------------------------------
 struct IS {
-    static constexpr int Q = 0, K = TCD, V = 2 * TCD, KQ = 3 * TCD, KC = 5 * TCD, XK = 6 * TCD, MISC = 7 * TCD;
-    // aliases: after the first MMA, KQ holds Akk / INV in fp32; after the last, W and U staging.
-    // after the first MMA, KC holds the bf16 INV tile and the inversion scratch.
-    static constexpr int AKK = KQ, FI = KQ + 16384, TINV = KC, XS = KC + TCC, WST = KQ, UST = KQ + TCD;
+    static constexpr int Q = 0, K = TCD, XB = 2 * TCD, KQ = 3 * TCD, KC = 5 * TCD, XK = 6 * TCD, MISC = 7 * TCD;
+    // aliases: after the first MMA, KQ holds Akk / INV in fp32; after the last, w staging.
+    // after the first MMA, KC holds the bf16 INV tile and the inversion scratch; XB holds the bf16 INVb tile.
+    static constexpr int AKK = KQ, FI = KQ + 16384, TINV = KC, XS = KC + TCC, TINVB = XB, WST = KQ;
     static constexpr int END = MISC + 512 + 64;  // beta (two item slots), barriers
 };
 constexpr int kIntraSmem = IS::END;
 
 struct IntraMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap q, k;
 };
 
 __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __restrict__ g,
@@ -201,8 +204,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     if (tid == 0) {
         *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
         if (*fail) *(volatile int*)ws.status = 10;
-        mbar_init(&bars[0], 2);
-        mbar_init(&bars[1], 2);
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
         mbar_init(&bars[2], 1);
         fence_mbar_init();
     }
@@ -221,10 +224,6 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 tma_load_3d(sm + IS::K + x * (TCD / 2), &maps.k, 64 * x, h, (int)r0, b);
             }
         };
-        auto issue_v = [&](int64_t r0, int hv, uint64_t* b) {
-            mbar_expect_tx(b, TCD);
-            for (int x = 0; x < 2; ++x) tma_load_3d(sm + IS::V + x * (TCD / 2), &maps.v, 64 * x, hv, (int)r0, b);
-        };
         int64_t w = blockIdx.x;
         int64_t r0;
         int c;
@@ -235,10 +234,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             float* sb0 = reinterpret_cast<float*>(sm + IS::MISC);
             sb0[tid] = tid < c ? __bfloat162float(beta[(r0 + tid) * HV + (int)(w % HV)]) : 0.f;
         }
-        if (tid == 0) {
-            issue_qk(r0, (int)(w % HV) / G, &bars[0]);
-            issue_v(r0, (int)(w % HV), &bars[0]);
-        }
+        if (tid == 0) issue_qk(r0, (int)(w % HV) / G, &bars[0]);
         uint32_t mph = 0;
         for (int i = 0; w < total; ++i, w += gridDim.x) {
             const int slot = i & 1;
@@ -270,7 +266,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             const float ref0 = tmp[512 + d0], ref1 = tmp[512 + d0 + 1], gC0 = tmp[640 + d0], gC1 = tmp[640 + d0 + 1];
             if (qt == 0) *reinterpret_cast<float2*>(ws.egc + ch * D + d0) = make_float2(exp2f(gC0), exp2f(gC1));
             if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
-            // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^, v -> beta V
+            // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^
 #pragma unroll
             for (int x = 0; x < 16; ++x) {
                 const int r = 16 * qt + x;
@@ -278,11 +274,9 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 const uint32_t o = a64.at(r);
                 const uint32_t k2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::K + o) : 0u;
                 const uint32_t q2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::Q + o) : 0u;
-                const uint32_t v2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::V + o) : 0u;
                 const float k0 = __uint_as_float(k2 << 16), k1 = __uint_as_float(k2 & 0xffff0000u);
                 const float q0 = __uint_as_float(q2 << 16), q1 = __uint_as_float(q2 & 0xffff0000u);
-                const float v0 = __uint_as_float(v2 << 16), v1 = __uint_as_float(v2 & 0xffff0000u);
-                const float b = sb[r], gm0 = G2[x], gm1 = G2[16 + x];
+                const float gm0 = G2[x], gm1 = G2[16 + x];
                 const float ep0 = fast_exp2(gm0 - ref0), em0 = fast_exp2(ref0 - gm0), E0 = fast_exp2(gm0),
                             eh0 = fast_exp2(gC0 - gm0);
                 const float ep1 = fast_exp2(gm1 - ref1), em1 = fast_exp2(ref1 - gm1), E1 = fast_exp2(gm1),
@@ -290,8 +284,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(k0 * ep0, k1 * ep1);
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(q0 * ep0, q1 * ep1);
                 *reinterpret_cast<uint32_t*>(sm + IS::KC + o) = pack2(k0 * em0, k1 * em1);
-                *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(b * k0 * E0, b * k1 * E1);
-                *reinterpret_cast<uint32_t*>(sm + IS::V + o) = pack2(b * v0, b * v1);
+                *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(k0 * E0, k1 * E1);
                 *reinterpret_cast<uint32_t*>(sm + IS::K + o) = pack2(k0 * eh0, k1 * eh1);
                 *reinterpret_cast<uint32_t*>(sm + IS::Q + o) = pack2(p.scale * q0 * E0, p.scale * q1 * E1);
             }
@@ -346,47 +339,51 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             tc_fence_before();
             __syncthreads();
             tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
+            // INV and INVb = INV diag(beta) (column j scaled by beta_j) as bf16 operand tiles
             for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
                 const int r = e >> 3, c0 = (e & 7) * 8;
-                if (inv_zero_block(r, c0))
+                if (inv_zero_block(r, c0)) {
                     *reinterpret_cast<uint4*>(sm + IS::TINV + tile_off(r, c0, kC)) = make_uint4(0u, 0u, 0u, 0u);
-                else
-                    st_tile_row8(sm + IS::TINV, r, c0, kC, Fi + r * kC + c0);
+                    *reinterpret_cast<uint4*>(sm + IS::TINVB + tile_off(r, c0, kC)) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
+                    const float* fr = Fi + r * kC + c0;
+                    st_tile_row8(sm + IS::TINV, r, c0, kC, fr);
+                    float xb[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) xb[t] = fr[t] * sb[c0 + t];
+                    st_tile_row8(sm + IS::TINVB, r, c0, kC, xb);
+                }
             }
             fence_async_smem();
             __syncthreads();
             if (tid == 0) {
                 tc_fence_after();
-                // w = INV (beta K~), u = INV (beta V): chunk rows on TMEM lanes (M = 64, N = 128)
+                // w = INVb K~: chunk rows on TMEM lanes (M = 64, N = 128)
                 const uint32_t id = idesc_bf16(64, 128, false, true);
-                const uint32_t ti = smem_u32(sm + IS::TINV);
+                const uint32_t ti = smem_u32(sm + IS::TINVB);
                 for (int ks = 0; ks < kC / 16; ++ks)
                     mma_bf16(tmem, desc_kmajor(ti, kC, ks), desc_mnmajor(smem_u32(sm + IS::XK), kC, ks), id, ks > 0);
-                for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_bf16(tmem + 128, desc_kmajor(ti, kC, ks), desc_mnmajor(smem_u32(sm + IS::V), kC, ks), id,
-                             ks > 0);
                 mma_commit(&bars[2]);
                 bulk_store(ws.inv + ch * TCC, sm + IS::TINV, TCC);
+                bulk_store(ws.invb + ch * TCC, sm + IS::TINVB, TCC);
                 bulk_commit();
             }
             if (!wait_all(&bars[2], mph, ws.status, 13, fail)) break;
             mph ^= 1;
-            if (tid == 0 && has_next) issue_v(r0n, hvn, &bars[slot ^ 1]);  // beta V is consumed
             if (has_next) load_g_pair(g, r0n, cn, HV, hvn, d0, qt, G2);
             tc_fence_after();
-            {  // w, u rows: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+            {  // w rows: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
                 const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
                 const uint32_t lb = (uint32_t)(32 * (warp & 3)) << 16;
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int col = 32 * (t & 1) + cb;
+                for (int t = 0; t < 2; ++t) {
+                    const int col = 32 * t + cb;
                     float x[32];
-                    tmem_ld32(tmem + lb + 128 * (t >> 1) + col, x);
+                    tmem_ld32(tmem + lb + col, x);
                     tmem_ld_wait();
                     if (lane < 16) {
-                        uint8_t* dst = sm + ((t >> 1) ? IS::UST : IS::WST);
 #pragma unroll
-                        for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(dst, r, col + c8, kC, x + c8);
+                        for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(sm + IS::WST, r, col + c8, kC, x + c8);
                     }
                 }
             }
@@ -396,7 +393,6 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             __syncthreads();
             if (tid == 0) {
                 bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
-                bulk_store(ws.u + ch * TCD, sm + IS::UST, TCD);
                 bulk_commit();
                 bulk_wait_read();  // the scratch and INV areas are rewritten by the next item
             }
@@ -428,17 +424,20 @@ struct SegArg {
 // tc_state_fwd: one CTA per (value head, sequence[, segment]), 256 threads;
 // thread t owns state row k = t % 128, columns 64 (t / 128) .. +63 in fp32
 // registers. A bf16 copy of S in shared memory feeds the MMAs and is the S_in
-// checkpoint. Chunk inputs: u and e^Gamma_C double-buffered; w and K^
-// single-buffered, each refetched as soon as its MMA has consumed it. delta
-// overwrites u in place.
+// checkpoint. Chunk inputs: V (TMA) and e^Gamma_C double-buffered; w with INVb,
+// and K^, single-buffered, each refetched as soon as its MMA has consumed it.
+// delta = INVb V - w S accumulates in one TMEM accumulator and overwrites V in
+// place.
 // ---------------------------------------------------------------------------
 struct FwdSm {
-    static constexpr int W = 0, KH = TCD, U = 2 * TCD, UBUF = TCD + 1024;  // u tile, then e^Gamma_C (512 B)
+    static constexpr int W = 0, IVB = TCD, KH = TCD + TCC, U = 2 * TCD + TCC;
+    static constexpr int UBUF = TCD + 1024;  // V (then delta) tile, then e^Gamma_C (512 B)
     static constexpr int S = U + 2 * UBUF, BARS = S + TDD, END = BARS + 64;
 };
 constexpr int kFwdSmem = 1024 + FwdSm::END;
 
-__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg) {
+__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg,
+                                                          const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + FwdSm::S;
@@ -475,16 +474,21 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
         for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : (mode == 2 && 64 * vh + j == k ? 1.f : 0.f);
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
-    auto issue_u = [&](int it) {
+    auto issue_u = [&](int it) {  // V rows of chunk it (TMA) and e^Gamma_C
         const int b = (it - lo) & 1;
         uint8_t* buf = sm + FwdSm::U + b * FwdSm::UBUF;
         mbar_expect_tx(&bars[b], (with_u ? TCD : 0) + 512);
-        if (with_u) bulk_load(buf, ws.u + chunk(it) * TCD, TCD, &bars[b]);
+        if (with_u) {
+            const int row = (int)(bos + (int64_t)it * kC);
+            tma_load_3d(buf, &tm_v, 0, hv, row, &bars[b]);
+            tma_load_3d(buf + TCD / 2, &tm_v, 64, hv, row, &bars[b]);
+        }
         bulk_load(buf + TCD, ws.egc + chunk(it) * D, 512, &bars[b]);
     };
-    auto issue_w = [&](int it) {
-        mbar_expect_tx(&bars[2], TCD);
+    auto issue_w = [&](int it) {  // w and INVb
+        mbar_expect_tx(&bars[2], TCD + (with_u ? TCC : 0));
         bulk_load(sm + FwdSm::W, ws.w + chunk(it) * TCD, TCD, &bars[2]);
+        if (with_u) bulk_load(sm + FwdSm::IVB, ws.invb + chunk(it) * TCC, TCC, &bars[2]);
     };
     auto issue_kh = [&](int it) {
         mbar_expect_tx(&bars[3], TCD);
@@ -512,12 +516,22 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
         if (!wait_all(&bars[2], ph, ws.status, 21, fail)) break;
-        if (tid == 0) {  // delta accumulator = w S (chunk rows on TMEM lanes, M = 64, N = 128)
+        // delta accumulator = -w S + INVb V (chunk rows on TMEM lanes, M = 64, N = 128): the w S part
+        // is issued first and runs while V may still be landing
+        const uint32_t idd = idesc_bf16(64, 128, false, true);
+        if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 128, false, true);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
-                         ks > 0);
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks),
+                         idesc_neg_a(idd), ks > 0);
+        }
+        if (!wait_all(&bars[rel & 1], (rel >> 1) & 1, ws.status, 24, fail)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            if (with_u)
+                for (int ks = 0; ks < kC / 16; ++ks)
+                    mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
+                             idd, 1);
             mma_commit(&bars[4]);
             if (ckpt) {
                 bulk_store(ws.sin + ch * TDD, tS, TDD);
@@ -526,10 +540,9 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
         }
         if (!wait_all(&bars[4], mph, ws.status, 22, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w is consumed
-        if (!wait_all(&bars[rel & 1], (rel >> 1) & 1, ws.status, 24, fail)) break;
+        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w and INVb are consumed
         tc_fence_after();
-        {  // delta = u - w S in place of u: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+        {  // delta (bf16) in place of V: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
             const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -538,13 +551,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                        float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                        if (with_u) ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
-                        st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-                    }
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * h + c8, kC, acc + c8);
                 }
             }
         }
@@ -824,15 +831,16 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
 // ---------------------------------------------------------------------------
 // tc_state_load: the backward's replacement of tc_state_fwd when the forward's
 // states are given. One CTA per (chunk, value head), 256 threads: S_in (fp32)
-// becomes the bf16 checkpoint tile, and delta = u - w S_in with chunk rows on
-// TMEM lanes; the same arithmetic as tc_state_fwd on the same state values.
+// becomes the bf16 checkpoint tile, and delta = INVb V - w S_in with chunk rows
+// on TMEM lanes; the same arithmetic as tc_state_fwd on the same state values.
 // ---------------------------------------------------------------------------
 struct LoadSm {
-    static constexpr int W = 0, U = TCD, S = 2 * TCD, BARS = S + TDD, END = BARS + 64;
+    static constexpr int W = 0, U = TCD, S = 2 * TCD, IVB = S + TDD, BARS = IVB + TCC, END = BARS + 64;
 };
 constexpr int kLoadSmem = 1024 + LoadSm::END;
 
-__global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* __restrict__ states, TcWs ws) {
+__global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* __restrict__ states, TcWs ws,
+                                                           const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     uint8_t* tS = sm + LoadSm::S;
@@ -849,9 +857,14 @@ __global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* _
         mbar_init(&bars[1], 1);
         fence_mbar_init();
         *fail = 0;
-        mbar_expect_tx(&bars[0], 2 * TCD);
+        int64_t r0;
+        int c;
+        chunk_rows(p, (int64_t)blockIdx.x, r0, c);
+        mbar_expect_tx(&bars[0], 2 * TCD + TCC);
         bulk_load(sm + LoadSm::W, ws.w + ch * TCD, TCD, &bars[0]);
-        bulk_load(tU, ws.u + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + LoadSm::IVB, ws.invb + ch * TCC, TCC, &bars[0]);
+        tma_load_3d(tU, &tm_v, 0, (int)blockIdx.y, (int)r0, &bars[0]);
+        tma_load_3d(tU + TCD / 2, &tm_v, 64, (int)blockIdx.y, (int)r0, &bars[0]);
     }
     if (warp == 0) tmem_alloc(tslot, 128);
     {  // row k, this thread's 64 columns of S_in as bf16
@@ -869,19 +882,22 @@ __global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* _
     tc_fence_after();
     const uint32_t tmem = *tslot;
     if (!wait_all(&bars[0], 0, ws.status, 51, fail)) goto cleanup;
-    if (tid == 0) {  // delta accumulator = w S_in (M = 64, N = 128)
+    if (tid == 0) {  // delta accumulator = -w S_in + INVb V (M = 64, N = 128), the order of tc_state_fwd
         tc_fence_after();
         const uint32_t id = idesc_bf16(64, 128, false, true);
         for (int ks = 0; ks < D / 16; ++ks)
-            mma_bf16(tmem, desc_kmajor(smem_u32(sm + LoadSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
-                     ks > 0);
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + LoadSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks),
+                     idesc_neg_a(id), ks > 0);
+        for (int ks = 0; ks < kC / 16; ++ks)
+            mma_bf16(tmem, desc_kmajor(smem_u32(sm + LoadSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks), id,
+                     1);
         mma_commit(&bars[1]);
         bulk_store(ws.sin + ch * TDD, tS, TDD);
         bulk_commit();
     }
     if (!wait_all(&bars[1], 0, ws.status, 52, fail)) goto cleanup;
     tc_fence_after();
-    {  // delta = u - w S_in in place of u: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
+    {  // delta (bf16) in place of V: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
         const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
         const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
 #pragma unroll
@@ -891,13 +907,7 @@ __global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* _
             tmem_ld_wait();
             if (lane < 16) {
 #pragma unroll
-                for (int c8 = 0; c8 < 32; c8 += 8) {
-                    float x[8];
-                    ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
-                    st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-                }
+                for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * h + c8, kC, acc + c8);
             }
         }
     }
@@ -917,23 +927,24 @@ cleanup:
 // ---------------------------------------------------------------------------
 // tc_fwd_out: the forward's state pass with the output fused in. One CTA per
 // (value head, sequence), 256 threads, thread t owns state row k = t % 128,
-// columns 64 (t / 128) .. +63. Per chunk: delta = u - w S (chunk rows on TMEM
-// lanes, in place of u), then S <- e^(Gamma_C) S + K^^T delta and
+// columns 64 (t / 128) .. +63. Per chunk: delta = INVb V - w S (chunk rows on
+// TMEM lanes, in place of V), then S <- e^(Gamma_C) S + K^^T delta and
 // o = (scale Q~) S + Aqk delta in one MMA group; o leaves as bf16 rows. Inputs
-// are single-buffered in two groups: w is refetched once the delta MMA has
-// consumed it, the rest once the state and output MMAs have.
+// are single-buffered in two groups: w and INVb are refetched once the delta
+// MMA has consumed them, the rest once the state and output MMAs have. Two
+// CTAs per SM: 112.6 KB of shared memory each, from a 1024-byte aligned base
+// (no alignment slack).
 // ---------------------------------------------------------------------------
 struct FoSm {
-    static constexpr int W = 0, KH = TCD, QS = 2 * TCD, U = 3 * TCD, AQK = 4 * TCD, EGC = 4 * TCD + TCC;
-    static constexpr int S = EGC + 1024, BARS = S + TDD, END = BARS + 64;
+    static constexpr int W = 0, IVB = TCD, KH = TCD + TCC, QS = 2 * TCD + TCC, U = 3 * TCD + TCC;
+    static constexpr int AQK = 4 * TCD + TCC, S = 4 * TCD + 2 * TCC, EGC = S + TDD, BARS = EGC + 512, END = BARS + 64;
 };
-constexpr int kFoSmem = 1024 + FoSm::END;
+constexpr int kFoSmem = FoSm::END;
 
 __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
                                                         float* __restrict__ states, bf16* __restrict__ o, TcWs ws,
-                                                        SegArg sg) {
-    extern __shared__ uint8_t smraw[];
-    uint8_t* sm = align1024(smraw);
+                                                        SegArg sg, const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ __align__(1024) uint8_t sm[];
     uint8_t* tS = sm + FoSm::S;
     uint8_t* tU = sm + FoSm::U;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FoSm::BARS);  // w, group 2, mma
@@ -953,7 +964,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     if (tid == 0) {
         for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
         fence_mbar_init();
-        *fail = 0;
+        *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
+        if (*fail) *(volatile int*)ws.status = 70;
     }
     if (warp == 0) tmem_alloc(tslot, 256);
     float S[64];
@@ -964,16 +976,19 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
-    auto issue_w = [&](int it) {
-        mbar_expect_tx(&bars[0], TCD);
+    auto issue_w = [&](int it) {  // w and INVb
+        mbar_expect_tx(&bars[0], TCD + TCC);
         bulk_load(sm + FoSm::W, ws.w + chunk(it) * TCD, TCD, &bars[0]);
+        bulk_load(sm + FoSm::IVB, ws.invb + chunk(it) * TCC, TCC, &bars[0]);
     };
-    auto issue_g2 = [&](int it) {  // K^, scale Q~, u, Aqk, e^Gamma_C
+    auto issue_g2 = [&](int it) {  // K^, scale Q~, V (TMA), Aqk, e^Gamma_C
         const int64_t ch = chunk(it);
+        const int row = (int)(bos + (int64_t)it * kC);
         mbar_expect_tx(&bars[1], 3 * TCD + TCC + 512);
         bulk_load(sm + FoSm::KH, ws.kh + ch * TCD, TCD, &bars[1]);
         bulk_load(sm + FoSm::QS, ws.qs + ch * TCD, TCD, &bars[1]);
-        bulk_load(tU, ws.u + ch * TCD, TCD, &bars[1]);
+        tma_load_3d(tU, &tm_v, 0, hv, row, &bars[1]);
+        tma_load_3d(tU + TCD / 2, &tm_v, 64, hv, row, &bars[1]);
         bulk_load(sm + FoSm::AQK, ws.aqk + ch * TCC, TCC, &bars[1]);
         bulk_load(sm + FoSm::EGC, ws.egc + ch * D, 512, &bars[1]);
     };
@@ -982,12 +997,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
-    if (tid == 0 && lo < hi) {
+    const bool run = *(volatile int*)fail == 0;
+    if (tid == 0 && lo < hi && run) {
         issue_w(lo);
         issue_g2(lo);
     }
     uint32_t mph = 0;
-    for (int it = lo; it < hi; ++it) {
+    for (int it = lo; it < hi && run; ++it) {
         const int64_t ch = chunk(it);
         const uint32_t ph = (uint32_t)(it - lo) & 1;
         // bf16 copy of S (row k, this thread's 64 columns): operand of the delta and output MMAs
@@ -1000,21 +1016,28 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
             for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
         }
         if (!wait_all(&bars[0], ph, ws.status, 71, fail)) break;
-        if (tid == 0) {  // delta accumulator = w S (M = 64, N = 128)
+        // delta accumulator = -w S + INVb V (M = 64, N = 128): the w S part runs while group 2 may still land
+        const uint32_t idd = idesc_bf16(64, 128, false, true);
+        if (tid == 0) {
             tc_fence_after();
-            const uint32_t id = idesc_bf16(64, 128, false, true);
             for (int ks = 0; ks < D / 16; ++ks)
-                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), id,
-                         ks > 0);
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks),
+                         idesc_neg_a(idd), ks > 0);
+        }
+        if (!wait_all(&bars[1], ph, ws.status, 73, fail)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
+                         idd, 1);
             mma_commit(&bars[2]);
         }
         if (!wait_all(&bars[2], mph, ws.status, 72, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w is consumed
-        if (!wait_all(&bars[1], ph, ws.status, 73, fail)) break;
+        if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w and INVb are consumed
         tc_fence_after();
         const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);  // M = 64 row of this lane, column half
-        {  // delta = u - w S in place of u
+        {  // delta (bf16) in place of V
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 float acc[32];
@@ -1022,13 +1045,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) {
-                        float x[8];
-                        ld_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-#pragma unroll
-                        for (int t = 0; t < 8; ++t) x[t] -= acc[c8 + t];
-                        st_tile_row8(tU, r, cb + 32 * h + c8, kC, x);
-                    }
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * h + c8, kC, acc + c8);
                 }
             }
         }
@@ -1130,10 +1147,9 @@ cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream
     const int64_t rows = (int64_t)p.B * p.T;
     IntraMaps im;
     memset(&im, 0, sizeof(im));
-    const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
+    const uint64_t rq = (uint64_t)p.H * D * 2;
     if (!make_tmap_bf16_3d(&im.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&im.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC))
+        !make_tmap_bf16_3d(&im.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC))
         return cudaErrorInvalidValue;
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1147,21 +1163,31 @@ cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream
 
 }  // namespace
 
+// Tensor map of V [rows, HV, 128] bf16 in 64 x 64 boxes (one 64-column half of a chunk's rows).
+static bool make_tmap_v(CUtensorMap* m, const Prob& p, const void* v) {
+    memset(m, 0, sizeof(*m));
+    const int64_t rows = (int64_t)p.B * p.T;
+    return rows == 0 || make_tmap_bf16_3d(m, v, D, (uint64_t)p.HV, (uint64_t)rows, (uint64_t)D * 2,
+                                          (uint64_t)p.HV * D * 2, 64, 1, kC);
+}
+
 cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
     if ((e = set_smem(k_tc_fwd_out, kFoSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
+    CUtensorMap tm_v;
+    if (!make_tmap_v(&tm_v, p, io.v)) return cudaErrorInvalidValue;
     if ((e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     const SegPlan sp = seg_plan(p);
     if (sp.len) {  // segment ends and transitions, their chain, then o per segment
         const SegArg ends{sp.len, sp.M, kSegEnds};
-        k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends);
+        k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends, tm_v);
         note_launch("tc_state_fwd_seg", st);
         k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
         note_launch("tc_seg_combine", st);
     }
     k_tc_fwd_out<<<dim3(p.HV, p.N, sp.M), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
-                                                              SegArg{sp.len, sp.M, sp.len ? kSegCkpt : kSegNone});
+                                                              SegArg{sp.len, sp.M, sp.len ? kSegCkpt : kSegNone}, tm_v);
     note_launch("tc_fwd_out", st);
     return cudaGetLastError();
 }
@@ -1177,24 +1203,26 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if (rows > 0 && !make_tmap_bf16_3d(&tm_do, io.d_o, D, (uint64_t)p.HV, (uint64_t)rows, (uint64_t)D * 2,
                                        (uint64_t)p.HV * D * 2, 64, 1, kC))
         return cudaErrorInvalidValue;
+    CUtensorMap tm_v;
+    if (!make_tmap_v(&tm_v, p, io.v)) return cudaErrorInvalidValue;
     if (stages >= 1 && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     const SegPlan sp = seg_plan(p);
     const SegArg ends{sp.len, sp.M, kSegEnds}, ckpt{sp.len, sp.M, kSegCkpt}, whole{0, 1, kSegNone};
     if (stages >= 2) {
         if (io.states_in) {  // the forward's saved states: no sequential recompute
             if (p.NT > 0) {
-                k_tc_state_load<<<dim3((unsigned)p.NT, p.HV), 256, kLoadSmem, st>>>(p, io.states_in, ws);
+                k_tc_state_load<<<dim3((unsigned)p.NT, p.HV), 256, kLoadSmem, st>>>(p, io.states_in, ws, tm_v);
                 note_launch("tc_state_load", st);
             }
         } else if (sp.len) {  // two-level: segment ends and transitions, their chain, then the checkpoints
-            k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends);
+            k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends, tm_v);
             note_launch("tc_state_fwd_seg", st);
             k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
             note_launch("tc_seg_combine", st);
-            k_tc_state_fwd<<<dim3(p.HV, p.N, sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ckpt);
+            k_tc_state_fwd<<<dim3(p.HV, p.N, sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ckpt, tm_v);
             note_launch("tc_state_fwd", st);
         } else {
-            k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, whole);
+            k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, whole, tm_v);
             note_launch("tc_state_fwd", st);
         }
     }

@@ -67,12 +67,17 @@ def setup():
 
     ref = run_chunked(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.scale, inp.h0, inp.do, inp.dht, inp.cu_seqlens,
                       keep=True)
-    return dict(region=region, ref=ref, HV=4, dh0=dh0.cpu().double().numpy(), dims=dims)
+    # rows of every global chunk, for the column scaling of INV diag(beta)
+    idx, _, _ = kda.prepare_chunks(inp.cu_seqlens)
+    cu = inp.cu_seqlens.tolist()
+    rows = {gc: (cu[n] + 64 * i, min(cu[n + 1], cu[n] + 64 * (i + 1))) for gc, (n, i) in enumerate(idx.tolist())}
+    beta = inp.beta[0].double().numpy()
+    return dict(region=region, ref=ref, HV=4, dh0=dh0.cpu().double().numpy(), dims=dims, rows=rows, beta=beta)
 
 
 # (workspace name, tile rows, tile cols, oracle key, transform of the oracle value)
 TILES = [
-    ("w", 64, 128, "w", None), ("u", 64, 128, "u", None), ("kh", 64, 128, "Kh", None),
+    ("w", 64, 128, "w", None), ("invb", 64, 64, "INV", "beta_cols"), ("kh", 64, 128, "Kh", None),
     ("aqk", 64, 64, "Aqk", None), ("inv", 64, 64, "INV", None),
     ("sin", 128, 128, "S_in", None), ("vn", 64, 128, "delta", None),
     ("dso", 128, 128, "dS_out", None), ("dvn", 64, 128, "d_delta", None),
@@ -89,8 +94,11 @@ def test_stage_tiles(setup, name, R, C, key, tf):
         raw = reg[(gc * HV + hv) * size:(gc * HV + hv + 1) * size]
         got = untile(raw, R, C)
         want = ch[key]
+        if tf == "beta_cols":  # INV diag(beta): column j scaled by beta of the chunk's row j
+            r0, r1 = setup["rows"][gc]
+            want = want * setup["beta"][r0:r1, hv][None, :]
         pad = np.zeros((R, C))
-        if key == "INV":  # padded rows of a partial chunk: (I + Akk) is the identity there
+        if key == "INV" and tf is None:  # padded rows of a partial chunk: (I + Akk) is the identity there
             pad = np.eye(R)
         pad[:want.shape[0], :want.shape[1]] = want
         got_all.append(got)
