@@ -392,10 +392,10 @@ def gpu_arm(args):
     lib = kda.load()
 
     spec = kda_inputs.WORKLOADS[args.workload]
-    if args.batch:
+    if args.batch or args.seq_len:
         import dataclasses
 
-        spec = dataclasses.replace(spec, B=args.batch)
+        spec = dataclasses.replace(spec, B=args.batch or spec.B, T=args.seq_len or spec.T)
     inp = kda_inputs.make(spec)
     B, T, H, K = inp.q.shape
     HV, V = inp.v.shape[2], inp.v.shape[3]
@@ -495,7 +495,8 @@ def gpu_arm(args):
     dom = max(tot, key=tot.get)
     avg = tot[dom] / len(per[dom])
     peaks, peak_src = load_peaks()
-    bound, abytes, aflops = kernel_cost(dom, B, T, H, HV, K, V, nck=nck)
+    ib = 2 if spec.dtype == "bf16" else 4
+    bound, abytes, aflops = kernel_cost(dom, B, T, H, HV, K, V, in_bytes=ib, nck=nck)
     if bound == "hbm":
         ach, pk, unit = abytes / avg / 1e9, peaks["hbm_gbs"], "GB/s"
     elif bound == "tensor":
@@ -509,7 +510,7 @@ def gpu_arm(args):
                 "kernels_ms": {n: 1e3 * tot[n] / len(per[n]) for n in names}}
     seq_states = N * HV * K * V * ((1 if "h0" in x else 0) + (0 if mode == "fwd" else
                                                              (1 if "dht" in x else 0) + (1 if "h0" in x else 0)))
-    sc = pass_cost(mode, B, T, H, HV, K, V, nck=nck, seq_states=seq_states)
+    sc = pass_cost(mode, B, T, H, HV, K, V, in_bytes=ib, nck=nck, seq_states=seq_states)
     step_s = elapsed / args.steps
     path = {"bytes_alg": sc["bytes"], "flops_alg": sc["flops"],
             "hbm_frac": sc["bytes"] / step_s / 1e9 / peaks["hbm_gbs"],
@@ -557,14 +558,14 @@ def gpu_arm(args):
     e2e_val, _ = aggregate(tokens * e2e_steps, e0.elapsed_time(e1) / 1e3, world, device)
 
     extra = {}
-    if args.batch:
-        extra["workload"] = f"{spec.name} with B={args.batch}"
+    if args.batch or args.seq_len:
+        extra["workload"] = f"{spec.name} with B={spec.B} T={spec.T}"
     if mode != "bwd":
         extra["pass"] = mode
     line = {"metric": METRICS[mode], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": tmax / args.steps * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(inp, world, extra),
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if spec.dtype == "bf16" else "f32",
+            "data": "synthetic", "config": workload_config(inp, world, extra),
             "timing": "value and ms_per_step: mean over the K back-to-back steps between two CUDA events; the "
                       "library records one CUDA event after each of its launches inside that region (per-kernel "
                       "times); step_ms: per-step spans from those events",
@@ -594,12 +595,16 @@ def main():
     ap.add_argument("--pass", dest="mode", default="bwd", choices=list(METRICS),
                     help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
                          "bwd-states: backward from saved chunk states")
-    ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[n for n in kda_inputs.WORKLOAD_ORDER if kda_inputs.WORKLOADS[n].dtype == "bf16"],
+    ap.add_argument("--workload", default=WORKLOAD, choices=kda_inputs.WORKLOAD_ORDER,
                     help="the workload of the JSON line (default: the B=8 T=4096 H=HV=32 benchmark)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="override the tokens per sequence of a dense workload (smaller cases for profiling; not "
+                         "the workload's own line)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size (smaller cases for profiling; not the benchmark workload)")
     args = ap.parse_args()
+    if args.seq_len and kda_inputs.WORKLOADS[args.workload].varlen_n:
+        ap.error("--seq-len applies to dense workloads only")
     if args.impl == "reference":
         reference_arm(args)
     else:

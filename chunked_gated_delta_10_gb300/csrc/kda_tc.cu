@@ -8,7 +8,8 @@
 //   tc_intra      persistent, per (chunk, value head): gate cumsum in log2
 //                 units, the decayed factors Kr = k e^(G-Gref), Qr =
 //                 q e^(G-Gref), Kc = k e^(Gref-G) (Gref = middle row of the
-//                 chunk), one MMA [Kr; Qr] Kc^T giving Akk and Aqk together,
+//                 chunk), one MMA group [Kr; Qr] Kc^T giving Akk and Aqk together
+//                 (Kc as a bf16 pair hi + lo, so its rounding drops out),
 //                 the inverse INV = (I + Akk)^-1 by blocked forward
 //                 substitution in fp32, then INVb = INV diag(beta) and
 //                 w = INVb K~. Writes w, K^, scale*Q~, Aqk, INV, INVb and
@@ -175,6 +176,7 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 // ---------------------------------------------------------------------------
 struct IS {
     static constexpr int Q = 0, K = TCD, XB = 2 * TCD, KQ = 3 * TCD, KC = 5 * TCD, XK = 6 * TCD, MISC = 7 * TCD;
+    // XB holds the low part of Kc (Kc - bf16(Kc), rounded to bf16) for the first MMA.
     // aliases: after the first MMA, KQ holds Akk / INV in fp32; after the last, w staging.
     // after the first MMA, KC holds the bf16 INV tile and the inversion scratch; XB holds the bf16 INVb tile.
     static constexpr int AKK = KQ, FI = KQ + 16384, TINV = KC, XS = KC + TCC, TINVB = XB, WST = KQ;
@@ -283,7 +285,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                             eh1 = fast_exp2(gC1 - gm1);
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(k0 * ep0, k1 * ep1);
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(q0 * ep0, q1 * ep1);
-                *reinterpret_cast<uint32_t*>(sm + IS::KC + o) = pack2(k0 * em0, k1 * em1);
+                {  // Kc as a bf16 pair and the bf16 pair of its rounding remainder
+                    const float c0 = k0 * em0, c1 = k1 * em1;
+                    const uint32_t hi = pack2(c0, c1);
+                    *reinterpret_cast<uint32_t*>(sm + IS::KC + o) = hi;
+                    *reinterpret_cast<uint32_t*>(sm + IS::XB + o) =
+                        pack2(c0 - __uint_as_float(hi << 16), c1 - __uint_as_float(hi & 0xffff0000u));
+                }
                 *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(k0 * E0, k1 * E1);
                 *reinterpret_cast<uint32_t*>(sm + IS::K + o) = pack2(k0 * eh0, k1 * eh1);
                 *reinterpret_cast<uint32_t*>(sm + IS::Q + o) = pack2(p.scale * q0 * E0, p.scale * q1 * E1);
@@ -293,10 +301,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             __syncthreads();
             tc_fence_after();
             if (tid == 0) {
+                // [Kr; Qr] (Kc_hi + Kc_lo)^T: the remainder of Kc's rounding is carried by a second product
                 const uint32_t id = idesc_bf16(128, 64, false, false);
                 for (int ks = 0; ks < D / 16; ++ks)
                     mma_bf16(tmem, desc_kmajor(smem_u32(sm + IS::KQ), 128, ks),
                              desc_kmajor(smem_u32(sm + IS::KC), kC, ks), id, ks > 0);
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16(tmem, desc_kmajor(smem_u32(sm + IS::KQ), 128, ks),
+                             desc_kmajor(smem_u32(sm + IS::XB), kC, ks), id, 1);
                 mma_commit(&bars[2]);
                 bulk_store(ws.kh + ch * TCD, sm + IS::K, TCD);
                 bulk_store(ws.qs + ch * TCD, sm + IS::Q, TCD);
