@@ -862,7 +862,6 @@ __global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* _
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k = tid & 127, vh = tid >> 7;
     const int64_t ch = (int64_t)blockIdx.x * p.HV + blockIdx.y;
     if (tid == 0) {
         mbar_init(&bars[0], 1);
@@ -879,13 +878,20 @@ __global__ void __launch_bounds__(256, 3) k_tc_state_load(Prob p, const float* _
         tma_load_3d(tU + TCD / 2, &tm_v, 64, (int)blockIdx.y, (int)r0, &bars[0]);
     }
     if (warp == 0) tmem_alloc(tslot, 128);
-    {  // row k, this thread's 64 columns of S_in as bf16
-        const float4* src = reinterpret_cast<const float4*>(states + (ch * D + k) * D + 64 * vh);
+    {  // S_in as bf16: warp w reads whole rows w, w + 8, ..., one 512-byte row per load instruction;
+       // lane l converts columns 4l .. 4l + 3
+        const float4* src = reinterpret_cast<const float4*>(states + ch * D * D) + lane;
 #pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) {
-            const float4 a = src[c8 / 4], b = src[c8 / 4 + 1];
-            const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            st_tile_row8(tS, k, 64 * vh + c8, D, x);
+        for (int h = 0; h < 2; ++h) {
+            float4 a[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a[i] = __ldg(src + (warp + 8 * (8 * h + i)) * (D / 4));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = warp + 8 * (8 * h + i);
+                *reinterpret_cast<uint2*>(tS + tile_off(r, 4 * lane, D)) =
+                    make_uint2(pack2(a[i].x, a[i].y), pack2(a[i].z, a[i].w));
+            }
         }
     }
     fence_async_smem();
