@@ -527,19 +527,16 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
 #pragma unroll
         for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
         fence_async_smem();
-        if (!wait_all(&bars[2], ph, ws.status, 21, fail)) break;
-        // delta accumulator = -w S + INVb V (chunk rows on TMEM lanes, M = 64, N = 128): the w S part
-        // is issued first and runs while V may still be landing
+        // w, INVb and V (both prefetched) in one wait
+        if (!wait_all2(&bars[2], ph, 21, &bars[rel & 1], (rel >> 1) & 1, 24, ws.status, fail)) break;
+        const float e = reinterpret_cast<const float*>(tU + TCD)[k];  // e^Gamma_C of this thread's state row
+        // delta accumulator = -w S + INVb V (chunk rows on TMEM lanes, M = 64, N = 128)
         const uint32_t idd = idesc_bf16(64, 128, false, true);
         if (tid == 0) {
             tc_fence_after();
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks),
                          idesc_neg_a(idd), ks > 0);
-        }
-        if (!wait_all(&bars[rel & 1], (rel >> 1) & 1, ws.status, 24, fail)) break;
-        if (tid == 0) {
-            tc_fence_after();
             if (with_u)
                 for (int ks = 0; ks < kC / 16; ++ks)
                     mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
@@ -582,25 +579,24 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 bulk_commit();
             }
         }
+        if (tid == 0) bulk_wait_read();  // S_in and delta copies have read tS and the V / delta buffer
+        // after this wait every thread has read e^Gamma_C and the state MMA has read delta: the buffer is free
         if (!wait_all(&bars[4], mph, ws.status, 23, fail)) break;
         mph ^= 1;
-        if (tid == 0 && it + 1 < hi) issue_kh(it + 1);  // K^ is consumed
+        if (tid == 0) {
+            if (it + 1 < hi) issue_kh(it + 1);  // K^ is consumed
+            if (it + 2 < hi) issue_u(it + 2);
+        }
         tc_fence_after();
-        {
-            const float e = reinterpret_cast<const float*>(tU + TCD)[k];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float acc[32];
-                tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
-                tmem_ld_wait();
+        for (int h = 0; h < 2; ++h) {
+            float acc[32];
+            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+            tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
-            }
+            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
         }
         tc_fence_before();
-        if (tid == 0) bulk_wait_read();  // S_in and delta copies have read tS and the u buffer
-        __syncthreads();
-        if (tid == 0 && it + 2 < hi) issue_u(it + 2);
     }
     if (mode != 0 && *(volatile int*)fail == 0) {
         float* dst = (mode == 1 ? ws.seg_e : ws.seg_p) + seg_at;
@@ -615,49 +611,103 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
 
 // ---------------------------------------------------------------------------
 // tc_seg_combine: start states of the segments of one (sequence, value head),
-// 16 state columns per CTA, 128 threads (one state row each), fp32:
-// S_start(first) = init (h0 or dht, or zero), S_start(next) = P S_start + E
+// fp32: S_start(first) = init (h0 or dht, or zero), S_start(next) = P S_start + E
 // with P the segment's transition and E its end state from zero; forward
-// segments in ascending order, reverse segments in descending order.
+// segments in ascending order, reverse segments in descending order. One CTA
+// per 16 state columns, 256 threads: thread t owns state row k = t % 128 and
+// one half of the reduction index j. The transitions do not depend on the
+// chain, so each thread holds its 64 values of P's row k in registers and
+// loads the next segment's while it works on the current one; S_start's 16
+// columns go through shared memory. Each thread forms 16 partial sums over its
+// 64 j in order, and the two halves are added in a fixed order.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) k_tc_seg_combine(Prob p, SegArg sg, int reverse, const float* __restrict__ init,
-                                                        TcWs ws) {
-    __shared__ float sS[D][17];
-    const int k = threadIdx.x, hv = blockIdx.x, n = blockIdx.y, v0 = 16 * blockIdx.z, HV = p.HV;
+constexpr int kCombCols = 16;
+
+__global__ void __launch_bounds__(256, 1) k_tc_seg_combine(Prob p, SegArg sg, int reverse,
+                                                           const float* __restrict__ init, TcWs ws) {
+    __shared__ float Cs[D * kCombCols];  // S_start[j][v], this CTA's 16 columns
+    __shared__ float Hs[D * kCombCols];  // partial sums of the upper j half
+    const int tid = threadIdx.x;
+    const int k = tid & 127, jh = tid >> 7;  // this thread's row and its half of j
+    const int hv = blockIdx.x, n = blockIdx.y, v0 = kCombCols * blockIdx.z, HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
     const int nseg = (nts + sg.len - 1) / sg.len;
-    float cur[16];
+    float cur[16];  // S_start[k][v0 ..] (held by the lower half)
     {
-        const float* src = init ? init + (((int64_t)n * HV + hv) * D + k) * D + v0 : nullptr;
+        const float* src = (init && jh == 0) ? init + (((int64_t)n * HV + hv) * D + k) * D + v0 : nullptr;
 #pragma unroll
         for (int v = 0; v < 16; ++v) cur[v] = src ? src[v] : 0.f;
     }
     const int64_t head = ((int64_t)n * HV + hv) * sg.M;
+    auto seg_at = [&](int s) { return (head + (reverse ? nseg - 1 - s : s)) * D * D; };
+    auto load_p = [&](int s, float4 (&dst)[16]) {  // P[k][64 jh .. 64 jh + 63] of step s
+        const float4* src = reinterpret_cast<const float4*>(ws.seg_p + seg_at(s) + (int64_t)k * D + 64 * jh);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = __ldg(src + i);
+    };
+    float4 pc[16], pn[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pn[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (nseg > 1) load_p(0, pc);
     for (int s = 0; s < nseg; ++s) {
-        const int m = reverse ? nseg - 1 - s : s;
-        const int64_t at = (head + m) * D * D;
-        float* st = ws.seg_s0 + at + (int64_t)k * D + v0;
+        const int64_t at = seg_at(s);
+        if (jh == 0) {
+            float* st = ws.seg_s0 + at + (int64_t)k * D + v0;
 #pragma unroll
-        for (int v = 0; v < 16; ++v) st[v] = cur[v];
-        if (s + 1 == nseg) break;
-        __syncthreads();
-#pragma unroll
-        for (int v = 0; v < 16; ++v) sS[k][v] = cur[v];
-        __syncthreads();
-        const float* prow = ws.seg_p + at + (int64_t)k * D;
-        const float* erow = ws.seg_e + at + (int64_t)k * D + v0;
-#pragma unroll
-        for (int v = 0; v < 16; ++v) cur[v] = erow[v];
-        for (int j4 = 0; j4 < D; j4 += 4) {
-            const float4 pk = *reinterpret_cast<const float4*>(prow + j4);
-            const float pj[4] = {pk.x, pk.y, pk.z, pk.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t)
-#pragma unroll
-                for (int v = 0; v < 16; ++v) cur[v] = fmaf(pj[t], sS[j4 + t][v], cur[v]);
+            for (int v = 0; v < 16; v += 4)
+                *reinterpret_cast<float4*>(st + v) = make_float4(cur[v], cur[v + 1], cur[v + 2], cur[v + 3]);
         }
+        if (s + 1 == nseg) break;
+        if (s + 2 < nseg) load_p(s + 1, pn);
+        float acc[16];
+        if (jh == 0) {
+            const float* erow = ws.seg_e + at + (int64_t)k * D + v0;
+#pragma unroll
+            for (int v = 0; v < 16; v += 4) {
+                const float4 e4 = *reinterpret_cast<const float4*>(erow + v);
+                acc[v] = e4.x;
+                acc[v + 1] = e4.y;
+                acc[v + 2] = e4.z;
+                acc[v + 3] = e4.w;
+            }
+        } else {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) acc[v] = 0.f;
+        }
+        __syncthreads();  // the previous step's reads of Cs and Hs are done
+        if (jh == 0) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) Cs[k * kCombCols + v] = cur[v];
+        }
+        __syncthreads();
+        const float* crow = Cs + 64 * jh * kCombCols;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+            const float4 p4 = pc[j >> 2];
+            const float pkj = (j & 3) == 0 ? p4.x : (j & 3) == 1 ? p4.y : (j & 3) == 2 ? p4.z : p4.w;
+            const float4* cj = reinterpret_cast<const float4*>(crow + j * kCombCols);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4) {
+                const float4 c4 = cj[v4];
+                acc[4 * v4] = fmaf(pkj, c4.x, acc[4 * v4]);
+                acc[4 * v4 + 1] = fmaf(pkj, c4.y, acc[4 * v4 + 1]);
+                acc[4 * v4 + 2] = fmaf(pkj, c4.z, acc[4 * v4 + 2]);
+                acc[4 * v4 + 3] = fmaf(pkj, c4.w, acc[4 * v4 + 3]);
+            }
+        }
+        if (jh == 1) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) Hs[k * kCombCols + v] = acc[v];
+        }
+        __syncthreads();
+        if (jh == 0) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v) cur[v] = acc[v] + Hs[k * kCombCols + v];
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pc[i] = pn[i];
     }
 }
 
@@ -772,13 +822,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
                 bulk_commit();
             }
         }
+        if (tid == 0) bulk_wait_read();  // the dS_out copy has read tS
         if (!wait_all(&bars[2], mph, ws.status, 32, fail)) break;
         mph ^= 1;
-        if (tid == 0) {
-            if (it > lo) issue1(it - 1);  // the first group's operands are consumed
-            bulk_wait_read();             // the dS_out copy has read tS
-        }
-        __syncthreads();
+        if (tid == 0 && it > lo) issue1(it - 1);  // the first group's operands are consumed
         tc_fence_after();
         {  // dDelta rows into tS: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
             const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
@@ -809,6 +856,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
             }
         }
         const float e = reinterpret_cast<const float*>(sm + RevSm::EGC)[k];
+        if (tid == 0) bulk_wait_read();  // the dDelta copy has read tS
         if (!wait_all(&bars[2], mph, ws.status, 33, fail)) break;
         mph ^= 1;
         if (tid == 0 && it > lo) issue2(it - 1);  // w and e^Gamma_C are consumed
@@ -822,8 +870,6 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
             for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
         }
         tc_fence_before();
-        if (tid == 0) bulk_wait_read();  // the dDelta copy has read tS
-        __syncthreads();
     }
     if (*(volatile int*)fail == 0) {
         float* dst = mode == 1 ? ws.seg_e + seg_at
@@ -1033,18 +1079,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
 #pragma unroll
             for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
         }
-        if (!wait_all(&bars[0], ph, ws.status, 71, fail)) break;
-        // delta accumulator = -w S + INVb V (M = 64, N = 128): the w S part runs while group 2 may still land
+        if (!wait_all2(&bars[0], ph, 71, &bars[1], ph, 73, ws.status, fail)) break;
+        // delta accumulator = -w S + INVb V (M = 64, N = 128)
         const uint32_t idd = idesc_bf16(64, 128, false, true);
         if (tid == 0) {
             tc_fence_after();
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::W), kC, ks), desc_mnmajor(smem_u32(tS), D, ks),
                          idesc_neg_a(idd), ks > 0);
-        }
-        if (!wait_all(&bars[1], ph, ws.status, 73, fail)) break;
-        if (tid == 0) {
-            tc_fence_after();
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          idd, 1);
@@ -1145,6 +1187,8 @@ bool tc_path_ok(const Prob& p, bool bf16) { return bf16 && p.K == D && p.V == D;
 
 // Dense batches whose (sequence, value head) sweeps cannot fill the GPU and whose sequences are long
 // run the state passes in segments: about 256 CTAs per pass (two per SM), at least 32 chunks each.
+// (Shorter sequences gain nothing: a segment step of the chain costs about as much as the chunk
+// steps it saves.)
 SegPlan seg_plan(const Prob& p) {
     SegPlan sp{0, 1};
     const int64_t sweeps = (int64_t)p.B * p.HV;
@@ -1201,7 +1245,7 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
         const SegArg ends{sp.len, sp.M, kSegEnds};
         k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends, tm_v);
         note_launch("tc_state_fwd_seg", st);
-        k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
+        k_tc_seg_combine<<<dim3(p.HV, p.N, D / kCombCols), 256, 0, st>>>(p, ends, 0, io.h0, ws);
         note_launch("tc_seg_combine", st);
     }
     k_tc_fwd_out<<<dim3(p.HV, p.N, sp.M), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
@@ -1235,7 +1279,7 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         } else if (sp.len) {  // two-level: segment ends and transitions, their chain, then the checkpoints
             k_tc_state_fwd<<<dim3(p.HV, p.N, 2 * sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ends, tm_v);
             note_launch("tc_state_fwd_seg", st);
-            k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 0, io.h0, ws);
+            k_tc_seg_combine<<<dim3(p.HV, p.N, D / kCombCols), 256, 0, st>>>(p, ends, 0, io.h0, ws);
             note_launch("tc_seg_combine", st);
             k_tc_state_fwd<<<dim3(p.HV, p.N, sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ckpt, tm_v);
             note_launch("tc_state_fwd", st);
@@ -1248,7 +1292,7 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         if (sp.len) {
             k_tc_ds_rev<<<dim3(p.HV, p.N, 2 * sp.M), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, ends);
             note_launch("tc_ds_rev_seg", st);
-            k_tc_seg_combine<<<dim3(p.HV, p.N, D / 16), 128, 0, st>>>(p, ends, 1, io.dht, ws);
+            k_tc_seg_combine<<<dim3(p.HV, p.N, D / kCombCols), 256, 0, st>>>(p, ends, 1, io.dht, ws);
             note_launch("tc_seg_combine", st);
             k_tc_ds_rev<<<dim3(p.HV, p.N, sp.M), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, ckpt);
             note_launch("tc_ds_rev", st);

@@ -295,6 +295,14 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, int* st
     __syncthreads();
     return *(volatile int*)fail == 0;
 }
+// wait_all on two barriers at once: one poll by warp 0 of each, then one CTA barrier.
+__device__ __forceinline__ bool wait_all2(uint64_t* bar_a, uint32_t par_a, int code_a, uint64_t* bar_b, uint32_t par_b,
+                                          int code_b, int* status, int* fail) {
+    if (threadIdx.x < 32 && (!mbar_wait(bar_a, par_a, status, code_a) || !mbar_wait(bar_b, par_b, status, code_b)))
+        *(volatile int*)fail = 1;
+    __syncthreads();
+    return *(volatile int*)fail == 0;
+}
 // The same for the group of threads 0 .. N-1 (group_sync); *fail must be written
 // by no thread outside the group, so that every thread of the group reads the
 // same value after the barrier.
