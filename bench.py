@@ -29,8 +29,9 @@ inputs; see kda_inputs.py). Prints one JSON line.
 * ``--impl reference``: the fp64 oracle timed as the reference arm.
 * ``--pass``: ``bwd`` (default, the headline step above); ``fwd`` times one
   ``kda_chunk_fwd`` call (o and ht) per step; ``bwd-states`` times the
-  backward that consumes the chunk states a forward saved (the states are
-  produced once before the timed region).
+  backward that consumes the fp32 chunk states a forward saved; ``bwd-saved``
+  times ``kda_chunk_bwd_from_saved`` on the context ``kda_chunk_fwd_save``
+  kept (the states or context are produced once before the timed region).
 * ``--workload``: one of the four bf16 workloads of kda_inputs.py (default
   the B=8 T=4096 H=HV=32 benchmark); the others (B=1 T=2048 H=16 with h0 and
   dht; 16 packed sequences of U[1,4096] tokens with h0; B=1 T=65536 with 16
@@ -63,7 +64,8 @@ import kda_inputs  # noqa: E402
 WORKLOAD = "bf16_b8_t4096_h32_k128"
 METRIC = "KDA fwd-recompute+bwd tokens/s on 1 GB300 and % of roofline vs CPU oracle"
 METRICS = {"bwd": METRIC, "fwd": "KDA chunk forward (o, ht) tokens/s on 1 GB300",
-           "bwd-states": "KDA backward from saved chunk states tokens/s on 1 GB300"}
+           "bwd-states": "KDA backward from saved chunk states tokens/s on 1 GB300",
+           "bwd-saved": "KDA backward from the forward's saved context tokens/s on 1 GB300"}
 UNIT = "tokens/s"
 
 # ----------------------------------------------------------------------------
@@ -98,7 +100,7 @@ def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None, seq_states=0)
         b += B * HV * K * V * 4
         f = nck * (6 * C * C * K + 2 * C * C * V + C ** 3 // 3 + 6 * C * K * V + 2 * C * C * V)
         return dict(s, bytes=b, flops=f)
-    if mode == "bwd-states":  # the saved fp32 states are read once instead of written and read
+    if mode in ("bwd-states", "bwd-saved"):  # the saved chunk states are read once instead of written and read
         return dict(s, bytes=s["io_in"] + s["io_out"] + s["states"] // 2)
     return s
 
@@ -437,12 +439,27 @@ def gpu_arm(args):
         if rc != 0:
             raise kda.KdaError(rc, "kda_chunk_fwd")
         del fws, o_tmp
+    if mode == "bwd-saved":  # the forward's saved context, produced once outside the timed region; it is also
+        wsb = kda.saved_bytes(dims)  # the backward's workspace
+        ws = torch.empty(wsb, dtype=torch.uint8, device=device)
+        o_tmp = torch.empty_like(x["v"])
+        rc = lib.kda_chunk_fwd_save(ctypes.byref(dims), P(x["q"]), P(x["k"]), P(x["v"]), P(x["g"]), P(x["beta"]),
+                                    P(x.get("h0")), P(vl.cu), P(vl.idx), P(vl.off), P(o_tmp), None, P(ws), wsb, sptr)
+        if rc != 0:
+            raise kda.KdaError(rc, "kda_chunk_fwd_save")
+        del o_tmp
 
     def step(inputs, outs):
         if mode == "fwd":
             rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
                                    P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
                                    P(vl.off), P(outs["o"]), P(outs["ht"]), None, P(ws), wsb, sptr)
+        elif mode == "bwd-saved":
+            rc = lib.kda_chunk_bwd_from_saved(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
+                                              P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu),
+                                              P(vl.idx), P(vl.off), P(inputs["do"]), P(inputs.get("dht")), P(ws),
+                                              wsb, P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]),
+                                              P(outs["dbeta"]), P(outs.get("dh0")), sptr)
         else:
             rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
                                    P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
@@ -450,7 +467,8 @@ def gpu_arm(args):
                                    P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]),
                                    P(outs.get("dh0")), P(ws), wsb, sptr)
         if rc != 0:
-            raise kda.KdaError(rc, "kda_chunk_fwd" if mode == "fwd" else "kda_chunk_bwd")
+            raise kda.KdaError(rc, {"fwd": "kda_chunk_fwd", "bwd-saved": "kda_chunk_bwd_from_saved"}.get(
+                mode, "kda_chunk_bwd"))
 
     for _ in range(args.warmup):
         step(x, out)
@@ -594,7 +612,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="mode", default="bwd", choices=list(METRICS),
                     help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
-                         "bwd-states: backward from saved chunk states")
+                         "bwd-states: backward from the fp32 chunk states a forward saved; bwd-saved: backward "
+                         "from the context kda_chunk_fwd_save kept (reverse pass and gradients only)")
     ap.add_argument("--workload", default=WORKLOAD, choices=kda_inputs.WORKLOAD_ORDER,
                     help="the workload of the JSON line (default: the B=8 T=4096 H=HV=32 benchmark)")
     ap.add_argument("--seq-len", type=int, default=None,

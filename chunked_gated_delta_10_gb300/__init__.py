@@ -19,8 +19,9 @@ import torch
 
 from .build import LIB, build  # noqa: F401
 
-__all__ = ["build", "load", "Dims", "prepare_chunks", "workspace_bytes", "chunk_fwd", "chunk_bwd", "KdaError",
-           "STATUS", "DTYPE_BF16", "DTYPE_F32", "PASS_FWD", "PASS_BWD"]
+__all__ = ["build", "load", "Dims", "prepare_chunks", "workspace_bytes", "saved_bytes", "chunk_fwd", "chunk_bwd",
+           "chunk_fwd_save", "chunk_bwd_from_saved", "KdaError", "STATUS", "DTYPE_BF16", "DTYPE_F32", "PASS_FWD",
+           "PASS_BWD"]
 
 DTYPE_BF16, DTYPE_F32 = 0, 1
 PASS_FWD, PASS_BWD = 0, 1
@@ -68,6 +69,13 @@ def load():
             lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(Dims)] + [_P] * 13 + [ctypes.c_size_t, _P]
             lib.kda_chunk_bwd.restype = ctypes.c_int
             lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(Dims)] + [_P] * 19 + [ctypes.c_size_t, _P]
+            lib.kda_saved_bytes.restype = ctypes.c_size_t
+            lib.kda_saved_bytes.argtypes = [ctypes.POINTER(Dims)]
+            lib.kda_chunk_fwd_save.restype = ctypes.c_int
+            lib.kda_chunk_fwd_save.argtypes = [ctypes.POINTER(Dims)] + [_P] * 12 + [ctypes.c_size_t, _P]
+            lib.kda_chunk_bwd_from_saved.restype = ctypes.c_int
+            lib.kda_chunk_bwd_from_saved.argtypes = ([ctypes.POINTER(Dims)] + [_P] * 12 + [ctypes.c_size_t] +
+                                                     [_P] * 6 + [_P])
             lib.kda_device_status.restype = ctypes.c_int
             lib.kda_device_status.argtypes = [_P, _P]
             lib.kda_set_profile_events.restype = ctypes.c_int
@@ -215,6 +223,59 @@ def chunk_bwd(q, k, v, g, beta, do, scale=None, h0=None, dht=None, cu_seqlens=No
                              _ptr(vl.cu), _ptr(vl.idx), _ptr(vl.off), _ptr(do), _ptr(dht), _ptr(states),
                              _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
                              _ptr(out.get("dh0")), _ptr(ws), ws.numel(), _stream()), "kda_chunk_bwd")
+    return out
+
+
+def saved_bytes(dims: Dims) -> int:
+    return int(load().kda_saved_bytes(ctypes.byref(dims)))
+
+
+def chunk_fwd_save(q, k, v, g, beta, scale=None, h0=None, cu_seqlens=None):
+    """Forward that also keeps the saved context for chunk_bwd_from_saved (bf16, K = V = 128).
+    Returns (o, ht, saved); saved is a uint8 device tensor of saved_bytes(dims)."""
+    lib = load()
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta")):
+        _req(t, n, dt)
+    _req(g, "g", torch.float32)
+    _opt(h0, "h0", torch.float32)
+    dims = make_dims(q, v, scale, cu_seqlens)
+    dev = q.device
+    vl = _Varlen(cu_seqlens, dev)
+    need = saved_bytes(dims)
+    if need == 0:
+        raise KdaError(2, "kda_saved_bytes")
+    saved = torch.empty(need, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(v)
+    ht = torch.empty(dims.num_seqs, dims.HV, dims.K, dims.V, dtype=torch.float32, device=dev)
+    _check(lib.kda_chunk_fwd_save(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                  _ptr(vl.cu), _ptr(vl.idx), _ptr(vl.off), _ptr(o), _ptr(ht), _ptr(saved),
+                                  saved.numel(), _stream()), "kda_chunk_fwd_save")
+    return o, ht, saved
+
+
+def chunk_bwd_from_saved(q, k, v, g, beta, do, saved, scale=None, h0=None, dht=None, cu_seqlens=None, out=None):
+    """Backward from chunk_fwd_save's context: only the reverse pass and the per-chunk gradients run.
+    Same returns as chunk_bwd, and the same values bit for bit."""
+    lib = load()
+    dt = q.dtype
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (do, "do")):
+        _req(t, n, dt)
+    _req(g, "g", torch.float32)
+    _opt(h0, "h0", torch.float32)
+    _opt(dht, "dht", torch.float32)
+    _req(saved, "saved", torch.uint8)
+    dims = make_dims(q, v, scale, cu_seqlens)
+    vl = _Varlen(cu_seqlens, q.device)
+    if out is None:
+        out = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                   dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
+                   dh0=torch.empty_like(h0) if h0 is not None else None)
+    _check(lib.kda_chunk_bwd_from_saved(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                        _ptr(vl.cu), _ptr(vl.idx), _ptr(vl.off), _ptr(do), _ptr(dht), _ptr(saved),
+                                        saved.numel(), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                                        _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out.get("dh0")), _stream()),
+           "kda_chunk_bwd_from_saved")
     return out
 
 

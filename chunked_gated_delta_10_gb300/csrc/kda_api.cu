@@ -342,6 +342,66 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
     return KDA_OK;
 }
 
+extern "C" size_t kda_saved_bytes(const kda_dims* dims) {
+    Prob p;
+    if (check_dims(dims, &p) != KDA_OK || !use_tc(dims, KDA_PASS_BWD)) return 0;
+    return layout(p, KDA_PASS_BWD, true).total;
+}
+
+extern "C" kda_status kda_chunk_fwd_save(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                         const float* g, const void* beta, const float* h0,
+                                         const int64_t* cu_seqlens, const int32_t* chunk_idx, const int64_t* chunk_off,
+                                         void* o, float* ht, void* saved, size_t saved_bytes, kda_stream_t stream) {
+    Prob p;
+    kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, saved, saved_bytes,
+                                KDA_PASS_BWD);
+    if (s != KDA_OK) return s;
+    if (!use_tc(dims, KDA_PASS_BWD)) return KDA_ERR_UNSUPPORTED;
+    if ((size_t)dims->B * dims->T > 0 && !o) return KDA_ERR_INVALID_ARG;
+    for (const void* x : {(const void*)o, (const void*)ht})
+        if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
+    const Layout L = layout(p, KDA_PASS_BWD, true);
+    cudaStream_t st = (cudaStream_t)stream;
+    IO io;
+    memset(&io, 0, sizeof(io));
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.g = g; io.h0 = h0;
+    io.o = o; io.ht = ht;
+    cudaError_t e = cudaMemsetAsync((char*)saved + L.status, 0, kAlign, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    begin_launches(st);
+    e = tc_fwd(p, io, carve_tc(saved, L), st);  // the backward layout: the state pass also keeps S_in and delta
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
+extern "C" kda_status kda_chunk_bwd_from_saved(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                               const float* g, const void* beta, const float* h0,
+                                               const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                                               const int64_t* chunk_off, const void* d_o, const float* dht,
+                                               void* saved, size_t saved_bytes, void* dq, void* dk, void* dv, float* dg,
+                                               void* dbeta, float* dh0, kda_stream_t stream) {
+    Prob p;
+    kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, saved, saved_bytes,
+                                KDA_PASS_BWD);
+    if (s != KDA_OK) return s;
+    if (!use_tc(dims, KDA_PASS_BWD)) return KDA_ERR_UNSUPPORTED;
+    if (dh0 && !h0) return KDA_ERR_INVALID_ARG;
+    if ((size_t)dims->B * dims->T > 0 && (!d_o || !dq || !dk || !dv || !dg || !dbeta)) return KDA_ERR_INVALID_ARG;
+    for (const void* x : {(const void*)d_o, (const void*)dht, (const void*)dq, (const void*)dk, (const void*)dv,
+                          (const void*)dg, (const void*)dbeta, (const void*)dh0})
+        if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
+    const Layout L = layout(p, KDA_PASS_BWD, true);
+    cudaStream_t st = (cudaStream_t)stream;
+    IO io;
+    memset(&io, 0, sizeof(io));
+    io.q = q; io.k = k; io.v = v; io.beta = beta; io.d_o = d_o; io.g = g; io.h0 = h0; io.dht = dht;
+    io.dq = dq; io.dk = dk; io.dv = dv; io.dbeta = dbeta; io.dg = dg; io.dh0 = dh0;
+    cudaError_t e = cudaMemsetAsync((char*)saved + L.status, 0, kAlign, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    begin_launches(st);
+    e = tc_bwd(p, io, carve_tc(saved, L), st, 4, true);
+    return e == cudaSuccess ? KDA_OK : cuda_fail(e);
+}
+
 extern "C" kda_status kda_debug_bwd_stages(const kda_dims* dims, const void* q, const void* k, const void* v,
                                            const float* g, const void* beta, const float* h0,
                                            const int64_t* cu_seqlens, const int32_t* chunk_idx,

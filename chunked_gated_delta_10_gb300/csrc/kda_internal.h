@@ -69,8 +69,10 @@ bool tc_path_ok(const Prob& p, bool bf16);
 cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 // Runs the first `stages` stages of the tensor-core backward (1: intra,
 // 2: + state pass, or the load of io.states_in, 3: + reverse pass,
-// 4: + gradients).
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages);
+// 4: + gradients). With from_saved, the workspace holds a saved context (the
+// forward's intra tiles, S_in and delta, written by tc_fwd into a backward-
+// layout workspace) and stages 1 and 2 are skipped.
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved = false);
 // The per-chunk gradient stage (and the grouped-value-head reduction).
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 

@@ -997,7 +997,9 @@ cleanup:
 // are single-buffered in two groups: w and INVb are refetched once the delta
 // MMA has consumed them, the rest once the state and output MMAs have. Two
 // CTAs per SM: 112.6 KB of shared memory each, from a 1024-byte aligned base
-// (no alignment slack).
+// (no alignment slack). With a saved-context workspace (ws.sin, ws.vn set) it
+// also stores every chunk's bf16 S_in and delta tiles, the ones the backward's
+// state pass would recompute.
 // ---------------------------------------------------------------------------
 struct FoSm {
     static constexpr int W = 0, IVB = TCD, KH = TCD + TCC, QS = 2 * TCD + TCC, U = 3 * TCD + TCC;
@@ -1062,6 +1064,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
     const bool run = *(volatile int*)fail == 0;
+    const bool save = ws.sin != nullptr && ws.vn != nullptr;
     if (tid == 0 && lo < hi && run) {
         issue_w(lo);
         issue_g2(lo);
@@ -1091,6 +1094,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          idd, 1);
             mma_commit(&bars[2]);
+            if (save) {
+                bulk_store(ws.sin + ch * TDD, tS, TDD);
+                bulk_commit();
+            }
         }
         if (!wait_all(&bars[2], mph, ws.status, 72, fail)) break;
         mph ^= 1;
@@ -1128,6 +1135,11 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::AQK), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks), io,
                          1);
             mma_commit(&bars[2]);
+            if (save) {
+                bulk_store(ws.vn + ch * TCD, tU, TCD);
+                bulk_commit();
+                bulk_wait_read();  // the S_in and delta copies have read tS and tU (both rewritten next)
+            }
         }
         const float e = reinterpret_cast<const float*>(sm + FoSm::EGC)[k];
         if (!wait_all(&bars[2], mph, ws.status, 74, fail)) break;
@@ -1146,14 +1158,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
             const int64_t r0 = bos + (int64_t)it * kC;
             const int c = (int)((eos - r0) < kC ? (eos - r0) : kC);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float x[32];
-                tmem_ld32(tmem + lq + cb + 32 * h, x);
+            for (int h = 0; h < 4; ++h) {  // 16 columns at a time (the 64 state values stay in registers)
+                float x[16];
+                tmem_ld16(tmem + lq + cb + 16 * h, x);
                 tmem_ld_wait();
                 if (lane < 16 && r < c) {
-                    bf16* dst = o + ((r0 + r) * HV + hv) * D + cb + 32 * h;
+                    bf16* dst = o + ((r0 + r) * HV + hv) * D + cb + 16 * h;
 #pragma unroll
-                    for (int u = 0; u < 32; u += 8) {
+                    for (int u = 0; u < 16; u += 8) {
                         uint4 vv;
                         vv.x = pack2(x[u], x[u + 1]);
                         vv.y = pack2(x[u + 2], x[u + 3]);
@@ -1171,6 +1183,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
 #pragma unroll
         for (int j = 0; j < 64; ++j) dst[j] = S[j];
     }
+    if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
@@ -1254,7 +1267,7 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages) {
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved) {
     cudaError_t e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
@@ -1267,10 +1280,10 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
         return cudaErrorInvalidValue;
     CUtensorMap tm_v;
     if (!make_tmap_v(&tm_v, p, io.v)) return cudaErrorInvalidValue;
-    if (stages >= 1 && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
+    if (stages >= 1 && !from_saved && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     const SegPlan sp = seg_plan(p);
     const SegArg ends{sp.len, sp.M, kSegEnds}, ckpt{sp.len, sp.M, kSegCkpt}, whole{0, 1, kSegNone};
-    if (stages >= 2) {
+    if (stages >= 2 && !from_saved) {
         if (io.states_in) {  // the forward's saved states: no sequential recompute
             if (p.NT > 0) {
                 k_tc_state_load<<<dim3((unsigned)p.NT, p.HV), 256, kLoadSmem, st>>>(p, io.states_in, ws, tm_v);

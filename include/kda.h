@@ -144,6 +144,45 @@ kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, con
                          size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Backward from a saved forward context (bf16 inputs with K = V = 128 only).
+ *
+ * The backward needs, per chunk, the WY factors (w, INV, INV diag(beta)), the
+ * decayed key/query factors, the in-chunk triangle Aqk, e^Gamma_C, the state
+ * entering the chunk and delta = u - w S_in: the quantities FLA's chunk_kda_bwd
+ * takes from the forward instead of recomputing them when recomputation is
+ * disabled (the "FLA chunk_bwd.py" page: w, u, qg, kg, v_new and h of its
+ * disable_recompute branch). kda_chunk_fwd_save runs the forward and keeps all
+ * of them, as bf16 tiles in the layout the backward's MMAs read, in `saved`;
+ * kda_chunk_bwd_from_saved then runs only the reverse state-gradient pass and
+ * the per-chunk gradients (no intra-chunk pass, no forward state pass). Its
+ * results equal kda_chunk_bwd's bit for bit on the same inputs.
+ *
+ * kda_saved_bytes: bytes of the saved context for these dims (equal to
+ *   kda_workspace_bytes(dims, KDA_PASS_BWD)); 0 if the dims are invalid or not
+ *   on this path (not bf16 with K = V = 128).
+ * kda_chunk_fwd_save: as kda_chunk_fwd (o, ht; no fp32 states) and writes the
+ *   context into `saved` (device, 16-byte aligned, at least kda_saved_bytes).
+ * kda_chunk_bwd_from_saved: as kda_chunk_bwd with `saved` (from
+ *   kda_chunk_fwd_save on the same inputs and dims) as both the saved context
+ *   and the workspace. It reads the context and overwrites only the backward's
+ *   own scratch regions of the buffer, so it may be called again with the same
+ *   buffer. Calls that overlap on the GPU with the same buffer race.
+ * Errors: those of kda_chunk_fwd / kda_chunk_bwd; KDA_ERR_UNSUPPORTED off this
+ * path; KDA_ERR_WORKSPACE when `saved` is null, misaligned or too small.
+ * kda_device_status(saved, stream) reports bounded device waits of either call.
+ */
+size_t kda_saved_bytes(const kda_dims* dims);
+kda_status kda_chunk_fwd_save(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                              const void* beta, const float* h0, const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                              const int64_t* chunk_off, void* o, float* ht, void* saved, size_t saved_bytes,
+                              kda_stream_t stream);
+kda_status kda_chunk_bwd_from_saved(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                                    const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                    const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
+                                    const float* dht, void* saved, size_t saved_bytes, void* dq, void* dk, void* dv,
+                                    float* dg, void* dbeta, float* dh0, kda_stream_t stream);
+
+/*
  * Status word that device-side bounded waits write into the workspace of the
  * last call (KDA_OK when none gave up). Synchronises `stream`, then reads it.
  * ws: the workspace passed to that call.

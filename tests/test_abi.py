@@ -102,3 +102,23 @@ def test_binding_requires_built_library(monkeypatch, tmp_path):
     monkeypatch.setattr(m, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         m.load()
+
+
+def test_saved_context_size_and_argument_checks(lib):
+    """kda_saved_bytes is the backward workspace size on the tensor-core path and 0 off it; the saved-context
+    entry points reject a small buffer and unsupported dims before any CUDA call."""
+    tc = kda.Dims(2, 130, 2, 4, 128, 128, 64, 2, 6, kda.DTYPE_BF16, 0.1)
+    need = kda.saved_bytes(tc)
+    assert need == kda.workspace_bytes(tc, kda.PASS_BWD) > 0
+    for dims in (_dims(), _dims(dtype=1, K=128, V=128)):  # K = 64 bf16, fp32
+        assert kda.saved_bytes(dims) == 0
+    P = ctypes.c_void_p
+    a = P(A)
+    fwd_args = [a] * 5 + [None] * 4 + [a, None]
+    assert lib.kda_chunk_fwd_save(ctypes.byref(tc), *fwd_args, a, need - 1, None) == 3  # KDA_ERR_WORKSPACE
+    bwd_args = [a] * 5 + [None] * 4 + [a, None]
+    outs = [a] * 5 + [None]
+    assert lib.kda_chunk_bwd_from_saved(ctypes.byref(tc), *bwd_args, a, need - 1, *outs, None) == 3
+    f32 = _dims(dtype=1, K=128, V=128)
+    assert lib.kda_chunk_fwd_save(ctypes.byref(f32), *fwd_args, a, 1 << 40, None) == 2  # KDA_ERR_UNSUPPORTED
+    assert lib.kda_chunk_bwd_from_saved(ctypes.byref(f32), *bwd_args, a, 1 << 40, *outs, None) == 2

@@ -164,6 +164,64 @@ def test_backward_from_saved_states_is_bitwise_recompute(kda, name):
     compare_full(inp, sv, oracle.run_inputs(inp))
 
 
+def _launches(kda):
+    lib = kda.load()
+    return [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+
+
+def _bwd_from_saved(kda, inp, x, saved):
+    out = kda.chunk_bwd_from_saved(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], saved, scale=inp.scale,
+                                   h0=x["h0"], dht=x["dht"], cu_seqlens=inp.cu_seqlens)
+    torch.cuda.synchronize()
+    return out
+
+
+def _check_saved_context(kda, inp, oracle_parity=True):
+    """chunk_fwd_save gives the forward's o and ht bit for bit; chunk_bwd_from_saved runs only the reverse
+    pass and the gradient kernel and gives the recompute path's gradients bit for bit, twice in a row on
+    the same saved buffer; and the oracle agrees."""
+    x = _cuda(inp)
+    o_ref, ht_ref, _ = gpu_fwd(kda, inp)
+    o, ht, saved = kda.chunk_fwd_save(x["q"], x["k"], x["v"], x["g"], x["beta"], scale=inp.scale, h0=x["h0"],
+                                      cu_seqlens=inp.cu_seqlens)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(ht, ht_ref)
+    rec = gpu_bwd(kda, inp)
+    for rep in range(2):
+        sv = _bwd_from_saved(kda, inp, x, saved)
+        names = _launches(kda)
+        assert b"tc_grads" in names and b"tc_intra" not in names and b"tc_state_fwd" not in names, names
+        for key in GRADS:
+            if rec[key] is not None:
+                assert torch.equal(rec[key], sv[key]), (rep, key)
+    assert kda.device_status(saved) == 0
+    if oracle_parity:
+        return compare_full(inp, sv, oracle.run_inputs(inp))
+
+
+SAVED = {
+    "varlen_gva": FWD_TC["varlen_gva"],
+    "no_state": FWD_TC["no_state"],
+    "t64": SMALL["t64"],
+}
+
+
+@pytest.mark.parametrize("name", list(SAVED))
+def test_backward_from_saved_context_is_bitwise_recompute(kda, name):
+    _check_saved_context(kda, kda_inputs.small(seed=44, dtype="bf16", **SAVED[name]))
+
+
+def test_backward_from_saved_context_segmented(kda):
+    """A long sequence with few sweeps: the forward runs segmented and keeps every chunk's S_in and delta;
+    the backward's reverse pass runs segmented from the saved context."""
+    inp = kda_inputs.small(seed=45, B=1, T=8192 + 37, H=1, HV=2, K=128, V=128, dtype="bf16")
+    print("saved segmented", _check_saved_context(kda, inp))
+
+
+def test_backward_from_saved_context_benchmark_workload(kda):
+    _check_saved_context(kda, _workload("bf16_b8_t4096_h32_k128"), oracle_parity=False)
+
+
 def test_saved_states_off_tensor_core_path_is_unsupported(kda):
     inp = kda_inputs.small(seed=37, dtype="f32", **SMALL["t65"])
     _, _, st = gpu_fwd(kda, inp)
