@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             __syncthreads();
             const float ref0 = tmp[512 + d0], ref1 = tmp[512 + d0 + 1], gC0 = tmp[640 + d0], gC1 = tmp[640 + d0 + 1];
             if (qt == 0) *reinterpret_cast<float2*>(ws.egc + ch * D + d0) = make_float2(exp2f(gC0), exp2f(gC1));
+            // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G = ep 2^ref and K^'s
+            // factor 2^(G_C-G) = em 2^(G_C-ref) follow from them (the formulas of the gradient kernel)
+            const float er0 = exp2f(ref0), er1 = exp2f(ref1), ec0 = exp2f(gC0 - ref0), ec1 = exp2f(gC1 - ref1);
             if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
             // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^
 #pragma unroll
@@ -279,10 +282,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 const float k0 = __uint_as_float(k2 << 16), k1 = __uint_as_float(k2 & 0xffff0000u);
                 const float q0 = __uint_as_float(q2 << 16), q1 = __uint_as_float(q2 & 0xffff0000u);
                 const float gm0 = G2[x], gm1 = G2[16 + x];
-                const float ep0 = fast_exp2(gm0 - ref0), em0 = fast_exp2(ref0 - gm0), E0 = fast_exp2(gm0),
-                            eh0 = fast_exp2(gC0 - gm0);
-                const float ep1 = fast_exp2(gm1 - ref1), em1 = fast_exp2(ref1 - gm1), E1 = fast_exp2(gm1),
-                            eh1 = fast_exp2(gC1 - gm1);
+                const float ep0 = fast_exp2(gm0 - ref0), em0 = fast_exp2(ref0 - gm0), E0 = ep0 * er0, eh0 = em0 * ec0;
+                const float ep1 = fast_exp2(gm1 - ref1), em1 = fast_exp2(ref1 - gm1), E1 = ep1 * er1, eh1 = em1 * ec1;
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(k0 * ep0, k1 * ep1);
                 *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(q0 * ep0, q1 * ep1);
                 {  // Kc as a bf16 pair and the bf16 pair of its rounding remainder
