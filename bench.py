@@ -65,7 +65,8 @@ WORKLOAD = "bf16_b8_t4096_h32_k128"
 METRIC = "KDA fwd-recompute+bwd tokens/s on 1 GB300 and % of roofline vs CPU oracle"
 METRICS = {"bwd": METRIC, "fwd": "KDA chunk forward (o, ht) tokens/s on 1 GB300",
            "bwd-states": "KDA backward from saved chunk states tokens/s on 1 GB300",
-           "bwd-saved": "KDA backward from the forward's saved context tokens/s on 1 GB300"}
+           "bwd-saved": "KDA backward from the forward's saved context tokens/s on 1 GB300",
+           "fwd-save": "KDA chunk forward (o, ht) keeping the backward's saved context tokens/s on 1 GB300"}
 UNIT = "tokens/s"
 
 # ----------------------------------------------------------------------------
@@ -95,9 +96,11 @@ def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None, seq_states=0)
     """Algorithmic bytes / FLOPs of one step of ``mode`` (see step_cost for the backward)."""
     s = step_cost(B, T, H, HV, K, V, in_bytes, C, nck, seq_states)
     th, tk, nck = B * T * HV, B * T * H, s["nck"]
-    if mode == "fwd":  # q, k, v, g, beta in; o and ht out; the chunk state stays on chip or in bf16 scratch
+    if mode in ("fwd", "fwd-save"):  # q, k, v, g, beta in; o and ht out (fwd-save: plus the chunk state written once)
         b = tk * K * in_bytes * 2 + th * V * in_bytes + th * K * 4 + th * in_bytes + th * V * in_bytes
         b += B * HV * K * V * 4
+        if mode == "fwd-save":
+            b += s["states"] // 2
         f = nck * (6 * C * C * K + 2 * C * C * V + C ** 3 // 3 + 6 * C * K * V + 2 * C * C * V)
         return dict(s, bytes=b, flops=f)
     if mode in ("bwd-states", "bwd-saved"):  # the saved chunk states are read once instead of written and read
@@ -156,9 +159,9 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 # source file is unchanged since that capture (sha1 prefix).
 MEASURED_TRAFFIC = {
     "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "1ef0f2ff3a78",
-                 "bytes_per_chunk_head": (841.619968e6 + 300.612096e6) / 4096},
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "16f27449290f",
-                 "bytes_per_chunk_head": (336.209152e6 + 283.242752e6) / 4096},
+                 "bytes_per_chunk_head": (841.772288e6 + 302.805504e6) / 4096},
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "82213fbf7aa5",
+                 "bytes_per_chunk_head": (269.135104e6 + 250.194944e6) / 4096},
 }
 
 
@@ -404,10 +407,11 @@ def gpu_arm(args):
     N = inp.num_seqs
     tokens = B * T
     mode = args.mode
+    fwd_like = mode in ("fwd", "fwd-save")
     host = dict(q=inp.q, k=inp.k, v=inp.v, g=inp.g, beta=inp.beta)
     if inp.h0 is not None:
         host["h0"] = inp.h0
-    if mode != "fwd":
+    if not fwd_like:
         host["do"] = inp.do
         if inp.dht is not None:
             host["dht"] = inp.dht
@@ -415,9 +419,10 @@ def gpu_arm(args):
     vl = kda._Varlen(inp.cu_seqlens, device)
     dims = kda.make_dims(x["q"], x["v"], inp.scale, inp.cu_seqlens)
     nck = int(dims.num_chunks) * HV
-    wsb = kda.workspace_bytes(dims, kda.PASS_FWD if mode == "fwd" else kda.PASS_BWD)
+    wsb = (kda.workspace_bytes(dims, kda.PASS_FWD) if mode == "fwd" else
+           kda.saved_bytes(dims) if mode == "fwd-save" else kda.workspace_bytes(dims, kda.PASS_BWD))
     ws = torch.empty(wsb, dtype=torch.uint8, device=device)
-    if mode == "fwd":
+    if fwd_like:
         out = dict(o=torch.empty_like(x["v"]), ht=torch.empty(N, HV, K, V, dtype=torch.float32, device=device))
     else:
         out = dict(dq=torch.empty_like(x["q"]), dk=torch.empty_like(x["k"]), dv=torch.empty_like(x["v"]),
@@ -454,6 +459,10 @@ def gpu_arm(args):
             rc = lib.kda_chunk_fwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
                                    P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
                                    P(vl.off), P(outs["o"]), P(outs["ht"]), None, P(ws), wsb, sptr)
+        elif mode == "fwd-save":
+            rc = lib.kda_chunk_fwd_save(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
+                                        P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
+                                        P(vl.off), P(outs["o"]), P(outs["ht"]), P(ws), wsb, sptr)
         elif mode == "bwd-saved":
             rc = lib.kda_chunk_bwd_from_saved(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
                                               P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu),
@@ -467,8 +476,8 @@ def gpu_arm(args):
                                    P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]),
                                    P(outs.get("dh0")), P(ws), wsb, sptr)
         if rc != 0:
-            raise kda.KdaError(rc, {"fwd": "kda_chunk_fwd", "bwd-saved": "kda_chunk_bwd_from_saved"}.get(
-                mode, "kda_chunk_bwd"))
+            raise kda.KdaError(rc, {"fwd": "kda_chunk_fwd", "fwd-save": "kda_chunk_fwd_save",
+                                    "bwd-saved": "kda_chunk_bwd_from_saved"}.get(mode, "kda_chunk_bwd"))
 
     for _ in range(args.warmup):
         step(x, out)
@@ -526,7 +535,7 @@ def gpu_arm(args):
                 "traffic": traffic, "peak_source": peak_src if bound != "alu" else "152 SMs x 128 FFMA lanes x SM clock",
                 "avg_launch_ms": avg * 1e3, "share": tot[dom] / sum(tot.values()),
                 "kernels_ms": {n: 1e3 * tot[n] / len(per[n]) for n in names}}
-    seq_states = N * HV * K * V * ((1 if "h0" in x else 0) + (0 if mode == "fwd" else
+    seq_states = N * HV * K * V * ((1 if "h0" in x else 0) + (0 if fwd_like else
                                                              (1 if "dht" in x else 0) + (1 if "h0" in x else 0)))
     sc = pass_cost(mode, B, T, H, HV, K, V, in_bytes=ib, nck=nck, seq_states=seq_states)
     step_s = elapsed / args.steps
@@ -613,7 +622,8 @@ def main():
     ap.add_argument("--pass", dest="mode", default="bwd", choices=list(METRICS),
                     help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
                          "bwd-states: backward from the fp32 chunk states a forward saved; bwd-saved: backward "
-                         "from the context kda_chunk_fwd_save kept (reverse pass and gradients only)")
+                         "from the context kda_chunk_fwd_save kept (reverse pass and gradients only); fwd-save: "
+                         "the forward that keeps that context")
     ap.add_argument("--workload", default=WORKLOAD, choices=kda_inputs.WORKLOAD_ORDER,
                     help="the workload of the JSON line (default: the B=8 T=4096 H=HV=32 benchmark)")
     ap.add_argument("--seq-len", type=int, default=None,
