@@ -129,7 +129,7 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
         b = s["io_out"] + tk * K * in_bytes * 2 + th * (2 * V * in_bytes + in_bytes)
         f = nck * (6 * C * C * V + 10 * C * C * K + 4 * C ** 3)
         return "alu", b, f
-    if name in ("gva_reduce", "tc_gva_reduce"):
+    if name == "gva_reduce":
         return "hbm", th * K * 4 * 2 + tk * K * in_bytes * 2, 0
     # Tensor-core path (bf16 K = V = 128): per chunk-head I/O of each kernel at
     # its dtypes (bf16 tiles CxK = 16 KB, CxC = 8 KB, KxV = 32 KB), read once

@@ -90,9 +90,10 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_sin = take(CH * TDD);
         L.t_dvn = take(CH * TCD);
         L.t_dso = take(CH * TDD);
-        if (p.HV != p.H) {
-            L.dqp = take(R * HV * K * f);
-            L.dkp = take(R * HV * K * f);
+        if (p.HV != p.H) {  // the gradient kernel's running dq / dk group sums, 64 x 128 fp32 per CTA
+            const size_t groups = NT * p.H, ctas = groups < (size_t)kGradsMaxCtas ? groups : kGradsMaxCtas;
+            L.dqp = take(ctas * kC * 128 * f);
+            L.dkp = take(ctas * kC * 128 * f);
         }
         L.total = off;
         return L;

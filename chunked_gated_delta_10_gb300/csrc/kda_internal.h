@@ -44,7 +44,9 @@ cudaError_t simt_bwd(const Prob& p, bool bf16, const IO& io, const Ws& ws, cudaS
 //   w, kh (K^), qs (scale Q~), vn (delta), dvn (d_delta): 64 x 128 (16 KB)
 //   aqk, inv, invb (INV diag(beta)): 64 x 64 (8 KB);  sin, dso: 128 x 128 (32 KB)
 //   egc: 128 fp32 (e^Gamma_C per key channel)
-// dqp, dkp: fp32 [R, HV, K] per-value-head dq/dk before the group sum.
+// dqp, dkp (grouped value heads only): per gradient-kernel CTA, the running fp32 dq / dk sum of a
+// (chunk, key head) group over its value heads, 64 x 128 values in the CTA's thread order.
+constexpr int kGradsMaxCtas = 256;
 struct TcWs {
     uint8_t *w, *invb, *kh, *qs, *vn, *dvn, *aqk, *inv, *sin, *dso;
     float *egc, *dqp, *dkp;
@@ -73,7 +75,7 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
 // forward's intra tiles, S_in and delta, written by tc_fwd into a backward-
 // layout workspace) and stages 1 and 2 are skipped.
 cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved = false);
-// The per-chunk gradient stage (and the grouped-value-head reduction).
+// The per-chunk gradient stage (dq, dk summed over the value heads of a group in the same kernel).
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 
 }  // namespace kda

@@ -1,5 +1,5 @@
 // Tensor-core per-chunk gradient kernel of the chunked KDA backward (bf16,
-// K = V = 128, chunks of 64), and the grouped-value-head reduction.
+// K = V = 128, chunks of 64), with the grouped-value-head sum of dq and dk.
 //
 // Persistent: one CTA per SM (512 SIMT threads and a producer warp) walks
 // (chunk, value head) items and prefetches the next item's inputs. Inputs: q, k, v, dO, g (TMA),
@@ -57,6 +57,8 @@ struct GS {
     static constexpr int INV = DW + TCD, DN = INV + TCC, DM = DN + TCC, TT = DM + 2 * TCC;  // DM .. TT: g tile part
     // the g tile (64 x 128 fp32) of a chunk lands on DN .. TT, which the previous chunk no longer needs after phase E
     static constexpr int GT = DN;
+    // dN = dN_hi + dN_lo as a bf16 pair (phases B and E take both); dM takes the first 8 KB of its region
+    static constexpr int DNL = DM + TCC;
     static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048;
     static constexpr int END = BARS + 128;
     // scratch in the dw tile while that tile is dead: cumsum quarter totals and the reference / last-row gates
@@ -69,8 +71,8 @@ struct GradMaps {
     CUtensorMap q, k, v, d_o, g;
 };
 
-// One work item = one (chunk, value head), index w = chunk * HV + hv; items are dealt to the
-// persistent CTAs round-robin.
+// One work item = one (chunk, value head), index w = chunk * HV + hv (the kernel says how items are dealt
+// to its persistent CTAs).
 struct Item {
     int64_t r0, ch;
     int hv, h, c, valid;
@@ -102,6 +104,8 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
 // epilogue has read them.
 constexpr int kSimt = 512, kProducerWarp = kSimt / 32, kGradsThreads = kSimt + 32;
 
+// GROUPED: HV = G H with G > 1 (the G value heads of a key head each add to its dq and dk).
+template <bool GROUPED>
 __global__ void __launch_bounds__(kGradsThreads, 1)
     k_tc_grads(Prob p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out, bf16* __restrict__ dk_out,
                bf16* __restrict__ dv_out, float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws,
@@ -116,7 +120,14 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     auto S = [&](int off) { return smem_u32(sm + off); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int HV = p.HV, H = p.H, G = HV / H;
+    const int HV = p.HV, H = p.H, G = GROUPED ? HV / H : 1;
+    // this CTA's items, round-robin: items b, b + grid, ...; with grouped value heads (w = group * G + j)
+    // groups b, b + grid, ..., each group's G items back to back, so that this CTA keeps their running
+    // dq / dk sum
+    auto next_w = [&](int64_t w) -> int64_t {
+        return GROUPED ? ((w + 1) % G ? w + 1 : w + 1 + (int64_t)(gridDim.x - 1) * G) : w + gridDim.x;
+    };
+    const int64_t w0 = GROUPED ? (int64_t)blockIdx.x * G : blockIdx.x;
     const int64_t total = p.NT * HV;
 
     if (tid == 0) {
@@ -163,7 +174,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 tma_load_3d(sm + GS::GT, &maps.g, 0, n.hv, (int)n.r0, b);
                 bulk_load(sm + GS::EGC + 512 * slot, ws.egc + n.ch * D, 512, b);
             };
-            int64_t w = blockIdx.x;
+            int64_t w = w0;
             {
                 const Item first = make_item(p, w, true);
                 issue_a(first, &bars[0]);
@@ -172,10 +183,10 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 issue_e(first, &bars[0], 0);
             }
             int i = 0;
-            for (; w < total; ++i, w += gridDim.x) {
+            for (; w < total; ++i, w = next_w(w)) {
                 const int slot = i & 1;
                 const uint32_t par = (uint32_t)i & 1;
-                const int64_t wn = w + gridDim.x;
+                const int64_t wn = next_w(w);
                 const bool has_next = wn < total;
                 const Item nx = make_item(p, has_next ? wn : w, has_next);
                 uint64_t* nbar = &bars[slot ^ 1];
@@ -236,6 +247,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_bf16(tmem + 384, desc_kmajor(S(GS::KC), D, ks), desc_mnmajor(S(GS::DN), kC, ks), imk,
                                  ks > 0);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 384, desc_kmajor(S(GS::KC), D, ks), desc_mnmajor(S(GS::DNL), kC, ks), imk, 1);
                     mma_commit(&bars[3]);
                 }
                 if (!pwait(&bars[3], par, 55)) break;
@@ -249,6 +262,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_bf16(tmem + 320, desc_kmajor(S(GS::QR), D, ks), desc_kmajor(S(GS::DN), kC, ks), ik,
                                  ks > 0);
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_bf16(tmem + 320, desc_kmajor(S(GS::QR), D, ks), desc_kmajor(S(GS::DNL), kC, ks), ik, 1);
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_bf16(tmem + 320, desc_kmajor(S(GS::KR), D, ks), desc_mnmajor(S(GS::DM), kC, ks), im, 1);
                     mma_commit(&bars[4]);
@@ -275,17 +290,17 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
         const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
         const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
         const bool rv = lane < 16;
-        int64_t w = blockIdx.x;
+        int64_t w = w0;
         if (tid < kC) {
             const Item first = make_item(p, w, true);
             float* sb = reinterpret_cast<float*>(sm + GS::BETA);
             sb[tid] = tid < first.c ? __bfloat162float(beta[(first.r0 + tid) * HV + first.hv]) : 0.f;
         }
-        for (int i = 0; w < total; ++i, w += gridDim.x) {
+        for (int i = 0; w < total; ++i, w = next_w(w)) {
             const int slot = i & 1;
             const uint32_t par = (uint32_t)i & 1;
             const Item cur = make_item(p, w, true);
-            const int64_t wn = w + gridDim.x;
+            const int64_t wn = next_w(w);
             const float* sbeta = reinterpret_cast<const float*>(sm + GS::BETA + 256 * slot);
             const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
             const int64_t r0 = cur.r0;
@@ -348,6 +363,9 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                         x[u] = (ii <= r && r < c) ? p.scale * x[u] : 0.f;
                     }
                     for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DN, ii, 16 * cq + 8 * u, kC, x + 8 * u);
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) x[u] -= __bfloat162float(__float2bfloat16_rn(x[u]));
+                    for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::DNL, ii, 16 * cq + 8 * u, kC, x + 8 * u);
                     tmem_ld16(tmem + lb + 192 + 16 * cq, x);  // T^T (bf16 operand of phase D)
                     tmem_ld_wait();
                     for (int u = 0; u < 2; ++u) st_tile_row8(sm + GS::TT, ii, 16 * cq + 8 * u, kC, x + 8 * u);
@@ -468,19 +486,23 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             if (!wait_group<kSimt>(&bars[4], par, ws.status, 46, fail)) break;
             tc_fence_after();
             {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
-                float dG[16];
+                // dGamma of each row replaces its Gamma2 in TMEM (columns 448 + row, read just before; the next
+                // item's MMAs leave those columns alone) until the reverse cumsum below
                 float dGC = 0.f;
                 const float sc = p.scale, sce = p.scale * e_ref;
-                // this thread's first output row and the row stride of dq / dk (or of the per-value-head partials)
-                const int HO = G == 1 ? H : HV;
-                const int64_t o0 = ((r0 + 16 * qtr) * HO + (G == 1 ? h : hv)) * D + d, rs = (int64_t)HO * D;
+                // this thread's first output row and the row stride of dq / dk
+                const int64_t o0 = ((r0 + 16 * qtr) * H + h) * D + d, rs = (int64_t)H * D;
+                // grouped value heads: value head j of a group adds its dq, dk to the running fp32 sum of the
+                // ones before it (kept per CTA in thread order, four rows per 16-byte slot, so that it stays
+                // in L2), and the last one writes the bf16 result
+                const int jg = GROUPED ? hv - h * G : 0;
                 // this thread's column in the 64-row q / k tiles: byte offset of (r, d) = qk0 + 128 r + (dd2 ^ 16 (r % 8))
                 const uint32_t qk0 = (uint32_t)((d >> 6) * kC * 128), dd2 = (uint32_t)((d & 63) * 2);
 #pragma unroll
                 for (int rb = 0; rb < 4; ++rb) {  // four rows at a time (register budget)
                     const uint32_t cb = (uint32_t)(16 * qtr + 4 * rb);
                     float aQt[4], aKh[4], aKr[4], aKc[4], aQr[4], aXk[4];
-                    uint32_t g2u[4], kb[4], qb[4];
+                    uint32_t g2u[4], kb[4], qb[4], dgb[4];
                     tmem_ld4(tmem + lb + 0 + cb, aQt);
                     tmem_ld4(tmem + lb + 256 + cb, aKh);
                     tmem_ld4(tmem + lb + 64 + cb, aKr);
@@ -488,6 +510,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     tmem_ld4(tmem + lb + 384 + cb, aQr);
                     tmem_ld4(tmem + lb + 128 + cb, aXk);
                     tmem_ld4u(tmem + lb + 448 + cb, g2u);
+                    float gq[4], gk[4];
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {  // raw k, q of this thread's channel (rows >= c read as zero)
                         const int r = 16 * qtr + 4 * rb + x;
@@ -524,23 +547,45 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                         dgv = fmaf(aQr[x], qr_b, dgv);
                         dgv = fmaf(aKr[x], kr_b, dgv);
                         dgv = fmaf(-aKc[x], kc_b, dgv);
-                        dG[ii] = in ? dgv : 0.f;
+                        dgb[x] = __float_as_uint(in ? dgv : 0.f);
+                        gq[x] = dqv;
+                        gk[x] = dkv;
                         if (in) {
                             dGC += khk;
-                            const int64_t o = o0 + ii * rs;
-                            if (G == 1) {
-                                st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o),
-                                             reinterpret_cast<uint8_t*>(dk_out + o), dqv, dkv);
-                            } else {
-                                ws.dqp[o] = dqv;
-                                ws.dkp[o] = dkv;
-                            }
+                            if (!GROUPED)
+                                st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o0 + ii * rs),
+                                             reinterpret_cast<uint8_t*>(dk_out + o0 + ii * rs), dqv, dkv);
+                        }
+                    }
+                    tmem_st4(tmem + lb + 448 + cb, dgb);
+                    if (GROUPED) {
+                        float4* sq = reinterpret_cast<float4*>(ws.dqp) + ((int64_t)blockIdx.x * 4 + rb) * kSimt + tid;
+                        float4* sk = reinterpret_cast<float4*>(ws.dkp) + ((int64_t)blockIdx.x * 4 + rb) * kSimt + tid;
+                        if (jg > 0) {
+                            const float4 a = *sq, b = *sk;
+                            gq[0] += a.x, gq[1] += a.y, gq[2] += a.z, gq[3] += a.w;  // running sum + this head
+                            gk[0] += b.x, gk[1] += b.y, gk[2] += b.z, gk[3] += b.w;
+                        }
+                        if (jg < G - 1) {
+                            *sq = make_float4(gq[0], gq[1], gq[2], gq[3]);
+                            *sk = make_float4(gk[0], gk[1], gk[2], gk[3]);
+                        } else {
+#pragma unroll
+                            for (int x = 0; x < 4; ++x)
+                                if (16 * qtr + 4 * rb + x < c)
+                                    st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o0 + (4 * rb + x) * rs),
+                                                 reinterpret_cast<uint8_t*>(dk_out + o0 + (4 * rb + x) * rs), gq[x],
+                                                 gk[x]);
                         }
                     }
                 }
                 // dg = reverse in-chunk cumsum of dGamma, whose last valid row also takes the Gamma_C terms
                 // dGCt: in-quarter suffix sums and quarter totals first (one exchange), then per row the later
                 // quarters' totals (added in the order 3, 2, 1) and dGCt where row c - 1 lies at or after it.
+                float dG[16];
+                tmem_st_wait();
+                tmem_ld16(tmem + lb + 448 + 16 * qtr, dG);
+                tmem_ld_wait();
                 float run = 0.f;
 #pragma unroll
                 for (int x = 15; x >= 0; --x) {
@@ -571,32 +616,11 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-// dq, dk of key head h = sum over its G value heads in ascending order; each thread
-// handles 4 consecutive key channels of one (row, key head).
-__global__ void __launch_bounds__(256) k_tc_gva_reduce(int64_t rows, int H, int G, const float* __restrict__ dqp,
-                                                       const float* __restrict__ dkp, bf16* __restrict__ dq,
-                                                       bf16* __restrict__ dk) {
-    const int64_t total = rows * H * (D / 4);
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int d4 = (int)(i & (D / 4 - 1));
-        const int64_t rh = i >> 5;  // row * H + key head (D / 4 = 32 channel groups)
-        const int64_t base = rh * G * D + 4 * d4;  // value heads hh * G .. hh * G + G - 1 of that row
-        float4 aq = make_float4(0.f, 0.f, 0.f, 0.f), ak = aq;
-        for (int j = 0; j < G; ++j) {
-            const float4 x = *reinterpret_cast<const float4*>(dqp + base + (int64_t)j * D);
-            const float4 y = *reinterpret_cast<const float4*>(dkp + base + (int64_t)j * D);
-            aq.x += x.x; aq.y += x.y; aq.z += x.z; aq.w += x.w;
-            ak.x += y.x; ak.y += y.y; ak.z += y.z; ak.w += y.w;
-        }
-        *reinterpret_cast<uint2*>(dq + rh * D + 4 * d4) = make_uint2(pack2(aq.x, aq.y), pack2(aq.z, aq.w));
-        *reinterpret_cast<uint2*>(dk + rh * D + 4 * d4) = make_uint2(pack2(ak.x, ak.y), pack2(ak.z, ak.w));
-    }
-}
-
 }  // namespace
 
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_grads, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
+    auto kern = p.HV != p.H ? k_tc_grads<true> : k_tc_grads<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
     if (e != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.B * p.T;
     if (p.NT == 0 || rows == 0) return cudaSuccess;
@@ -612,16 +636,16 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const int64_t items = p.NT * p.HV;  // persistent: one CTA per SM, items dealt round-robin
-    const unsigned grid = (unsigned)(items < nsm ? items : nsm);
-    k_tc_grads<<<grid, kGradsThreads, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk,
-                                                        (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
+    // persistent: one CTA per SM, at most one per (chunk, key head) group and at most kGradsMaxCtas (the
+    // CTAs the group-sum scratch is sized for)
+    const bool grouped = p.HV != p.H;
+    const int64_t groups = p.NT * p.H;
+    int64_t grid = groups < nsm ? groups : nsm;
+    if (grid > kGradsMaxCtas) grid = kGradsMaxCtas;
+    if (grouped && (!ws.dqp || !ws.dkp)) return cudaErrorInvalidValue;
+    kern<<<(unsigned)grid, kGradsThreads, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk,
+                                                            (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
-    if (p.HV != p.H) {
-        k_tc_gva_reduce<<<8 * 152, 256, 0, st>>>(rows, p.H, p.HV / p.H, ws.dqp, ws.dkp, (bf16*)io.dq,
-                                                  (bf16*)io.dk);
-        note_launch("tc_gva_reduce", st);
-    }
     return cudaGetLastError();
 }
 
