@@ -326,21 +326,17 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
             const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
 
-            float rd = 0.f;
+            float2 rd2 = bc2(0.f);  // even and odd columns accumulate separately, then add
 #pragma unroll
             for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
                 const uint4 a = *reinterpret_cast<const uint4*>(sm + GS::SIN + tile_off(d, c8, D));
                 const uint4 b = *reinterpret_cast<const uint4*>(sm + GS::DSO + tile_off(d, c8, D));
-                const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-                const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 fa = __bfloat1622float2(pa[u]), fb = __bfloat1622float2(pb[u]);
-                    rd = fmaf(fa.x, fb.x, rd);
-                    rd = fmaf(fa.y, fb.y, rd);
-                }
+                rd2 = fma2(f2(bf_lo(a.x), bf_hi(a.x)), f2(bf_lo(b.x), bf_hi(b.x)), rd2);
+                rd2 = fma2(f2(bf_lo(a.y), bf_hi(a.y)), f2(bf_lo(b.y), bf_hi(b.y)), rd2);
+                rd2 = fma2(f2(bf_lo(a.z), bf_hi(a.z)), f2(bf_lo(b.z), bf_hi(b.z)), rd2);
+                rd2 = fma2(f2(bf_lo(a.w), bf_hi(a.w)), f2(bf_lo(b.w), bf_hi(b.w)), rd2);
             }
-            xrd[qtr * 128 + d] = rd;
+            xrd[qtr * 128 + d] = rd2.x + rd2.y;
             if (!wait_group<kSimt>(&bars[2], par, ws.status, 42, fail)) break;
             tc_fence_after();
             {  // epilogue A: dw^T, dN^T and T^T row segments (16 columns), dv row segments (32 columns)
@@ -402,19 +398,25 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 float kr[8], kc[8], qr[8], kt[8];
                 uint32_t g2b[8];
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
+                for (int x = 0; x < 8; x += 2) {  // rows r and r + 1 as packed fp32 pairs
                     const int r = 16 * qtr + 8 * h8 + x;
-                    const bool in = r < c;
-                    const uint32_t kbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
-                    const uint32_t qbits = in ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
-                    const float kv = __uint_as_float(kbits << 16), qv = __uint_as_float(qbits << 16);
-                    const float gm = G2[8 * h8 + x];
-                    g2b[x] = __float_as_uint(gm);
-                    const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref;
-                    kr[x] = kv * ep;
-                    kc[x] = kv * em;
-                    qr[x] = qv * ep;
-                    kt[x] = kv * E;
+                    const bool in0 = r < c, in1 = r + 1 < c;
+                    const uint32_t kb0 = in0 ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r)) : 0u;
+                    const uint32_t qb0 = in0 ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r)) : 0u;
+                    const uint32_t kb1 = in1 ? *reinterpret_cast<const uint16_t*>(sm + GS::K + ad.at(r + 1)) : 0u;
+                    const uint32_t qb1 = in1 ? *reinterpret_cast<const uint16_t*>(sm + GS::Q + ad.at(r + 1)) : 0u;
+                    const float2 kv = f2(bf_lo(kb0), bf_lo(kb1)), qv = f2(bf_lo(qb0), bf_lo(qb1));
+                    const float2 gm = f2(G2[8 * h8 + x], G2[8 * h8 + x + 1]);
+                    g2b[x] = __float_as_uint(gm.x);
+                    g2b[x + 1] = __float_as_uint(gm.y);
+                    const float2 gd = add2(gm, bc2(-ref));
+                    const float2 ep = f2(fast_exp2(gd.x), fast_exp2(gd.y)), em = f2(fast_exp2(-gd.x), fast_exp2(-gd.y));
+                    const float2 E = mul2(ep, bc2(e_ref));
+                    const float2 a = mul2(kv, ep), b = mul2(kv, em), cq2 = mul2(qv, ep), t = mul2(kv, E);
+                    kr[x] = a.x, kr[x + 1] = a.y;
+                    kc[x] = b.x, kc[x + 1] = b.y;
+                    qr[x] = cq2.x, qr[x + 1] = cq2.y;
+                    kt[x] = t.x, kt[x + 1] = t.y;
                 }
                 const int c0 = 16 * qtr + 8 * h8;
                 st_tile_row8(sm + GS::KR, d, c0, D, kr);
@@ -525,36 +527,48 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                         if (lane == 0) mbar_arrive(&bars[7]);
                     }
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
+                    for (int x = 0; x < 4; x += 2) {  // rows r and r + 1 as packed fp32 pairs
                         const int ii = 4 * rb + x, r = 16 * qtr + ii;
-                        const bool in = r < c;
-                        const float kv = __uint_as_float(kb[x] << 16), qv = __uint_as_float(qb[x] << 16);
-                        const float gm = __uint_as_float(g2u[x]);
-                        const float ep = fast_exp2(gm - ref), em = fast_exp2(ref - gm), E = ep * e_ref, eh = em * e_cr;
-                        const float bX = sbeta[r] * aXk[x];
+                        const float2 kv = f2(bf_lo(kb[x]), bf_lo(kb[x + 1])), qv = f2(bf_lo(qb[x]), bf_lo(qb[x + 1]));
+                        const float2 gd = add2(f2(__uint_as_float(g2u[x]), __uint_as_float(g2u[x + 1])), bc2(-ref));
+                        const float2 ep = f2(fast_exp2(gd.x), fast_exp2(gd.y)), em = f2(fast_exp2(-gd.x), fast_exp2(-gd.y));
+                        const float2 E = mul2(ep, bc2(e_ref)), eh = mul2(em, bc2(e_cr));
+                        const float2 bX = mul2(*reinterpret_cast<const float2*>(sbeta + r), f2(aXk[x], aXk[x + 1]));
+                        const float2 aQt2 = f2(aQt[x], aQt[x + 1]), aQr2 = f2(aQr[x], aQr[x + 1]);
+                        const float2 aKr2 = f2(aKr[x], aKr[x + 1]), aKc2 = f2(aKc[x], aKc[x + 1]);
+                        const float2 aKh2 = f2(aKh[x], aKh[x + 1]);
                         // dq = E scale dQ~ + ep dQr;  dk = eh dK^ + E beta dXk + ep dKr + em dKc
-                        const float dqv = ep * fmaf(sce, aQt[x], aQr[x]);
-                        const float dkv = fmaf(ep, fmaf(e_ref, bX, aKr[x]), em * fmaf(e_cr, aKh[x], aKc[x]));
-                        const float khk = aKh[x] * (kv * eh);
+                        const float2 dqv = mul2(ep, fma2(bc2(sce), aQt2, aQr2));
+                        const float2 dkv =
+                            fma2(ep, fma2(bc2(e_ref), bX, aKr2), mul2(em, fma2(bc2(e_cr), aKh2, aKc2)));
+                        const float2 khk = mul2(aKh2, mul2(kv, eh));
                         // The factor values of the dGamma pair terms are the bf16 values the MMAs used (rounded
                         // two at a time here as in the factor tiles), so that each in-chunk pair's contributions
                         // to its two rows cancel in the chunk sum as they do exactly.
-                        const uint32_t p1 = pack2(kv * E, qv * ep), p2 = pack2(kv * ep, kv * em);
-                        const float kt_b = __uint_as_float(p1 << 16), qr_b = __uint_as_float(p1 & 0xffff0000u);
-                        const float kr_b = __uint_as_float(p2 << 16), kc_b = __uint_as_float(p2 & 0xffff0000u);
-                        float dgv = fmaf(sc * aQt[x], qv * E, -khk);
-                        dgv = fmaf(bX, kt_b, dgv);
-                        dgv = fmaf(aQr[x], qr_b, dgv);
-                        dgv = fmaf(aKr[x], kr_b, dgv);
-                        dgv = fmaf(-aKc[x], kc_b, dgv);
-                        dgb[x] = __float_as_uint(in ? dgv : 0.f);
-                        gq[x] = dqv;
-                        gk[x] = dkv;
-                        if (in) {
-                            dGC += khk;
+                        const float2 kE = mul2(kv, E), qp = mul2(qv, ep), kp = mul2(kv, ep), km = mul2(kv, em);
+                        const uint32_t p1a = pack2(kE.x, qp.x), p1b = pack2(kE.y, qp.y);
+                        const uint32_t p2a = pack2(kp.x, km.x), p2b = pack2(kp.y, km.y);
+                        float2 dgv = fma2(mul2(bc2(sc), aQt2), mul2(qv, E), neg2(khk));
+                        dgv = fma2(bX, f2(bf_lo(p1a), bf_lo(p1b)), dgv);
+                        dgv = fma2(aQr2, f2(bf_hi(p1a), bf_hi(p1b)), dgv);
+                        dgv = fma2(aKr2, f2(bf_lo(p2a), bf_lo(p2b)), dgv);
+                        dgv = fma2(neg2(aKc2), f2(bf_hi(p2a), bf_hi(p2b)), dgv);
+                        const bool in0 = r < c, in1 = r + 1 < c;
+                        dgb[x] = __float_as_uint(in0 ? dgv.x : 0.f);
+                        dgb[x + 1] = __float_as_uint(in1 ? dgv.y : 0.f);
+                        gq[x] = dqv.x, gq[x + 1] = dqv.y;
+                        gk[x] = dkv.x, gk[x + 1] = dkv.y;
+                        if (in0) {
+                            dGC += khk.x;
                             if (!GROUPED)
                                 st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o0 + ii * rs),
-                                             reinterpret_cast<uint8_t*>(dk_out + o0 + ii * rs), dqv, dkv);
+                                             reinterpret_cast<uint8_t*>(dk_out + o0 + ii * rs), dqv.x, dkv.x);
+                        }
+                        if (in1) {
+                            dGC += khk.y;
+                            if (!GROUPED)
+                                st_bf16_pair(reinterpret_cast<uint8_t*>(dq_out + o0 + (ii + 1) * rs),
+                                             reinterpret_cast<uint8_t*>(dk_out + o0 + (ii + 1) * rs), dqv.y, dkv.y);
                         }
                     }
                     tmem_st4(tmem + lb + 448 + cb, dgb);

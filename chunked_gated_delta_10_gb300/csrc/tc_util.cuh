@@ -347,6 +347,17 @@ __device__ __forceinline__ void st_bf16_pair(uint8_t* pa, uint8_t* pb, float a, 
 __device__ __forceinline__ void st_col_pair(uint8_t* tile, const ColAddr& a, int r, float x0, float x1) {
     st_bf16_pair(tile + a.at(r), tile + a.at(r + 1), x0, x1);
 }
+// Packed fp32 pairs: one instruction for two IEEE fp32 operations (each lane rounds as its scalar form).
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+__device__ __forceinline__ float2 bc2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+// The two bf16 halves of a packed pair, widened: low (first) and high (second) element.
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
 // 2^x with the hardware approximation (ex2.approx.ftz: relative error ~2^-22).
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
