@@ -93,28 +93,24 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     // Each thread forms a 1 x 2 strip (256 strips per product).
     {
         const int pr = tid >> 7, base = 32 * pr, a = (tid >> 3) & 15, c = 2 * (tid & 7);
-        float s0 = 0.f, s1 = 0.f;
+        float2 s = bc2(0.f);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
             const float l = L[lsk(base + 16 + a, base + m)];
-            const float2 o = *reinterpret_cast<const float2*>(Out + (base + m) * kC + base + c);
-            s0 = fmaf(l, o.x, s0);
-            s1 = fmaf(l, o.y, s1);
+            s = fma2(bc2(l), *reinterpret_cast<const float2*>(Out + (base + m) * kC + base + c), s);
         }
-        *reinterpret_cast<float2*>(X + pr * 256 + a * 16 + c) = make_float2(s0, s1);
+        *reinterpret_cast<float2*>(X + pr * 256 + a * 16 + c) = s;
     }
     __syncthreads();
     {
         const int pr = tid >> 7, base = 32 * pr, a = (tid >> 3) & 15, c = 2 * (tid & 7);
-        float s0 = 0.f, s1 = 0.f;
+        float2 s = bc2(0.f);
 #pragma unroll
         for (int m = 0; m < 16; ++m) {
             const float l = Out[(base + 16 + a) * kC + base + 16 + m];
-            const float2 xv = *reinterpret_cast<const float2*>(X + pr * 256 + m * 16 + c);
-            s0 = fmaf(l, xv.x, s0);
-            s1 = fmaf(l, xv.y, s1);
+            s = fma2(bc2(l), *reinterpret_cast<const float2*>(X + pr * 256 + m * 16 + c), s);
         }
-        *reinterpret_cast<float2*>(Out + (base + 16 + a) * kC + base + c) = make_float2(-s0, -s1);
+        *reinterpret_cast<float2*>(Out + (base + 16 + a) * kC + base + c) = neg2(s);
     }
     __syncthreads();
     // 32 -> 64, rows 32..63, columns 0..31. X = L[32:64, 0:32] D0 with D0 the (block lower
@@ -122,14 +118,12 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
     // of D0's upper-right zero block (16..31 for rows 0..15) only take rows 16..31.
     {
         const int a = lane, c0 = 4 * warp;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        float2 s01 = bc2(0.f), s23 = bc2(0.f);
         auto term = [&](int m) {
             const float l = L[lsk(32 + a, m)];
             const float4 o = *reinterpret_cast<const float4*>(Out + m * kC + c0);
-            s0 = fmaf(l, o.x, s0);
-            s1 = fmaf(l, o.y, s1);
-            s2 = fmaf(l, o.z, s2);
-            s3 = fmaf(l, o.w, s3);
+            s01 = fma2(bc2(l), f2(o.x, o.y), s01);
+            s23 = fma2(bc2(l), f2(o.z, o.w), s23);
         };
         if (c0 < 16) {
 #pragma unroll
@@ -138,21 +132,19 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 #pragma unroll
             for (int m = 16; m < 32; ++m) term(m);
         }
-        *reinterpret_cast<float4*>(X + a * 36 + c0) = make_float4(s0, s1, s2, s3);
+        *reinterpret_cast<float4*>(X + a * 36 + c0) = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
     __syncthreads();
     // then -D1 X with D1 the bottom-right 32 x 32 inverse: row 32 + a, columns c0 .. c0+3,
     // a = 4 warp + lane / 8 (rows 0..15 of D1 end at its column 15)
     {
         const int a = tid >> 3, c0 = (tid & 7) * 4;
-        float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+        float2 s01 = bc2(0.f), s23 = bc2(0.f);
         auto term = [&](int m) {
             const float l = Out[(32 + a) * kC + 32 + m];
             const float4 xv = *reinterpret_cast<const float4*>(X + m * 36 + c0);
-            s0 = fmaf(l, xv.x, s0);
-            s1 = fmaf(l, xv.y, s1);
-            s2 = fmaf(l, xv.z, s2);
-            s3 = fmaf(l, xv.w, s3);
+            s01 = fma2(bc2(l), f2(xv.x, xv.y), s01);
+            s23 = fma2(bc2(l), f2(xv.z, xv.w), s23);
         };
         if (a < 16) {
 #pragma unroll
@@ -161,7 +153,7 @@ __device__ void tri_inverse64(const float* L, float* Out, float* X) {
 #pragma unroll
             for (int m = 0; m < 32; ++m) term(m);
         }
-        *reinterpret_cast<float4*>(Out + (32 + a) * kC + c0) = make_float4(-s0, -s1, -s2, -s3);
+        *reinterpret_cast<float4*>(Out + (32 + a) * kC + c0) = make_float4(-s01.x, -s01.y, -s23.x, -s23.y);
     }
     __syncthreads();
 }
@@ -269,7 +261,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             if (qt == 0) *reinterpret_cast<float2*>(ws.egc + ch * D + d0) = make_float2(exp2f(gC0), exp2f(gC1));
             // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G = ep 2^ref and K^'s
             // factor 2^(G_C-G) = em 2^(G_C-ref) follow from them (the formulas of the gradient kernel)
-            const float er0 = exp2f(ref0), er1 = exp2f(ref1), ec0 = exp2f(gC0 - ref0), ec1 = exp2f(gC1 - ref1);
+            const float2 er = f2(exp2f(ref0), exp2f(ref1)), ec = f2(exp2f(gC0 - ref0), exp2f(gC1 - ref1));
+            const float2 nref = f2(-ref0, -ref1);
             if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
             // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^
 #pragma unroll
@@ -279,23 +272,24 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 const uint32_t o = a64.at(r);
                 const uint32_t k2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::K + o) : 0u;
                 const uint32_t q2 = in ? *reinterpret_cast<const uint32_t*>(sm + IS::Q + o) : 0u;
-                const float k0 = __uint_as_float(k2 << 16), k1 = __uint_as_float(k2 & 0xffff0000u);
-                const float q0 = __uint_as_float(q2 << 16), q1 = __uint_as_float(q2 & 0xffff0000u);
-                const float gm0 = G2[x], gm1 = G2[16 + x];
-                const float ep0 = fast_exp2(gm0 - ref0), em0 = fast_exp2(ref0 - gm0), E0 = ep0 * er0, eh0 = em0 * ec0;
-                const float ep1 = fast_exp2(gm1 - ref1), em1 = fast_exp2(ref1 - gm1), E1 = ep1 * er1, eh1 = em1 * ec1;
-                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(k0 * ep0, k1 * ep1);
-                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(q0 * ep0, q1 * ep1);
+                // channels d0 and d0 + 1 as packed fp32 pairs
+                const float2 kk = f2(bf_lo(k2), bf_hi(k2)), qq = f2(bf_lo(q2), bf_hi(q2));
+                const float2 gd = add2(f2(G2[x], G2[16 + x]), nref);  // G - Gref
+                const float2 ep = f2(fast_exp2(gd.x), fast_exp2(gd.y)), em = f2(fast_exp2(-gd.x), fast_exp2(-gd.y));
+                const float2 E = mul2(ep, er), eh = mul2(em, ec);
+                const float2 kr = mul2(kk, ep), qr = mul2(qq, ep), kc = mul2(kk, em);
+                const float2 kt = mul2(kk, E), kh = mul2(kk, eh), qs = mul2(mul2(bc2(p.scale), qq), E);
+                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(r)) = pack2(kr.x, kr.y);
+                *reinterpret_cast<uint32_t*>(sm + IS::KQ + a128.at(kC + r)) = pack2(qr.x, qr.y);
                 {  // Kc as a bf16 pair and the bf16 pair of its rounding remainder
-                    const float c0 = k0 * em0, c1 = k1 * em1;
-                    const uint32_t hi = pack2(c0, c1);
+                    const uint32_t hi = pack2(kc.x, kc.y);
                     *reinterpret_cast<uint32_t*>(sm + IS::KC + o) = hi;
-                    *reinterpret_cast<uint32_t*>(sm + IS::XB + o) =
-                        pack2(c0 - __uint_as_float(hi << 16), c1 - __uint_as_float(hi & 0xffff0000u));
+                    const float2 lo = add2(kc, neg2(f2(bf_lo(hi), bf_hi(hi))));
+                    *reinterpret_cast<uint32_t*>(sm + IS::XB + o) = pack2(lo.x, lo.y);
                 }
-                *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(k0 * E0, k1 * E1);
-                *reinterpret_cast<uint32_t*>(sm + IS::K + o) = pack2(k0 * eh0, k1 * eh1);
-                *reinterpret_cast<uint32_t*>(sm + IS::Q + o) = pack2(p.scale * q0 * E0, p.scale * q1 * E1);
+                *reinterpret_cast<uint32_t*>(sm + IS::XK + o) = pack2(kt.x, kt.y);
+                *reinterpret_cast<uint32_t*>(sm + IS::K + o) = pack2(kh.x, kh.y);
+                *reinterpret_cast<uint32_t*>(sm + IS::Q + o) = pack2(qs.x, qs.y);
             }
             fence_async_smem();
             tc_fence_before();
@@ -332,20 +326,24 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 tmem_ld_wait();
                 if (R < kC) {
                     const int r = R;
-                    for (int j = 0; j < 32; ++j) Akk[lsk(r, c0 + j)] = (c0 + j < r) ? sb[r] * row[j] : 0.f;
+                    const float2 br = bc2(sb[r]);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float2 v = mul2(br, f2(row[j], row[j + 1]));
+                        Akk[lsk(r, c0 + j)] = (c0 + j < r) ? v.x : 0.f;
+                        Akk[lsk(r, c0 + j + 1)] = (c0 + j + 1 < r) ? v.y : 0.f;
+                    }
                 } else {
                     const int r = R - kC;
                     uint8_t* gA = ws.aqk + ch * TCC;
                     for (int u = 0; u < 32; u += 8) {
-                        float xx[8];
+                        uint32_t pk[4];
 #pragma unroll
-                        for (int t = 0; t < 8; ++t) xx[t] = (c0 + u + t <= r) ? p.scale * row[u + t] : 0.f;
-                        uint4 vv;
-                        vv.x = pack2(xx[0], xx[1]);
-                        vv.y = pack2(xx[2], xx[3]);
-                        vv.z = pack2(xx[4], xx[5]);
-                        vv.w = pack2(xx[6], xx[7]);
-                        *reinterpret_cast<uint4*>(gA + tile_off(r, c0 + u, kC)) = vv;
+                        for (int t = 0; t < 8; t += 2) {
+                            const float2 v = mul2(bc2(p.scale), f2(row[u + t], row[u + t + 1]));
+                            pk[t / 2] = pack2((c0 + u + t <= r) ? v.x : 0.f, (c0 + u + t + 1 <= r) ? v.y : 0.f);
+                        }
+                        *reinterpret_cast<uint4*>(gA + tile_off(r, c0 + u, kC)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
                 }
             }
@@ -363,7 +361,11 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                     st_tile_row8(sm + IS::TINV, r, c0, kC, fr);
                     float xb[8];
 #pragma unroll
-                    for (int t = 0; t < 8; ++t) xb[t] = fr[t] * sb[c0 + t];
+                    for (int t = 0; t < 8; t += 2) {
+                        const float2 v = mul2(*reinterpret_cast<const float2*>(fr + t),
+                                              *reinterpret_cast<const float2*>(sb + c0 + t));
+                        xb[t] = v.x, xb[t + 1] = v.y;
+                    }
                     st_tile_row8(sm + IS::TINVB, r, c0, kC, xb);
                 }
             }
@@ -595,7 +597,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
             tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
+            for (int j = 0; j < 32; j += 2) {
+                const float2 v = fma2(bc2(e), f2(S[32 * h + j], S[32 * h + j + 1]), f2(acc[j], acc[j + 1]));
+                S[32 * h + j] = v.x, S[32 * h + j + 1] = v.y;
+            }
         }
         tc_fence_before();
     }
@@ -692,10 +697,9 @@ __global__ void __launch_bounds__(256, 1) k_tc_seg_combine(Prob p, SegArg sg, in
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
                 const float4 c4 = cj[v4];
-                acc[4 * v4] = fmaf(pkj, c4.x, acc[4 * v4]);
-                acc[4 * v4 + 1] = fmaf(pkj, c4.y, acc[4 * v4 + 1]);
-                acc[4 * v4 + 2] = fmaf(pkj, c4.z, acc[4 * v4 + 2]);
-                acc[4 * v4 + 3] = fmaf(pkj, c4.w, acc[4 * v4 + 3]);
+                const float2 lo = fma2(bc2(pkj), f2(c4.x, c4.y), f2(acc[4 * v4], acc[4 * v4 + 1]));
+                const float2 hi = fma2(bc2(pkj), f2(c4.z, c4.w), f2(acc[4 * v4 + 2], acc[4 * v4 + 3]));
+                acc[4 * v4] = lo.x, acc[4 * v4 + 1] = lo.y, acc[4 * v4 + 2] = hi.x, acc[4 * v4 + 3] = hi.y;
             }
         }
         if (jh == 1) {
@@ -868,7 +872,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
             tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
+            for (int j = 0; j < 32; j += 2) {
+                const float2 v = fma2(bc2(e), f2(S[32 * h + j], S[32 * h + j + 1]), f2(acc[j], acc[j + 1]));
+                S[32 * h + j] = v.x, S[32 * h + j + 1] = v.y;
+            }
         }
         tc_fence_before();
     }
