@@ -254,6 +254,23 @@ def test_segmented_forward_long_sequence(kda):
     assert all(e <= _tol(inp) for e in errs.values()), errs
 
 
+# Tensor-core gradient kernel with grouped value heads: a group's G value heads run back to back on one
+# CTA, which carries their dq / dk sum; groups of 3 and 4, partial chunks, empty sequences, fewer groups
+# than CTAs, and a group count that does not divide among the CTAs.
+GROUPED = {
+    "g4_one_head": dict(B=1, T=200, H=1, HV=4, K=128, V=128),
+    "g3_varlen": dict(B=1, T=0, H=2, HV=6, K=128, V=128, seq_lens=[130, 1, 0, 64, 77]),
+    "g2_many_groups": dict(B=2, T=64 * 90 + 5, H=1, HV=2, K=128, V=128),
+}
+
+
+@pytest.mark.parametrize("name", list(GROUPED))
+def test_grouped_value_heads_tensor_core(kda, name):
+    inp = kda_inputs.small(seed=46, dtype="bf16", **GROUPED[name])
+    out = gpu_bwd(kda, inp)
+    compare_full(inp, out, oracle.run_inputs(inp))
+
+
 # ------------------------------------------------------- the five workloads
 
 @functools.lru_cache(maxsize=1)
