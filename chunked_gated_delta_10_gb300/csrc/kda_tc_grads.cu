@@ -60,10 +60,13 @@ struct GS {
     // dN = dN_hi + dN_lo as a bf16 pair (phases B and E take both); dM takes the first 8 KB of its region
     static constexpr int DNL = DM + TCC;
     static constexpr int EGC = TT + TCC, BETA = EGC + 1024, XRD = BETA + 512, BARS = XRD + 2048;
-    static constexpr int END = BARS + 128;
-    // scratch in the dw tile while that tile is dead: cumsum quarter totals and the reference / last-row gates
-    // (chunk start), dbeta partials (epilogues B and D), Gamma_C terms and dg quarter totals (final epilogue)
-    static constexpr int XTOT = DW, XRG = DW + 2048, XDB = DW + 4096, XGC = DW + 8192, XT1 = DW + 10240;
+    // cumsum quarter totals and the reference / last-row gates (chunk start), in a region of their own: the
+    // warps write the dw tile in epilogue A without waiting for each other to have read them
+    static constexpr int XTOT = BARS + 128, XRG = XTOT + 2048;
+    static constexpr int END = XRG + 1024;
+    // scratch in the dw tile while that tile is dead: dbeta partials (epilogues B and D), Gamma_C terms and dg
+    // quarter totals (final epilogue)
+    static constexpr int XDB = DW + 4096, XGC = DW + 8192, XT1 = DW + 10240;
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
@@ -133,7 +136,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     if (tid == 0) {
         mbar_init(&bars[0], 4);  // four input groups per item
         mbar_init(&bars[1], 4);
-        for (int x = 2; x < 9; ++x) mbar_init(&bars[x], x == 7 ? kSimt / 32 : 1);
+        // [2, 3, 4] by the producer's MMA commits; [5, 6, 7, 8] by each SIMT warp
+        for (int x = 2; x < 9; ++x) mbar_init(&bars[x], x >= 5 ? kSimt / 32 : 1);
         fence_mbar_init();
         *fail = 0;
     }
@@ -320,12 +324,6 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 if (16 * qtr + x == rmid) xrg[d] = G2[x];
                 if (16 * qtr + x == c - 1) xrg[128 + d] = G2[x];
             }
-            group_sync<kSimt>();
-            const float ref = xrg[d], gC = xrg[128 + d];
-            // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
-            // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
-            const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
-
             float2 rd2 = bc2(0.f);  // even and odd columns accumulate separately, then add
 #pragma unroll
             for (int c8 = 32 * qtr; c8 < 32 * qtr + 32; c8 += 8) {  // <S_in[d, v], dS_out[d, v]> over 32 columns v
@@ -337,7 +335,13 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 rd2 = fma2(f2(bf_lo(a.w), bf_hi(a.w)), f2(bf_lo(b.w), bf_hi(b.w)), rd2);
             }
             xrd[qtr * 128 + d] = rd2.x + rd2.y;
+            // phase A complete, the reference rows written and every warp past its reads of S_in and dS_out
+            // (which the factor pass overwrites)
             if (!wait_group<kSimt>(&bars[2], par, ws.status, 42, fail)) break;
+            const float ref = xrg[d], gC = xrg[128 + d];
+            // per element only ep = 2^(G-ref) and em = 2^(ref-G) are evaluated; E = 2^G and
+            // K^'s factor 2^(G_C-G) follow from them (the same formulas in both passes below)
+            const float e_ref = exp2f(ref), e_cr = exp2f(gC - ref);
             tc_fence_after();
             {  // epilogue A: dw^T, dN^T and T^T row segments (16 columns), dv row segments (32 columns)
                 const float br = rv ? sbeta[rrow] : 0.f;
@@ -386,8 +390,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             }
             tc_fence_before();
             fence_async_smem();
-            group_sync<kSimt>();  // epilogue A's tiles are written and its accumulators read
-            if (tid == 0) mbar_arrive(&bars[8]);  // operands of phase B's first part are in place
+            __syncwarp();  // this warp's part of epilogue A's tiles is written and its accumulators read
+            if (lane == 0) mbar_arrive(&bars[8]);  // (all warps: operands of phase B's first part in place)
             tc_fence_after();
             // decayed factor tiles, stored transposed (row = key channel, column = chunk row): channel d,
             // this thread's 16 rows as two 16-byte row segments per tile (rows >= c are zero). Gamma2 goes
@@ -428,8 +432,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             tmem_st_wait();
             tc_fence_before();
             fence_async_smem();
-            group_sync<kSimt>();
-            if (tid == 0) mbar_arrive(&bars[5]);  // operands of phase B are in place
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[5]);  // (all warps: operands of phase B are in place)
             if (tid < kC) {  // beta of the next item to its shared slot, while phase B runs
                 float nb = 0.f;
                 if (wn < total) {
@@ -479,13 +483,13 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             }
             tc_fence_before();
             fence_async_smem();
-            group_sync<kSimt>();
-            if (tid == 0) mbar_arrive(&bars[6]);  // dM is in place and INV has been read
-            if (tid < kC && tid < c)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[6]);  // (all warps: dM is in place and INV has been read)
+            if (!wait_group<kSimt>(&bars[4], par, ws.status, 46, fail)) break;
+            if (tid < kC && tid < c)  // every warp's dbeta partials are written
                 db_out[(r0 + tid) * HV + hv] =
                     __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
                                         ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
-            if (!wait_group<kSimt>(&bars[4], par, ws.status, 46, fail)) break;
             tc_fence_after();
             {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
                 // dGamma of each row replaces its Gamma2 in TMEM (columns 448 + row, read just before; the next
@@ -622,7 +626,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     if (r < c) dg_out[((r0 + r) * HV + hv) * D + d] = t + carry;
                 }
             }
-            group_sync<kSimt>();  // the next item's scratch is reused from here
+            // (no barrier here: the next item's first write to shared scratch follows its input barrier, which
+            // every warp reaches only after this item's reads)
         }
     }
     tc_fence_before();
