@@ -189,7 +189,9 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
     int* fail = reinterpret_cast<int*>(tslot + 1);
     float* Akk = reinterpret_cast<float*>(sm + IS::AKK);
     float* Fi = reinterpret_cast<float*>(sm + IS::FI);
-    float* tmp = reinterpret_cast<float*>(sm + IS::KQ);  // item-start scratch (6 x 128 floats)
+    // item-start scratch (6 x 128 floats) in the K~ tile, dead from the second product of the previous item
+    // to this item's factor pass
+    float* tmp = reinterpret_cast<float*>(sm + IS::XK);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d0 = 2 * (tid & 63), qt = tid >> 6;  // key channels d0, d0 + 1; chunk rows 16 qt .. +15
@@ -263,6 +265,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             // factor 2^(G_C-G) = em 2^(G_C-ref) follow from them (the formulas of the gradient kernel)
             const float2 er = f2(exp2f(ref0), exp2f(ref1)), ec = f2(exp2f(gC0 - ref0), exp2f(gC1 - ref1));
             const float2 nref = f2(-ref0, -ref1);
+            // this item's q and k landed, and every thread has read the reference rows (the factor pass
+            // overwrites the scratch)
             if (!wait_all(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 11, fail)) break;
             // decayed factors, two key channels per 32-bit access; in place: q -> scale Q~, k -> K^
 #pragma unroll
@@ -409,9 +413,10 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             if (tid == 0) {
                 bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
                 bulk_commit();
-                bulk_wait_read();  // the scratch and INV areas are rewritten by the next item
+                bulk_wait_read();  // the w, INV and INV diag(beta) tiles are rewritten by the next item's factor pass
             }
-            __syncthreads();
+            // (no barrier here: before its first barrier the next item writes only the item-start scratch, in the
+            // dead K~ tile, and thread 0 reaches that barrier only once the copies above have read their tiles)
         }
     }
 cleanup:
