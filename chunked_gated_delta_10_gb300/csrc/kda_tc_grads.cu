@@ -290,6 +290,13 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
         float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
         float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
         const float* gt = reinterpret_cast<const float*>(sm + GS::GT);
+        // a wait on the producer's barrier `b`: per warp (a time-out is noticed at the next group barrier), or for
+        // the grouped instantiation as a group (a time-out leaves the loop at once)
+        auto phase_wait = [&](uint64_t* b, uint32_t parity, int code) {
+            if constexpr (GROUPED) return wait_group<kSimt>(b, parity, ws.status, code, fail);
+            warp_wait(b, parity, ws.status, code, fail);
+            return true;
+        };
         const int d = tid & 127, qtr = tid >> 7, q4 = warp & 3, cq = warp >> 2;
         const uint32_t lb = (uint32_t)(32 * q4) << 16;  // this warp's TMEM lane quarter
         const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
@@ -309,7 +316,16 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
             const int64_t r0 = cur.r0;
             const int c = cur.c, hv = cur.hv, h = cur.h;
-            if (!wait_group<kSimt>(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 41, fail)) break;
+            // dbeta of the item's rows: the eight partial sums of epilogue B/D in a fixed order
+            auto store_dbeta = [&]() {
+                if (tid < kC && tid < c)
+                    db_out[(r0 + tid) * HV + hv] =
+                        __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
+                                            ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
+            };
+            // the item's inputs: each warp waits on its own (the cumsum's barrier below absorbs the warps' skew);
+            // with grouped value heads the CTA waits together (per-warp waits spill that instantiation)
+            if (!phase_wait(&bars[slot], (uint32_t)(i >> 1) & 1, 41)) break;
             // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
             float G2[16];
 #pragma unroll
@@ -442,7 +458,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 }
                 reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nb;
             }
-            if (!wait_group<kSimt>(&bars[3], par, ws.status, 43, fail)) break;
+            if (!phase_wait(&bars[3], par, 43)) break;  // phase B complete
             tc_fence_after();
             {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
                 if (q4 < 2) {  // INV part from PR^T row j (lanes 0..63 of an M = 128 accumulator), 16 columns
@@ -485,11 +501,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[6]);  // (all warps: dM is in place and INV has been read)
-            if (!wait_group<kSimt>(&bars[4], par, ws.status, 46, fail)) break;
-            if (tid < kC && tid < c)  // every warp's dbeta partials are written
-                db_out[(r0 + tid) * HV + hv] =
-                    __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
-                                        ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
+            if (!phase_wait(&bars[4], par, 46)) break;  // phase E complete
+            if (GROUPED) store_dbeta();  // (after the group's barrier: every warp's dbeta partials are written)
             tc_fence_after();
             {  // final epilogue, channel d, rows 16 * quarter .. +15: dq, dk, dGamma -> dg
                 // dGamma of each row replaces its Gamma2 in TMEM (columns 448 + row, read just before; the next
@@ -613,6 +626,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 xgc[qtr * 128 + d] = dGC;
                 xt1[qtr * 128 + d] = run;
                 group_sync<kSimt>();
+                if (*(volatile int*)fail) break;  // a warp's wait above gave up
+                if (!GROUPED) store_dbeta();  // every warp's dbeta partials (epilogue B/D) are written
                 const float dGCt = segc[d] * ((xrd[d] + xrd[128 + d]) + (xrd[256 + d] + xrd[384 + d])) +
                                    ((xgc[d] + xgc[128 + d]) + (xgc[256 + d] + xgc[384 + d]));
                 const int qc = (c - 1) >> 4, xc = (c - 1) & 15;

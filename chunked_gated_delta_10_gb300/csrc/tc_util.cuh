@@ -309,6 +309,13 @@ __device__ __forceinline__ bool wait_all2(uint64_t* bar_a, uint32_t par_a, int c
     __syncthreads();
     return *(volatile int*)fail == 0;
 }
+// Per-warp bounded wait (every lane polls, so every lane acquires the completed phase): no CTA barrier. On
+// time-out *fail becomes nonzero and the warp goes on; the caller's next group barrier reads *fail and
+// leaves the loop, so that no warp waits at a barrier another warp has left.
+__device__ __forceinline__ void warp_wait(uint64_t* bar, uint32_t parity, int* status, int code, int* fail) {
+    if (!mbar_wait(bar, parity, status, code)) *(volatile int*)fail = 1;
+    __syncwarp();
+}
 // The same for the group of threads 0 .. N-1 (group_sync); *fail must be written
 // by no thread outside the group, so that every thread of the group reads the
 // same value after the barrier.
