@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             // beta of the next item: loaded now, stored to its shared slot at the end of this item
             const float nbeta =
                 (has_next && tid < cn) ? __bfloat162float(beta[(r0n + tid) * HV + hvn]) : 0.f;
-            if (!wait_all(&bars[2], mph, ws.status, 12, fail)) break;
+            warp_wait(&bars[2], mph, ws.status, 12, fail);  // per warp; a time-out leaves at the next barrier
             mph ^= 1;
             if (tid == 0 && has_next) {
                 bulk_wait_read();  // the K^ and scale Q~ copies have read their tiles
@@ -353,6 +353,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             }
             tc_fence_before();
             __syncthreads();
+            if (*(volatile int*)fail) break;
             tri_inverse64(Akk, Fi, reinterpret_cast<float*>(sm + IS::XS));
             // INV and INVb = INV diag(beta) (column j scaled by beta_j) as bf16 operand tiles
             for (int e = tid; e < kC * (kC / 8); e += blockDim.x) {
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 bulk_store(ws.invb + ch * TCC, sm + IS::TINVB, TCC);
                 bulk_commit();
             }
-            if (!wait_all(&bars[2], mph, ws.status, 13, fail)) break;
+            warp_wait(&bars[2], mph, ws.status, 13, fail);
             mph ^= 1;
             if (has_next) load_g_pair(g, r0n, cn, HV, hvn, d0, qt, G2);
             tc_fence_after();
@@ -410,6 +411,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
             tc_fence_before();
             fence_async_smem();
             __syncthreads();
+            if (*(volatile int*)fail) break;
             if (tid == 0) {
                 bulk_store(ws.w + ch * TCD, sm + IS::WST, TCD);
                 bulk_commit();
@@ -555,7 +557,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
                 bulk_commit();
             }
         }
-        if (!wait_all(&bars[4], mph, ws.status, 22, fail)) break;
+        // per warp (the next barrier reads *fail): after it a warp touches only what the finished MMAs have read
+        warp_wait(&bars[4], mph, ws.status, 22, fail);
         mph ^= 1;
         if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w and INVb are consumed
         tc_fence_after();
