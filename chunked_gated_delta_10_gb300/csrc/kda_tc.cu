@@ -1215,15 +1215,31 @@ cudaError_t set_smem(F* f, int bytes) {
 bool tc_path_ok(const Prob& p, bool bf16) { return bf16 && p.K == D && p.V == D; }
 
 // Dense batches whose (sequence, value head) sweeps cannot fill the GPU and whose sequences are long
-// run the state passes in segments: about 256 CTAs per pass (two per SM), at least 32 chunks each.
-// (Shorter sequences gain nothing: a segment step of the chain costs about as much as the chunk
-// steps it saves.)
+// run the state passes in segments of at least 32 chunks. (Shorter sequences gain nothing: a segment
+// step of the chain costs about as much as the chunk steps it saves.) The segment count M minimises a
+// pass's critical path in chunk steps: the "ends" launch (2 S M CTAs for S sweeps) and the checkpoint
+// launch (S M CTAs) each take ceil(CTAs / slots) waves of ceil(chunks / M) steps, slots = two CTAs per
+// SM; the combine chain adds about 2.5 chunk steps per segment.
 SegPlan seg_plan(const Prob& p) {
     SegPlan sp{0, 1};
     const int64_t sweeps = (int64_t)p.B * p.HV;
     if (p.cu || p.K != D || p.V != D || sweeps > 64 || p.NTs < 128) return sp;
-    int M = (int)(256 / sweeps);
-    M = M < 2 ? 2 : (M > p.NTs / 32 ? p.NTs / 32 : M);
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || nsm <= 0)
+        nsm = 152;
+    const int64_t slots = 2 * (int64_t)nsm;
+    int M = 2;
+    double best = 0.0;
+    for (int m = 2; m <= p.NTs / 32; ++m) {
+        const int64_t len = (p.NTs + m - 1) / m;
+        const double cost = (double)(((2 * sweeps * m + slots - 1) / slots + (sweeps * m + slots - 1) / slots) * len) +
+                            2.5 * m;
+        if (m == 2 || cost < best) {
+            best = cost;
+            M = m;
+        }
+    }
     sp.len = (p.NTs + M - 1) / M;
     sp.M = (p.NTs + sp.len - 1) / sp.len;
     return sp;
