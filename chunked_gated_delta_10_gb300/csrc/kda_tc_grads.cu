@@ -290,8 +290,9 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
         float* xt1 = reinterpret_cast<float*>(sm + GS::XT1);
         float* xdb = reinterpret_cast<float*>(sm + GS::XDB);
         const float* gt = reinterpret_cast<const float*>(sm + GS::GT);
-        // a wait on the producer's barrier `b`: per warp (a time-out is noticed at the next group barrier), or for
-        // the grouped instantiation as a group (a time-out leaves the loop at once)
+        // the wait for phase E: per warp (a time-out is noticed at the next group barrier), or for the grouped
+        // instantiation as a group, whose barrier orders the dbeta partials before their sum (per-warp waits
+        // there spill that instantiation)
         auto phase_wait = [&](uint64_t* b, uint32_t parity, int code) {
             if constexpr (GROUPED) return wait_group<kSimt>(b, parity, ws.status, code, fail);
             warp_wait(b, parity, ws.status, code, fail);
@@ -323,9 +324,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                         __float2bfloat16_rn(((xdb[tid] + xdb[64 + tid]) + (xdb[128 + tid] + xdb[192 + tid])) +
                                             ((xdb[256 + tid] + xdb[320 + tid]) + (xdb[384 + tid] + xdb[448 + tid])));
             };
-            // the item's inputs: each warp waits on its own (the cumsum's barrier below absorbs the warps' skew);
-            // with grouped value heads the CTA waits together (per-warp waits spill that instantiation)
-            if (!phase_wait(&bars[slot], (uint32_t)(i >> 1) & 1, 41)) break;
+            // the item's inputs: each warp waits on its own (the cumsum's barrier below absorbs the warps' skew)
+            warp_wait(&bars[slot], (uint32_t)(i >> 1) & 1, ws.status, 41, fail);
             // Gamma2 of channel d for this thread's 16 rows (the canonical order of tc_intra)
             float G2[16];
 #pragma unroll
@@ -458,7 +458,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 }
                 reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nb;
             }
-            if (!phase_wait(&bars[3], par, 43)) break;  // phase B complete
+            warp_wait(&bars[3], par, ws.status, 43, fail);  // phase B complete
             tc_fence_after();
             {  // epilogue B/D: dbeta (INV and Akk parts), dM row segments
                 if (q4 < 2) {  // INV part from PR^T row j (lanes 0..63 of an M = 128 accumulator), 16 columns
