@@ -93,11 +93,16 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
 // Persistent, one CTA per SM: 512 SIMT threads (warps 0..15) and one producer warp (warp 16).
 // The producer's lane 0 issues every TMA copy and tensor-core MMA; an MMA's issue runs only a
 // couple of instructions ahead of its execution, so the issuing thread is held for about the
-// length of a phase, and in a warp of its own it holds nobody else. The SIMT threads meet on
-// barrier 1 (group_sync<512>). Barriers between the two: inputs of an item (by item parity),
-// phase A / B / E MMAs complete, operands of phase B / phase E written, and the accumulators
-// of the final epilogue read (TMEM free): phase A of the next item then runs while the SIMT
-// threads finish the current one.
+// length of a phase, and in a warp of its own it holds nobody else. Mbarriers carry the hand-offs
+// between the two: inputs of an item (by item parity) and MMA phases A / B / E complete, which each
+// SIMT warp waits for on its own (phase A and, with grouped value heads, phase E as a group), and
+// operands of phase B / phase E written and the accumulators of the final epilogue read (TMEM free),
+// which each SIMT warp signals on its own once its part is done: phase A of the next item then runs
+// while the SIMT threads finish the current one. The SIMT threads meet on barrier 1
+// (group_sync<512>) three times per item: for the cumsum's quarter totals, with the phase-A wait (the
+// reference rows, and S_in / dS_out no longer read before the factor pass overwrites them), and for
+// dg's cross-quarter sums. A time-out of a per-warp wait sets the failure flag, which the next of
+// these barriers reads.
 // Channel-oriented work: thread (d = tid % 128, quarter = tid / 128) owns key channel d for chunk
 // rows 16 * quarter .. 16 * quarter + 15. Row-oriented work on M = 64 accumulators: row r =
 // 16 * (warp % 4) + lane (lane < 16), column quarter warp / 4. Every cross-thread sum is
