@@ -6,7 +6,7 @@ bf16 workload B=8, T=4096, H=HV=32, K=V=128, chunk 64 (seeded synthetic
 inputs; see kda_inputs.py). Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--pass bwd|fwd|bwd-states] [--workload NAME]
+                    [--pass bwd|fwd|bwd-states|bwd-saved|fwd-save|bwd-fused] [--workload NAME]
 
 * ``value``: device-timed tokens/s (inputs resident in HBM; K steps between
   CUDA events, barrier + synchronize on both sides, max over ranks). The
@@ -31,7 +31,9 @@ inputs; see kda_inputs.py). Prints one JSON line.
   ``kda_chunk_fwd`` call (o and ht) per step; ``bwd-states`` times the
   backward that consumes the fp32 chunk states a forward saved; ``bwd-saved``
   times ``kda_chunk_bwd_from_saved`` on the context ``kda_chunk_fwd_save``
-  kept (the states or context are produced once before the timed region).
+  kept (the states or context are produced once before the timed region);
+  ``bwd-fused`` times ``kda_chunk_bwd_fused`` (the step of ``bwd`` with the
+  reverse pass and the per-chunk gradients fused into one launch).
 * ``--workload``: one of the four bf16 workloads of kda_inputs.py (default
   the B=8 T=4096 H=HV=32 benchmark); the others (B=1 T=2048 H=16 with h0 and
   dht; 16 packed sequences of U[1,4096] tokens with h0; B=1 T=65536 with 16
@@ -66,7 +68,8 @@ METRIC = "KDA fwd-recompute+bwd tokens/s on 1 GB300 and % of roofline vs CPU ora
 METRICS = {"bwd": METRIC, "fwd": "KDA chunk forward (o, ht) tokens/s on 1 GB300",
            "bwd-states": "KDA backward from saved chunk states tokens/s on 1 GB300",
            "bwd-saved": "KDA backward from the forward's saved context tokens/s on 1 GB300",
-           "fwd-save": "KDA chunk forward (o, ht) keeping the backward's saved context tokens/s on 1 GB300"}
+           "fwd-save": "KDA chunk forward (o, ht) keeping the backward's saved context tokens/s on 1 GB300",
+           "bwd-fused": "KDA fwd-recompute+bwd with the fused reverse kernel tokens/s on 1 GB300"}
 UNIT = "tokens/s"
 
 # ----------------------------------------------------------------------------
@@ -146,6 +149,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
         return "hbm", nck * (3 * tcd + tcc + C * V * in_bytes + K * 4 + tdd + tcd), nck * (6 * C * K * V + 2 * C * C * V)
     if name == "tc_grads":
         b = nck * (per_in + C * V * in_bytes + 2 * tcd + 2 * tdd + tcc + K * 4) + s["io_out"]
+        return "hbm", b, s["flops"]
+    if name == "tc_rev_fused":  # tc_ds_rev's and tc_grads' inputs (dO, e^Gamma_C once) and outputs, no
+        # dS_out / d_delta round trip
+        b = nck * (per_in + C * V * in_bytes + 4 * tcd + tdd + 2 * tcc + K * 4) + s["io_out"]
         return "hbm", b, s["flops"]
     if name == "tc_fwd_out":  # w, INV diag(beta), V, K^, scale Q~, Aqk, e^Gamma_C in; o out (state on chip)
         return "hbm", nck * (4 * tcd + 2 * tcc + K * 4 + C * V * in_bytes), nck * (6 * C * K * V + 2 * C * C * V)
@@ -472,14 +479,16 @@ def gpu_arm(args):
                                               wsb, P(outs["dq"]), P(outs["dk"]), P(outs["dv"]), P(outs["dg"]),
                                               P(outs["dbeta"]), P(outs.get("dh0")), sptr)
         else:
-            rc = lib.kda_chunk_bwd(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
+            entry = lib.kda_chunk_bwd_fused if mode == "bwd-fused" else lib.kda_chunk_bwd
+            rc = entry(ctypes.byref(dims), P(inputs["q"]), P(inputs["k"]), P(inputs["v"]),
                                    P(inputs["g"]), P(inputs["beta"]), P(inputs.get("h0")), P(vl.cu), P(vl.idx),
                                    P(vl.off), P(inputs["do"]), P(inputs.get("dht")), P(states), P(outs["dq"]),
                                    P(outs["dk"]), P(outs["dv"]), P(outs["dg"]), P(outs["dbeta"]),
                                    P(outs.get("dh0")), P(ws), wsb, sptr)
         if rc != 0:
             raise kda.KdaError(rc, {"fwd": "kda_chunk_fwd", "fwd-save": "kda_chunk_fwd_save",
-                                    "bwd-saved": "kda_chunk_bwd_from_saved"}.get(mode, "kda_chunk_bwd"))
+                                    "bwd-saved": "kda_chunk_bwd_from_saved",
+                                    "bwd-fused": "kda_chunk_bwd_fused"}.get(mode, "kda_chunk_bwd"))
 
     for _ in range(args.warmup):
         step(x, out)
@@ -625,7 +634,7 @@ def main():
                     help="bwd: forward recompute + backward (the benchmark metric); fwd: forward only; "
                          "bwd-states: backward from the fp32 chunk states a forward saved; bwd-saved: backward "
                          "from the context kda_chunk_fwd_save kept (reverse pass and gradients only); fwd-save: "
-                         "the forward that keeps that context")
+                         "the forward that keeps that context; bwd-fused: bwd with the fused reverse kernel")
     ap.add_argument("--workload", default=WORKLOAD, choices=kda_inputs.WORKLOAD_ORDER,
                     help="the workload of the JSON line (default: the B=8 T=4096 H=HV=32 benchmark)")
     ap.add_argument("--seq-len", type=int, default=None,

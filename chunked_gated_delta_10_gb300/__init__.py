@@ -69,6 +69,8 @@ def load():
             lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(Dims)] + [_P] * 13 + [ctypes.c_size_t, _P]
             lib.kda_chunk_bwd.restype = ctypes.c_int
             lib.kda_chunk_bwd.argtypes = [ctypes.POINTER(Dims)] + [_P] * 19 + [ctypes.c_size_t, _P]
+            lib.kda_chunk_bwd_fused.restype = ctypes.c_int
+            lib.kda_chunk_bwd_fused.argtypes = [ctypes.POINTER(Dims)] + [_P] * 19 + [ctypes.c_size_t, _P]
             lib.kda_saved_bytes.restype = ctypes.c_size_t
             lib.kda_saved_bytes.argtypes = [ctypes.POINTER(Dims)]
             lib.kda_chunk_fwd_save.restype = ctypes.c_int
@@ -203,6 +205,17 @@ def chunk_bwd(q, k, v, g, beta, do, scale=None, h0=None, dht=None, cu_seqlens=No
 
     Returns a dict with dq, dk ([B,T,H,K]), dv, dg (fp32), dbeta and dh0
     (fp32, or None without h0). ``out`` may pass preallocated outputs."""
+    return _chunk_bwd("kda_chunk_bwd", q, k, v, g, beta, do, scale, h0, dht, cu_seqlens, states, ws, out)
+
+
+def chunk_bwd_fused(q, k, v, g, beta, do, scale=None, h0=None, dht=None, cu_seqlens=None, states=None, ws=None,
+                    out=None):
+    """As :func:`chunk_bwd` through ``kda_chunk_bwd_fused`` (the reverse pass and the per-chunk gradients in
+    one launch; bf16, K = V = 128, H == HV)."""
+    return _chunk_bwd("kda_chunk_bwd_fused", q, k, v, g, beta, do, scale, h0, dht, cu_seqlens, states, ws, out)
+
+
+def _chunk_bwd(entry, q, k, v, g, beta, do, scale, h0, dht, cu_seqlens, states, ws, out):
     lib = load()
     dt = q.dtype
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (beta, "beta"), (do, "do")):
@@ -219,10 +232,10 @@ def chunk_bwd(q, k, v, g, beta, do, scale=None, h0=None, dht=None, cu_seqlens=No
                    dg=torch.empty_like(g), dbeta=torch.empty_like(beta),
                    dh0=torch.empty_like(h0) if h0 is not None else None)
     ws = _workspace(dims, PASS_BWD, dev, ws)
-    _check(lib.kda_chunk_bwd(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
-                             _ptr(vl.cu), _ptr(vl.idx), _ptr(vl.off), _ptr(do), _ptr(dht), _ptr(states),
-                             _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
-                             _ptr(out.get("dh0")), _ptr(ws), ws.numel(), _stream()), "kda_chunk_bwd")
+    _check(getattr(lib, entry)(ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                _ptr(vl.cu), _ptr(vl.idx), _ptr(vl.off), _ptr(do), _ptr(dht), _ptr(states),
+                                _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                                _ptr(out["dbeta"]), _ptr(out.get("dh0")), _ptr(ws), ws.numel(), _stream()), entry)
     return out
 
 

@@ -311,11 +311,12 @@ extern "C" kda_status kda_chunk_fwd(const kda_dims* dims, const void* q, const v
     return KDA_OK;
 }
 
-extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, const void* v,
-                                    const float* g, const void* beta, const float* h0, const int64_t* cu_seqlens,
-                                    const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
-                                    const float* dht, const float* states, void* dq, void* dk, void* dv, float* dg,
-                                    void* dbeta, float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
+namespace {
+kda_status chunk_bwd(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                     const void* beta, const float* h0, const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                     const int64_t* chunk_off, const void* d_o, const float* dht, const float* states, void* dq,
+                     void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                     kda_stream_t stream, bool fused) {
     Prob p;
     kda_status s = check_common(dims, &p, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, ws, ws_bytes,
                                 KDA_PASS_BWD);
@@ -327,6 +328,7 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
         if (x && !aligned16(x)) return KDA_ERR_INVALID_ARG;
     const Layout L = layout(p, KDA_PASS_BWD, use_tc(dims, KDA_PASS_BWD));
     if (states && !L.tc) return KDA_ERR_UNSUPPORTED;  // saved states are consumed on the tensor-core path
+    if (fused && (!L.tc || p.HV != p.H)) return KDA_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     IO io;
     memset(&io, 0, sizeof(io));
@@ -336,11 +338,31 @@ extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const v
     if (e != cudaSuccess) return cuda_fail(e);
     begin_launches(st);
     if (L.tc)
-        e = tc_bwd(p, io, carve_tc(ws, L), st, 4);
+        e = tc_bwd(p, io, carve_tc(ws, L), st, 4, false, fused);
     else
         e = simt_bwd(p, dims->dtype == KDA_DTYPE_BF16, io, carve(ws, L), st);
     if (e != cudaSuccess) return cuda_fail(e);
     return KDA_OK;
+}
+}  // namespace
+
+extern "C" kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                    const float* g, const void* beta, const float* h0, const int64_t* cu_seqlens,
+                                    const int32_t* chunk_idx, const int64_t* chunk_off, const void* d_o,
+                                    const float* dht, const float* states, void* dq, void* dk, void* dv, float* dg,
+                                    void* dbeta, float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    return chunk_bwd(dims, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, d_o, dht, states, dq, dk, dv, dg,
+                     dbeta, dh0, ws, ws_bytes, stream, false);
+}
+
+extern "C" kda_status kda_chunk_bwd_fused(const kda_dims* dims, const void* q, const void* k, const void* v,
+                                          const float* g, const void* beta, const float* h0,
+                                          const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                                          const int64_t* chunk_off, const void* d_o, const float* dht,
+                                          const float* states, void* dq, void* dk, void* dv, float* dg, void* dbeta,
+                                          float* dh0, void* ws, size_t ws_bytes, kda_stream_t stream) {
+    return chunk_bwd(dims, q, k, v, g, beta, h0, cu_seqlens, chunk_idx, chunk_off, d_o, dht, states, dq, dk, dv, dg,
+                     dbeta, dh0, ws, ws_bytes, stream, true);
 }
 
 extern "C" size_t kda_saved_bytes(const kda_dims* dims) {

@@ -73,9 +73,15 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
 // 2: + state pass, or the load of io.states_in, 3: + reverse pass,
 // 4: + gradients). With from_saved, the workspace holds a saved context (the
 // forward's intra tiles, S_in and delta, written by tc_fwd into a backward-
-// layout workspace) and stages 1 and 2 are skipped.
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved = false);
+// layout workspace) and stages 1 and 2 are skipped. With fused, stages 3 and 4 run as one launch
+// (tc_rev_fused; equal key and value heads only).
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved = false,
+                   bool fused = false);
 // The per-chunk gradient stage (dq, dk summed over the value heads of a group in the same kernel).
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
+// The fused reverse: per (sequence, value head) a cluster of two CTAs, one running the reverse
+// state-gradient sweep and one the per-chunk gradients of its chunks, dS_out and d_delta passed
+// between them in shared memory (H == HV).
+cudaError_t tc_rev_fused(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 
 }  // namespace kda

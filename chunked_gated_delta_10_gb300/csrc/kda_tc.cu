@@ -1299,7 +1299,8 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved) {
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved,
+                   bool fused) {
     cudaError_t e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
@@ -1332,6 +1333,11 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
             k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, whole, tm_v);
             note_launch("tc_state_fwd", st);
         }
+    }
+    if (fused) {  // the reverse pass and the gradients in one launch (whole sweeps)
+        if (stages < 4) return cudaGetLastError();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        return tc_rev_fused(p, io, ws, st);
     }
     if (stages >= 3) {
         if (sp.len) {

@@ -70,6 +70,17 @@ struct GS {
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
+// Shared-memory map of the sweep CTA of a fused reverse pair: the chunk inputs K^, scale Q~, Aqk, dO, w,
+// e^Gamma_C, then two bf16 dS_out tiles and two d_delta tiles (by item parity: one is pushed to the
+// gradient CTA while the next is written). Barriers: [0] K^, Q~, Aqk, dO landed; [1] w, e^Gamma_C
+// landed; [2] MMA; [kFree] a gradient item finished (remote arrivals).
+struct RevF {
+    static constexpr int KH = 0, QS = TCD, AQK = 2 * TCD, DO = 2 * TCD + TCC, W = 3 * TCD + TCC, EGC = 4 * TCD + TCC;
+    static constexpr int S0 = EGC + 1024, DD0 = S0 + 2 * TDD, BARS = DD0 + 2 * TCD, END = BARS + 64;
+    static constexpr int kFree = 3;
+};
+static_assert(RevF::END <= GS::END, "the sweep CTA fits the gradient CTA's shared memory");
+
 struct GradMaps {
     CUtensorMap q, k, v, d_o, g;
 };
@@ -113,13 +124,13 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
 constexpr int kSimt = 512, kProducerWarp = kSimt / 32, kGradsThreads = kSimt + 32;
 
 // GROUPED: HV = G H with G > 1 (the G value heads of a key head each add to its dq and dk).
-template <bool GROUPED>
-__global__ void __launch_bounds__(kGradsThreads, 1)
-    k_tc_grads(Prob p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out, bf16* __restrict__ dk_out,
-               bf16* __restrict__ dv_out, float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws,
-               const __grid_constant__ GradMaps maps) {
-    extern __shared__ uint8_t smraw[];
-    uint8_t* sm = align1024(smraw);
+// FUSED: the gradient CTA of a fused reverse pair (below): items fw0, fw0 - HV, ..., wlo (the chunks of
+// one sweep, last first), with d_delta and dS_out pushed by the sweep CTA instead of loaded.
+template <bool GROUPED, bool FUSED>
+__device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
+                                           bf16* __restrict__ dk_out, bf16* __restrict__ dv_out,
+                                           float* __restrict__ dg_out, bf16* __restrict__ db_out, const TcWs& ws,
+                                           const GradMaps& maps, uint8_t* sm, int64_t fw0, int64_t wlo) {
     // [0, 1] inputs (by item parity); [2] phase A, [3] phase B, [4] phase E complete; operands
     // written: [8] of phase B's first part, [5] of its second part, [6] of phase E; [7] accumulators read
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);
@@ -133,10 +144,12 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     // groups b, b + grid, ..., each group's G items back to back, so that this CTA keeps their running
     // dq / dk sum
     auto next_w = [&](int64_t w) -> int64_t {
+        if (FUSED) return w - HV;
         return GROUPED ? ((w + 1) % G ? w + 1 : w + 1 + (int64_t)(gridDim.x - 1) * G) : w + gridDim.x;
     };
-    const int64_t w0 = GROUPED ? (int64_t)blockIdx.x * G : blockIdx.x;
+    const int64_t w0 = FUSED ? fw0 : GROUPED ? (int64_t)blockIdx.x * G : blockIdx.x;
     const int64_t total = p.NT * HV;
+    auto live = [&](int64_t w) { return FUSED ? w >= wlo : w < total; };
 
     if (tid == 0) {
         mbar_init(&bars[0], 4);  // four input groups per item
@@ -150,6 +163,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (FUSED) cluster_sync();  // the sweep CTA's barriers are initialised, and ours for its copies
     const uint32_t tmem = *tslot;
 
     if (warp == kProducerWarp) {
@@ -162,7 +176,8 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                     tma_load_3d(sm + GS::DO + x * TCD, &maps.d_o, 64 * x, n.hv, (int)n.r0, b);
                     tma_load_3d(sm + GS::V + x * TCD, &maps.v, 64 * x, n.hv, (int)n.r0, b);
                     bulk_load(sm + GS::DL + x * TCD, ws.vn + n.ch * TCD + x * (TCD / 2), TCD / 2, b);
-                    bulk_load(sm + GS::DDL + x * TCD, ws.dvn + n.ch * TCD + x * (TCD / 2), TCD / 2, b);
+                    if (!FUSED)  // (fused: pushed by the sweep CTA, counted on the same barrier)
+                        bulk_load(sm + GS::DDL + x * TCD, ws.dvn + n.ch * TCD + x * (TCD / 2), TCD / 2, b);
                 }
             };
             auto issue_qk = [&](const Item& n, uint64_t* b) {
@@ -179,12 +194,14 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             auto issue_e = [&](const Item& n, uint64_t* b, int slot) {  // S_in, dS_out, g, e^Gamma_C
                 mbar_expect_tx(b, 2 * TDD + kC * D * 4 + 512);
                 bulk_load(sm + GS::SIN, ws.sin + n.ch * TDD, TDD, b);
-                bulk_load(sm + GS::DSO, ws.dso + n.ch * TDD, TDD, b);
+                if (!FUSED) bulk_load(sm + GS::DSO, ws.dso + n.ch * TDD, TDD, b);
                 tma_load_3d(sm + GS::GT, &maps.g, 0, n.hv, (int)n.r0, b);
                 bulk_load(sm + GS::EGC + 512 * slot, ws.egc + n.ch * D, 512, b);
             };
             int64_t w = w0;
-            {
+            // (fused) the sweep CTA's barrier on which each finished item frees dS_out's and d_delta's regions
+            const uint32_t rev_free = FUSED ? peer_addr(S(RevF::BARS + 8 * RevF::kFree), 0) : 0u;
+            if (!FUSED || live(w)) {
                 const Item first = make_item(p, w, true);
                 issue_a(first, &bars[0]);
                 issue_qk(first, &bars[0]);
@@ -192,11 +209,11 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 issue_e(first, &bars[0], 0);
             }
             int i = 0;
-            for (; w < total; ++i, w = next_w(w)) {
+            for (; live(w); ++i, w = next_w(w)) {
                 const int slot = i & 1;
                 const uint32_t par = (uint32_t)i & 1;
                 const int64_t wn = next_w(w);
-                const bool has_next = wn < total;
+                const bool has_next = live(wn);
                 const Item nx = make_item(p, has_next ? wn : w, has_next);
                 uint64_t* nbar = &bars[slot ^ 1];
                 if (i > 0) {  // the last item's accumulators and q, k tiles are read: this item's q, k
@@ -279,8 +296,10 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
                 }
                 if (!pwait(&bars[4], par, 57)) break;
                 if (has_next) issue_e(nx, nbar, slot ^ 1);  // factor tiles, dN, dM, T are consumed
+                // (fused) the next item's dS_out and d_delta may land: their bytes are expected by now
+                if (FUSED && has_next) mbar_arrive_peer(rev_free);
             }
-            if (w < total) {  // a wait gave up: let copies already issued land before the block exits
+            if (live(w)) {  // a wait gave up: let copies already issued land before the block exits
                 const long long t0 = clock64();
                 while (clock64() - t0 < 2000000) {
                 }
@@ -308,12 +327,12 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
         const int rrow = 16 * q4 + lane;                // row of an M = 64 accumulator (lane < 16)
         const bool rv = lane < 16;
         int64_t w = w0;
-        if (tid < kC) {
+        if (tid < kC && (!FUSED || live(w))) {
             const Item first = make_item(p, w, true);
             float* sb = reinterpret_cast<float*>(sm + GS::BETA);
             sb[tid] = tid < first.c ? __bfloat162float(beta[(first.r0 + tid) * HV + first.hv]) : 0.f;
         }
-        for (int i = 0; w < total; ++i, w = next_w(w)) {
+        for (int i = 0; live(w); ++i, w = next_w(w)) {
             const int slot = i & 1;
             const uint32_t par = (uint32_t)i & 1;
             const Item cur = make_item(p, w, true);
@@ -457,7 +476,7 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
             if (lane == 0) mbar_arrive(&bars[5]);  // (all warps: operands of phase B are in place)
             if (tid < kC) {  // beta of the next item to its shared slot, while phase B runs
                 float nb = 0.f;
-                if (wn < total) {
+                if (live(wn)) {
                     const Item nx = make_item(p, wn, true);
                     if (tid < nx.c) nb = __bfloat162float(beta[(nx.r0 + tid) * HV + nx.hv]);
                 }
@@ -655,6 +674,212 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
+template <bool GROUPED>
+__global__ void __launch_bounds__(kGradsThreads, 1)
+    k_tc_grads(Prob p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out, bf16* __restrict__ dk_out,
+               bf16* __restrict__ dv_out, float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws,
+               const __grid_constant__ GradMaps maps) {
+    extern __shared__ uint8_t smraw[];
+    grads_body<GROUPED, false>(p, beta, dq_out, dk_out, dv_out, dg_out, db_out, ws, maps, align1024(smraw), 0, 0);
+}
+
+// The sweep CTA of a fused reverse pair: the reverse state-gradient pass of one (sequence, value head),
+// chunks last to first, on 512 threads: thread t owns dS row k = t % 128, columns 32 (t / 128) .. +31, in
+// fp32 registers. Per chunk, with dS the gradient of the state leaving it (dS_out):
+//   d_delta = Aqk^T dO + K^ dS,   dS <- e^Gamma_C dS + Q~s^T dO - w^T d_delta,
+// the arithmetic of the split reverse pass (tc_ds_rev) on the same operands, so the tiles are the same
+// bits. Instead of writing dS_out and d_delta to the workspace, it pushes their bf16 tiles into the
+// gradient CTA's input regions (the bytes count on that CTA's input barrier of the item); both pushes of
+// item i wait until the gradient CTA has finished item i - 1 (its arrival on barrier kFree), whose
+// factor tiles fill the dS_out region until then. That wait also means the push of item i - 1 has
+// landed, so its source tiles (the other parity's) may be rewritten by item i + 1.
+__device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict__ dht, float* __restrict__ dh0,
+                                         const TcWs& ws, const CUtensorMap* tm_do, int n, int hv, uint8_t* sm) {
+    constexpr int NR = kSimt;  // threads of the sweep
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + RevF::BARS);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+    int* fail = reinterpret_cast<int*>(tslot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k = tid & 127, vq = tid >> 7;
+    const int HV = p.HV;
+    int64_t bos, eos, c0;
+    seq_range(p, n, bos, eos, c0);
+    const int nts = (int)((eos - bos + kC - 1) / kC);
+    if (tid == 0) {
+        for (int x = 0; x < 4; ++x) mbar_init(&bars[x], 1);
+        fence_mbar_init();
+        *fail = 0;
+    }
+    if (warp == 0) tmem_alloc(tslot, 256);
+    float S[32];
+    {
+        const float* src = dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + 32 * vq : nullptr;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = src ? src[j] : 0.f;
+    }
+    auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
+    auto issue1 = [&](int it) {  // operands of the first MMA group: K^, Q~s, Aqk, dO
+        const int64_t ch = chunk(it);
+        mbar_expect_tx(&bars[0], 3 * TCD + TCC);
+        bulk_load(sm + RevF::KH, ws.kh + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + RevF::QS, ws.qs + ch * TCD, TCD, &bars[0]);
+        bulk_load(sm + RevF::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
+        const int row = (int)(bos + (int64_t)it * kC);
+        tma_load_3d(sm + RevF::DO, tm_do, 0, hv, row, &bars[0]);
+        tma_load_3d(sm + RevF::DO + TCD / 2, tm_do, 64, hv, row, &bars[0]);
+    };
+    auto issue2 = [&](int it) {  // w (second MMA group) and e^Gamma_C (state update)
+        const int64_t ch = chunk(it);
+        mbar_expect_tx(&bars[1], TCD + 512);
+        bulk_load(sm + RevF::W, ws.w + ch * TCD, TCD, &bars[1]);
+        bulk_load(sm + RevF::EGC, ws.egc + ch * D, 512, &bars[1]);
+    };
+    // the gradient CTA (rank 1): its dS_out and d_delta regions and its input barriers
+    const uint32_t pdso = peer_addr(smem_u32(sm + GS::DSO), 1), pddl = peer_addr(smem_u32(sm + GS::DDL), 1);
+    const uint32_t pbar = peer_addr(smem_u32(sm + GS::BARS), 1);
+    tc_fence_before();
+    group_sync<NR>();
+    tc_fence_after();
+    cluster_sync();  // both CTAs' barriers are initialised
+    const uint32_t tmem = *tslot;
+    const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
+    if (tid == 0 && nts > 0) {
+        issue1(nts - 1);
+        issue2(nts - 1);
+    }
+    uint32_t mph = 0;
+    int i = 0;
+    for (int it = nts - 1; it >= 0; --it, ++i) {
+        const uint32_t ph = (uint32_t)i & 1;
+        uint8_t* tS = sm + RevF::S0 + (i & 1) * TDD;   // bf16 dS_out: MMA operand and the pushed tile
+        uint8_t* tD = sm + RevF::DD0 + (i & 1) * TCD;  // bf16 d_delta
+        const uint32_t ibar = pbar + 8u * (uint32_t)(i & 1);  // the gradient CTA's input barrier of item i
+#pragma unroll
+        for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tS, k, 32 * vq + c8, D, S + c8);
+        fence_async_smem();
+        if (!wait_group<NR>(&bars[0], ph, ws.status, 61, fail)) break;
+        if (tid == 0) {
+            tc_fence_after();
+            // d_delta = Aqk^T dO + K^ dS (chunk rows on TMEM lanes, M = 64, N = 128)
+            const uint32_t ida = idesc_bf16(64, 128, true, true), idb = idesc_bf16(64, 128, false, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem, desc_mnmajor(smem_u32(sm + RevF::AQK), kC, ks),
+                         desc_mnmajor(smem_u32(sm + RevF::DO), kC, ks), ida, ks > 0);
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_bf16(tmem, desc_kmajor(smem_u32(sm + RevF::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
+                         1);
+            // dS accumulator = Q~s^T dO (M = 128, N = 128)
+            const uint32_t idc = idesc_bf16(128, 128, true, true);
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevF::QS), kC, ks),
+                         desc_mnmajor(smem_u32(sm + RevF::DO), kC, ks), idc, ks > 0);
+            mma_commit(&bars[2]);
+            if (i > 0 && !mbar_wait_cluster(&bars[RevF::kFree], (uint32_t)(i - 1) & 1, ws.status, 62))
+                *(volatile int*)fail = 1;  // (read after the next group barrier)
+            else
+                bulk_push(pdso, tS, TDD, ibar);
+        }
+        if (!wait_group<NR>(&bars[2], mph, ws.status, 63, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && it > 0) issue1(it - 1);  // the first group's operands are consumed
+        tc_fence_after();
+        {  // d_delta rows into tD: row r = 16 (warp % 4) + lane (lane < 16), columns 32 (warp / 4) .. +31
+            const int r = 16 * (warp & 3) + lane, cb = 32 * (warp >> 2);
+            float acc[32];
+            tmem_ld32(tmem + lq + cb, acc);
+            tmem_ld_wait();
+            if (lane < 16) {
+#pragma unroll
+                for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tD, r, cb + c8, kC, acc + c8);
+            }
+        }
+        tc_fence_before();
+        fence_async_smem();
+        if (!wait_group<NR>(&bars[1], ph, ws.status, 64, fail)) break;
+        if (tid == 0) {  // dS accumulator -= w^T d_delta
+            tc_fence_after();
+            const uint32_t id = idesc_neg_a(idesc_bf16(128, 128, true, true));
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevF::W), kC, ks), desc_mnmajor(smem_u32(tD), kC, ks),
+                         id, 1);
+            mma_commit(&bars[2]);
+            // the gradient CTA keeps d_delta's two 64-column halves TCD bytes apart
+            bulk_push(pddl, tD, TCD / 2, ibar);
+            bulk_push(pddl + TCD, tD + TCD / 2, TCD / 2, ibar);
+        }
+        const float e = reinterpret_cast<const float*>(sm + RevF::EGC)[k];
+        if (!wait_group<NR>(&bars[2], mph, ws.status, 65, fail)) break;
+        mph ^= 1;
+        if (tid == 0 && it > 0) issue2(it - 1);  // w and e^Gamma_C are consumed
+        tc_fence_after();
+        {
+            float acc[32];
+            tmem_ld32(tmem + lq + 128 + 32 * vq, acc);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float2 v = fma2(bc2(e), f2(S[j], S[j + 1]), f2(acc[j], acc[j + 1]));
+                S[j] = v.x, S[j + 1] = v.y;
+            }
+        }
+        tc_fence_before();
+    }
+    if (*(volatile int*)fail == 0) {
+        if (dh0) {
+            float* dst = dh0 + (((int64_t)n * HV + hv) * D + k) * D + 32 * vq;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dst[j] = S[j];
+        }
+    } else if (tid == 0) {  // a wait gave up: let copies already issued land before the pair exits
+        const long long t0 = clock64();
+        while (clock64() - t0 < 2000000) {
+        }
+    }
+    tc_fence_before();
+    group_sync<NR>();
+    if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+// Fused reverse (state-gradient sweep and per-chunk gradients in one launch, dS_out and d_delta kept on
+// chip): one cluster of two CTAs per (sequence, value head), on two SMs. CTA 0 runs the sweep (rev_role,
+// warps 0..15; warp 16 only meets the cluster barriers), CTA 1 the gradient work of the sweep's chunks in
+// the same order (grads_body), its dS_out and d_delta inputs pushed by CTA 0 into its shared memory.
+// Equal key and value heads only (the grouped sum of dq, dk runs across sweeps).
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGradsThreads, 1)
+    k_tc_rev_fused(Prob p, const float* __restrict__ dht, float* __restrict__ dh0, const bf16* __restrict__ beta,
+                   bf16* __restrict__ dq_out, bf16* __restrict__ dk_out, bf16* __restrict__ dv_out,
+                   float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t* sm = align1024(smraw);
+    const int sweep = (int)cluster_index();
+    const int hv = sweep % p.HV, n = sweep / p.HV;
+    if (cluster_rank() == 0) {
+        if (threadIdx.x < kSimt)
+            rev_role(p, dht, dh0, ws, &maps.d_o, n, hv, sm);
+        else
+            cluster_sync();  // (the pair's start barrier)
+    } else {
+        int64_t bos, eos, c0;
+        seq_range(p, n, bos, eos, c0);
+        const int64_t nts = (eos - bos + kC - 1) / kC;
+        grads_body<false, true>(p, beta, dq_out, dk_out, dv_out, dg_out, db_out, ws, maps, sm,
+                                (c0 + nts - 1) * p.HV + hv, c0 * p.HV + hv);
+    }
+    cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+}
+
+bool make_grad_maps(const Prob& p, const IO& io, GradMaps* m) {
+    memset(m, 0, sizeof(*m));
+    const int64_t rows = (int64_t)p.B * p.T;
+    if (rows == 0) return true;
+    const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
+    return make_tmap_bf16_3d(&m->q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) &&
+           make_tmap_bf16_3d(&m->k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) &&
+           make_tmap_bf16_3d(&m->v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) &&
+           make_tmap_bf16_3d(&m->d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC) &&
+           make_tmap_f32_3d(&m->g, io.g, D, p.HV, rows, D * 4, (uint64_t)p.HV * D * 4, D, 1, kC);
+}
+
 }  // namespace
 
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
@@ -664,14 +889,7 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
     const int64_t rows = (int64_t)p.B * p.T;
     if (p.NT == 0 || rows == 0) return cudaSuccess;
     GradMaps m;
-    memset(&m, 0, sizeof(m));
-    const uint64_t rq = (uint64_t)p.H * D * 2, rv = (uint64_t)p.HV * D * 2;
-    if (!make_tmap_bf16_3d(&m.q, io.q, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&m.k, io.k, D, p.H, rows, D * 2, rq, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&m.v, io.v, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
-        !make_tmap_bf16_3d(&m.d_o, io.d_o, D, p.HV, rows, D * 2, rv, 64, 1, kC) ||
-        !make_tmap_f32_3d(&m.g, io.g, D, p.HV, rows, D * 4, (uint64_t)p.HV * D * 4, D, 1, kC))
-        return cudaErrorInvalidValue;
+    if (!make_grad_maps(p, io, &m)) return cudaErrorInvalidValue;
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
@@ -685,6 +903,21 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
     kern<<<(unsigned)grid, kGradsThreads, kGradsSmem, st>>>(p, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk,
                                                             (bf16*)io.dv, io.dg, (bf16*)io.dbeta, ws, m);
     note_launch("tc_grads", st);
+    return cudaGetLastError();
+}
+
+cudaError_t tc_rev_fused(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(k_tc_rev_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
+    if (e != cudaSuccess) return e;
+    if (p.HV != p.H) return cudaErrorInvalidValue;
+    const int64_t sweeps = (int64_t)p.N * p.HV;
+    if (sweeps == 0) return cudaSuccess;
+    GradMaps m;
+    if (!make_grad_maps(p, io, &m)) return cudaErrorInvalidValue;
+    k_tc_rev_fused<<<(unsigned)(2 * sweeps), kGradsThreads, kGradsSmem, st>>>(
+        p, io.dht, io.dh0, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta,
+        ws, m);
+    note_launch("tc_rev_fused", st);
     return cudaGetLastError();
 }
 

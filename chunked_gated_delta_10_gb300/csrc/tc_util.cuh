@@ -281,6 +281,66 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ------------------------------------------------------------------ clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_index() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster; orders each thread's earlier accesses (and mbarrier inits
+// fenced by fence_mbar_init) before the other CTAs' later ones.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address in the shared memory of cluster CTA `rank` of the variable at this CTA's shared address `a`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// Bulk copy from this CTA's shared memory into another cluster CTA's (dst and its mbarrier as
+// peer_addr addresses; 16-byte aligned, size % 16 == 0). Completion is counted in bytes on that
+// mbarrier; nothing here tells when the source has been read.
+__device__ __forceinline__ void bulk_push(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+// Arrive on another cluster CTA's mbarrier (a peer_addr address), releasing this thread's earlier
+// accesses at cluster scope.
+__device__ __forceinline__ void mbar_arrive_peer(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mbar) : "memory");
+}
+// Bounded wait on this CTA's mbarrier whose arrivals come from other CTAs of the cluster (acquire at
+// cluster scope); on time-out writes `code` to *status and returns false.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status, int code) {
+    auto poll = [&]() {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        return done != 0;
+    };
+    if (poll()) return true;
+    const long long t0 = clock64();
+    while (!poll()) {
+        if (clock64() - t0 > kWaitCycles) {
+            if (status) *(volatile int*)status = code;
+            return false;
+        }
+    }
+    return true;
+}
+
 // Negated-A variant of the __nv_bfloat16 instruction descriptor.
 __host__ __device__ constexpr uint32_t idesc_neg_a(uint32_t id) { return id | (1u << 13); }
 

@@ -144,6 +144,28 @@ kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, con
                          size_t ws_bytes, kda_stream_t stream);
 
 /*
+ * Backward with a fused reverse pass: the same results as kda_chunk_bwd, bit
+ * for bit, with the reverse state-gradient sweep and the per-chunk gradients
+ * run as one launch in which the state gradient never leaves the chip (the
+ * structure of the FlashKDA backward (K2) page's kernel: one sweep per
+ * (sequence, head) over the chunks from last to first with dS resident in
+ * shared memory, the per-chunk gradient work inside the sweep).
+ * Per (sequence, value head) a cluster of two CTAs on two SMs: one carries dS
+ * in registers through the sweep, the other computes each chunk's dq, dk, dv,
+ * dbeta and dg; each chunk's dS_out and d_delta tiles pass from the first to
+ * the second through distributed shared memory instead of the workspace.
+ * Arguments, layouts, workspace and errors as kda_chunk_bwd, plus
+ * KDA_ERR_UNSUPPORTED off the tensor-core path (bf16, K = V = 128) or when
+ * HV != H. The split path (kda_chunk_bwd) is the faster one on the workloads
+ * measured here; this entry point is the alternative structure.
+ */
+kda_status kda_chunk_bwd_fused(const kda_dims* dims, const void* q, const void* k, const void* v, const float* g,
+                               const void* beta, const float* h0, const int64_t* cu_seqlens, const int32_t* chunk_idx,
+                               const int64_t* chunk_off, const void* d_o, const float* dht, const float* states,
+                               void* dq, void* dk, void* dv, float* dg, void* dbeta, float* dh0, void* ws,
+                               size_t ws_bytes, kda_stream_t stream);
+
+/*
  * Backward from a saved forward context (bf16 inputs with K = V = 128 only).
  *
  * The backward needs, per chunk, the WY factors (w, INV, INV diag(beta)), the
