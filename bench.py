@@ -165,11 +165,13 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 # B=2 case of the benchmark workload and scaled by chunk-heads; reported only while the kernel's
 # source file is unchanged since that capture (sha1 prefix).
 MEASURED_TRAFFIC = {
-    # captured at kda_tc_grads.cu 955f3edd3073; the file's later revision changes only comments
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "eb00d6af26c1",
-                 "bytes_per_chunk_head": (841.614336e6 + 303.004928e6) / 4096},
-    # captured at kda_tc.cu cef808f4f3f1; the file's later revision changes only host code (the segment plan)
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "90da6f912fde",
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
+                 "bytes_per_chunk_head": (841.637632e6 + 303.195904e6) / 4096},
+    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
+                     "bytes_per_chunk_head": (875.185152e6 + 309.354240e6) / 4096},
+    # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change only host code (the segment plan,
+    # the fused-reverse dispatch)
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "9b7a2244ee51",
                  "bytes_per_chunk_head": (269.066240e6 + 249.859328e6) / 4096},
 }
 

@@ -689,10 +689,10 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
 //   d_delta = Aqk^T dO + K^ dS,   dS <- e^Gamma_C dS + Q~s^T dO - w^T d_delta,
 // the arithmetic of the split reverse pass (tc_ds_rev) on the same operands, so the tiles are the same
 // bits. Instead of writing dS_out and d_delta to the workspace, it pushes their bf16 tiles into the
-// gradient CTA's input regions (the bytes count on that CTA's input barrier of the item); both pushes of
-// item i wait until the gradient CTA has finished item i - 1 (its arrival on barrier kFree), whose
-// factor tiles fill the dS_out region until then. That wait also means the push of item i - 1 has
-// landed, so its source tiles (the other parity's) may be rewritten by item i + 1.
+// gradient CTA's input regions (the bytes count on that CTA's input barrier of the item). Item i's two
+// tiles are formed first; their pushes then wait until the gradient CTA has finished item i - 1 (its
+// arrival on barrier kFree), whose factor tiles fill the dS_out region until then. That wait also means the push of item i - 1 has landed, so its source tiles (the other
+// parity's) may be rewritten by item i + 1.
 __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict__ dht, float* __restrict__ dh0,
                                          const TcWs& ws, const CUtensorMap* tm_do, int n, int hv, uint8_t* sm) {
     constexpr int NR = kSimt;  // threads of the sweep
@@ -774,10 +774,6 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
                 mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevF::QS), kC, ks),
                          desc_mnmajor(smem_u32(sm + RevF::DO), kC, ks), idc, ks > 0);
             mma_commit(&bars[2]);
-            if (i > 0 && !mbar_wait_cluster(&bars[RevF::kFree], (uint32_t)(i - 1) & 1, ws.status, 62))
-                *(volatile int*)fail = 1;  // (read after the next group barrier)
-            else
-                bulk_push(pdso, tS, TDD, ibar);
         }
         if (!wait_group<NR>(&bars[2], mph, ws.status, 63, fail)) break;
         mph ^= 1;
@@ -803,9 +799,15 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
                 mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevF::W), kC, ks), desc_mnmajor(smem_u32(tD), kC, ks),
                          id, 1);
             mma_commit(&bars[2]);
-            // the gradient CTA keeps d_delta's two 64-column halves TCD bytes apart
-            bulk_push(pddl, tD, TCD / 2, ibar);
-            bulk_push(pddl + TCD, tD + TCD / 2, TCD / 2, ibar);
+            // both tiles of item i, as soon as the gradient CTA has finished item i - 1; the gradient CTA
+            // keeps d_delta's two 64-column halves TCD bytes apart
+            if (i > 0 && !mbar_wait_cluster(&bars[RevF::kFree], (uint32_t)(i - 1) & 1, ws.status, 62)) {
+                *(volatile int*)fail = 1;  // (read after the next group barrier)
+            } else {
+                bulk_push(pdso, tS, TDD, ibar);
+                bulk_push(pddl, tD, TCD / 2, ibar);
+                bulk_push(pddl + TCD, tD + TCD / 2, TCD / 2, ibar);
+            }
         }
         const float e = reinterpret_cast<const float*>(sm + RevF::EGC)[k];
         if (!wait_group<NR>(&bars[2], mph, ws.status, 65, fail)) break;
