@@ -68,7 +68,7 @@ def test_workspace_bytes(lib):
     assert kda.workspace_bytes(d, 7) == 0
 
 
-def _bwd(lib, d, ws_bytes=None, **ptr):
+def _bwd(lib, d, ws_bytes=None, entry="kda_chunk_bwd", **ptr):
     p = dict(q=A, k=A, v=A, g=A, beta=A, h0=None, cu=None, idx=None, off=None, do=A, dht=None, states=None,
              dq=A, dk=A, dv=A, dg=A, db=A, dh0=None, ws=A)
     p.update(ptr)
@@ -76,8 +76,8 @@ def _bwd(lib, d, ws_bytes=None, **ptr):
         ws_bytes = kda.workspace_bytes(d, kda.PASS_BWD)
     args = [p[n] for n in ("q", "k", "v", "g", "beta", "h0", "cu", "idx", "off", "do", "dht", "states", "dq", "dk",
                            "dv", "dg", "db", "dh0", "ws")]
-    return lib.kda_chunk_bwd(ctypes.byref(d), *[None if a is None else ctypes.c_void_p(a) for a in args],
-                             ws_bytes, None)
+    return getattr(lib, entry)(ctypes.byref(d), *[None if a is None else ctypes.c_void_p(a) for a in args],
+                               ws_bytes, None)
 
 
 def test_bwd_rejects_invalid_arguments_before_launch(lib):
@@ -94,6 +94,20 @@ def test_bwd_rejects_invalid_arguments_before_launch(lib):
     assert _bwd(lib, d, dh0=A) == 1                        # dh0 without h0
     assert _bwd(lib, d, cu=A) == 1                         # cu_seqlens without chunk table
     assert _bwd(lib, d, cu=A, idx=A, off=A) == 1           # packed sequences need B == 1
+
+
+def test_fused_reverse_rejects_before_launch(lib):
+    """kda_chunk_bwd_fused checks its arguments as kda_chunk_bwd does, and refuses, before any CUDA call,
+    the cases it does not cover: the fp32 path (K = 64, or fp32 inputs) and grouped value heads."""
+    fused = dict(entry="kda_chunk_bwd_fused")
+    assert lib.kda_chunk_bwd_fused(None, *([None] * 19), 0, None) == 1
+    assert _bwd(lib, _dims(HV=2), **fused) == 2                         # bf16 with K = 64: the fp32 path
+    assert _bwd(lib, _dims(dtype=1, K=128, V=128, HV=2), **fused) == 2  # fp32 inputs
+    assert _bwd(lib, _dims(K=128, V=128, HV=4), **fused) == 2           # grouped value heads (H = 2)
+    d = _dims(K=128, V=128, HV=2)
+    assert _bwd(lib, d, q=A + 8, **fused) == 1                          # misaligned
+    assert _bwd(lib, d, ws_bytes=16, **fused) == 3                      # workspace too small
+    assert _bwd(lib, d, dh0=A, **fused) == 1                            # dh0 without h0
 
 
 def test_binding_requires_built_library(monkeypatch, tmp_path):
