@@ -183,7 +183,9 @@ kda_status check_common(const kda_dims* dims, Prob* p, const void* q, const void
     kda_status s = check_dims(dims, p);
     if (s != KDA_OK) return s;
     const bool packed = cu != nullptr;
-    if (packed != (cidx != nullptr) || packed != (coff != nullptr)) return KDA_ERR_INVALID_ARG;
+    // (a packed batch of empty sequences has no chunk table to pass: chunk_idx may then be NULL)
+    if (packed != (coff != nullptr) || (!packed && cidx) || (packed && !cidx && dims->num_chunks > 0))
+        return KDA_ERR_INVALID_ARG;
     if (packed) {
         if (dims->B != 1) return KDA_ERR_INVALID_ARG;
     } else {

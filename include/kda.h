@@ -37,7 +37,8 @@
  *       h0, ht, dht, dh0   [N, HV, K, V]   fp32
  *       states             [num_chunks, HV, K, V] fp32: S entering each chunk
  *       cu_seqlens         int64 [N + 1]   (packed sequences; then B == 1)
- *       chunk_idx          int32 [num_chunks][2] = (sequence, chunk in seq)
+ *       chunk_idx          int32 [num_chunks][2] = (sequence, chunk in seq);
+ *                          may be NULL when num_chunks == 0
  *       chunk_off          int64 [N + 1]   first global chunk of each sequence
  *   - Value head hv reads key head hv / (HV / H).
  */
@@ -112,7 +113,8 @@ size_t kda_workspace_bytes(const kda_dims* dims, int32_t pass);
  * Chunked forward: o, the final state ht and the state entering every chunk.
  *   q, k, v, g, beta (and optional h0) as in the layouts above.
  *   cu_seqlens, chunk_idx, chunk_off: all NULL (B equal-length sequences) or
- *     all non-NULL device arrays (packed sequences, B == 1).
+ *     all non-NULL device arrays (packed sequences, B == 1); chunk_idx may be
+ *     NULL for a packed batch with no chunk (every sequence empty).
  *   o: required. ht, states: nullable (skipped when NULL).
  *   ws / ws_bytes: device workspace of at least kda_workspace_bytes(FWD).
  * Errors: KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE before

@@ -271,6 +271,26 @@ def test_grouped_value_heads_tensor_core(kda, name):
     compare_full(inp, out, oracle.run_inputs(inp))
 
 
+@pytest.mark.parametrize("dtype,K", [("f32", 64), ("bf16", 128)])
+def test_packed_batch_of_empty_sequences(kda, dtype, K):
+    """Packed sequences that are all empty own no chunk (chunk_idx is an empty array): the forward returns
+    ht = h0 and the backward dh0 = dht exactly (the identity of a sequence with no token), on both paths and,
+    for the tensor-core shape, through the fused reverse too."""
+    inp = kda_inputs.small(seed=51, B=1, T=0, H=2, HV=2, K=K, V=K, dtype=dtype, seq_lens=[0, 0, 0])
+    o, ht, st = gpu_fwd(kda, inp)
+    assert o.numel() == 0 and st.numel() == 0
+    assert torch.equal(ht.cpu(), inp.h0)
+    outs = [gpu_bwd(kda, inp)]
+    if dtype == "bf16":
+        x = _cuda(inp)
+        outs.append(kda.chunk_bwd_fused(x["q"], x["k"], x["v"], x["g"], x["beta"], x["do"], scale=inp.scale,
+                                        h0=x["h0"], dht=x["dht"], cu_seqlens=inp.cu_seqlens))
+        torch.cuda.synchronize()
+    for out in outs:
+        assert torch.equal(out["dh0"].cpu(), inp.dht)
+        assert all(out[key].numel() == 0 for key in ("dq", "dk", "dv", "dg", "dbeta"))
+
+
 # ------------------------------------------------------- the five workloads
 
 @functools.lru_cache(maxsize=1)
