@@ -145,6 +145,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
         return "hbm", b, f
     if name == "tc_state_fwd":  # w, INV diag(beta), V, K^, e^Gamma_C in; S_in, delta out
         return "hbm", nck * (3 * tcd + tcc + K * 4 + tdd + tcd), nck * 4 * C * K * V
+    if name == "tc_state_both":  # tc_state_fwd and tc_ds_rev in one launch
+        sf, sr = kernel_cost("tc_state_fwd", B, T, H, HV, K, V, in_bytes, C, nck), kernel_cost(
+            "tc_ds_rev", B, T, H, HV, K, V, in_bytes, C, nck)
+        return "hbm", sf[1] + sr[1], sf[2] + sr[2]
     if name == "tc_ds_rev":
         return "hbm", nck * (3 * tcd + tcc + C * V * in_bytes + K * 4 + tdd + tcd), nck * (6 * C * K * V + 2 * C * C * V)
     if name == "tc_grads":
@@ -163,15 +167,16 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 
 # DRAM traffic per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) on the
 # B=2 case of the benchmark workload and scaled by chunk-heads; reported only while the kernel's
-# source file is unchanged since that capture (sha1 prefix).
+# source file is the revision named (sha1 prefix): the captured one, or a later one that leaves
+# that kernel's code as it was (the entry says so).
 MEASURED_TRAFFIC = {
     "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
                  "bytes_per_chunk_head": (841.637632e6 + 303.195904e6) / 4096},
     "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
                      "bytes_per_chunk_head": (875.185152e6 + 309.354240e6) / 4096},
-    # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change only host code (the segment plan,
-    # the fused-reverse dispatch)
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "9b7a2244ee51",
+    # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change host code (the segment plan, the
+    # launch choices) and the two state passes' kernels, not tc_intra
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "3c5d175eeee0",
                  "bytes_per_chunk_head": (269.066240e6 + 249.859328e6) / 4096},
 }
 

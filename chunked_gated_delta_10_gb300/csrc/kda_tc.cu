@@ -458,10 +458,10 @@ struct FwdSm {
 };
 constexpr int kFwdSmem = 1024 + FwdSm::END;
 
-__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg,
-                                                          const __grid_constant__ CUtensorMap tm_v) {
-    extern __shared__ uint8_t smraw[];
-    uint8_t* sm = align1024(smraw);
+// (sequence n, value head hv, grid z: the segment, or for kSegEnds segment and mode)
+__device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __restrict__ h0, const TcWs& ws,
+                                               const SegArg& sg, const CUtensorMap& tm_v, uint8_t* sm, int hv, int n,
+                                               int z) {
     uint8_t* tS = sm + FwdSm::S;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FwdSm::BARS);  // u[2], w, K^, mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
@@ -469,13 +469,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int k = tid & 127, vh = tid >> 7;
-    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
+    const int HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
     // segment and mode: 0 checkpoints, 1 end state from zero, 2 transition
-    const int m = sg.mode == kSegEnds ? (int)blockIdx.z % sg.M : (int)blockIdx.z;
-    const int mode = sg.mode == kSegEnds ? 1 + (int)blockIdx.z / sg.M : 0;
+    const int m = sg.mode == kSegEnds ? z % sg.M : z;
+    const int mode = sg.mode == kSegEnds ? 1 + z / sg.M : 0;
     const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
     if (sg.len && lo >= hi) return;
     const bool ckpt = mode == 0, with_u = mode != 2;
@@ -623,6 +623,12 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     if (warp == 0) tmem_dealloc(tmem, 256);
 }
 
+__global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg,
+                                                          const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ uint8_t smraw[];
+    state_fwd_body(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
 // ---------------------------------------------------------------------------
 // tc_seg_combine: start states of the segments of one (sequence, value head),
 // fp32: S_start(first) = init (h0 or dht, or zero), S_start(next) = P S_start + E
@@ -738,10 +744,10 @@ struct RevSm {
 };
 constexpr int kRevSmem = 1024 + RevSm::END;
 
-__global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
-                                                       TcWs ws, const __grid_constant__ CUtensorMap tm_do, SegArg sg) {
-    extern __shared__ uint8_t smraw[];
-    uint8_t* sm = align1024(smraw);
+// (sequence n, value head hv, grid z as in state_fwd_body)
+__device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restrict__ dht, float* __restrict__ dh0,
+                                            const TcWs& ws, const CUtensorMap& tm_do, const SegArg& sg, uint8_t* sm,
+                                            int hv, int n, int z) {
     uint8_t* tS = sm + RevSm::S;  // bf16 dS (128 x 128), later dDelta (64 x 128)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + RevSm::BARS);  // group 1, group 2, mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
@@ -749,13 +755,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int k = tid & 127, vh = tid >> 7;
-    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
+    const int HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
     // segment and mode: 0 checkpoints, 1 end state from zero, 2 transition (dO taken as zero)
-    const int m = sg.mode == kSegEnds ? (int)blockIdx.z % sg.M : (int)blockIdx.z;
-    const int mode = sg.mode == kSegEnds ? 1 + (int)blockIdx.z / sg.M : 0;
+    const int m = sg.mode == kSegEnds ? z % sg.M : z;
+    const int mode = sg.mode == kSegEnds ? 1 + z / sg.M : 0;
     const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
     if (sg.len && lo >= hi) return;
     const bool ckpt = mode == 0, with_do = mode != 2;
@@ -900,6 +906,28 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+__global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
+                                                       TcWs ws, const __grid_constant__ CUtensorMap tm_do, SegArg sg) {
+    extern __shared__ uint8_t smraw[];
+    ds_rev_body(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z);
+}
+
+// The forward state pass and the reverse state-gradient pass, whole sweeps, in one launch: grid z = 0 runs
+// tc_state_fwd's sweep of (sequence, value head), z = 1 tc_ds_rev's. The reverse pass reads only the
+// intra-chunk tiles and dO (not S_in nor delta), so the two sweeps are independent and, when all their
+// CTAs are resident at once, run side by side instead of one after the other.
+constexpr int kBothSmem = kFwdSmem > kRevSmem ? kFwdSmem : kRevSmem;
+__global__ void __launch_bounds__(256, 2)
+    k_tc_state_both(Prob p, const float* __restrict__ h0, const float* __restrict__ dht, float* __restrict__ dh0,
+                    TcWs ws, const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do) {
+    extern __shared__ uint8_t smraw[];
+    const SegArg whole{0, 1, kSegNone};
+    if (blockIdx.z == 0)
+        state_fwd_body(p, h0, ws, whole, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, 0);
+    else
+        ds_rev_body(p, dht, dh0, ws, tm_do, whole, align1024(smraw), blockIdx.x, blockIdx.y, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1305,6 +1333,7 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_ds_rev, kRevSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_both, kBothSmem)) != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.B * p.T;
     CUtensorMap tm_do;
     memset(&tm_do, 0, sizeof(tm_do));
@@ -1316,6 +1345,20 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if (stages >= 1 && !from_saved && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     const SegPlan sp = seg_plan(p);
     const SegArg ends{sp.len, sp.M, kSegEnds}, ckpt{sp.len, sp.M, kSegCkpt}, whole{0, 1, kSegNone};
+    // the two state passes side by side when each has at most one sweep per SM (both fit at two CTAs per SM)
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const bool both = stages >= 3 && !fused && !from_saved && !io.states_in && !sp.len && (int64_t)p.N * p.HV <= nsm;
+    if (both) {
+        k_tc_state_both<<<dim3(p.HV, p.N, 2), 256, kBothSmem, st>>>(p, io.h0, io.dht, io.dh0, ws, tm_v, tm_do);
+        note_launch("tc_state_both", st);
+        if (stages >= 4) {
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            return tc_grads(p, io, ws, st);
+        }
+        return cudaGetLastError();
+    }
     if (stages >= 2 && !from_saved) {
         if (io.states_in) {  // the forward's saved states: no sequential recompute
             if (p.NT > 0) {

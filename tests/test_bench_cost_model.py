@@ -44,3 +44,7 @@ def test_forward_and_state_load_bytes():
     assert _kb_per_chunk_head("tc_fwd_out") == 4 * 16 + 2 * 8 + 0.5 + 16
     # tc_state_load: the fp32 state 64 KB, w, V 16 KB each, INV diag(beta) 8 KB in; S_in 32 KB, delta 16 KB out
     assert _kb_per_chunk_head("tc_state_load") == 64 + 2 * 16 + 8 + 32 + 16
+
+
+def test_merged_state_passes_bytes():
+    assert _kb_per_chunk_head("tc_state_both") == _kb_per_chunk_head("tc_state_fwd") + _kb_per_chunk_head("tc_ds_rev")

@@ -49,8 +49,11 @@ def _workspace(kda, inp):
 
 
 def _check_bitwise(kda, inp, reps=2):
-    """The fused path, twice on one workspace, equals the split path bit for bit; clean status word."""
+    """The fused path, twice on one workspace, equals the split path bit for bit; clean status word.
+    (With at most one (sequence, head) sweep per SM the split path runs its two state passes as one launch,
+    tc_state_both; the fused path runs tc_state_fwd on its own.)"""
     split = gpu_bwd(kda, inp)
+    split_names = _launches(kda)
     ws = _workspace(kda, inp)
     for rep in range(reps):
         got = fused_bwd(kda, inp, ws=ws)
@@ -62,7 +65,7 @@ def _check_bitwise(kda, inp, reps=2):
                 assert got[key] is None, key
             else:
                 assert torch.equal(split[key], got[key]), (rep, key)
-    return got
+    return got, split_names
 
 
 FUSED = {
@@ -78,14 +81,14 @@ FUSED = {
 @pytest.mark.parametrize("name", list(FUSED))
 def test_fused_reverse_bitwise_and_oracle(kda, name):
     inp = kda_inputs.small(seed=47, dtype="bf16", **FUSED[name])
-    got = _check_bitwise(kda, inp)
+    got, _ = _check_bitwise(kda, inp)
     print(name, compare_full(inp, got, oracle.run_inputs(inp)))
 
 
 def test_fused_reverse_long_sequence(kda):
     """129 chunks in one sweep, after a segmented forward state pass."""
     inp = kda_inputs.small(seed=48, B=1, T=8192 + 37, H=1, HV=1, K=128, V=128, dtype="bf16")
-    got = _check_bitwise(kda, inp, reps=1)
+    got, _ = _check_bitwise(kda, inp, reps=1)
     print("long", compare_full(inp, got, oracle.run_inputs(inp)))
 
 
@@ -114,7 +117,10 @@ def test_fused_reverse_workloads_bitwise(kda, name):
     """The workloads with equal key and value heads, in the launch configuration the benchmark times:
     bit for bit the split path's gradients (whose whole-tensor oracle parity the parity tests check)."""
     inp = _workload(name)
-    got = _check_bitwise(kda, inp, reps=1)
+    got, split_names = _check_bitwise(kda, inp, reps=1)
+    side_by_side = name == "bf16_b1_t2048_h16_k128"  # 16 sweeps; the others have 256 and 512
+    assert (b"tc_state_both" in split_names) == side_by_side, split_names
+    assert (b"tc_ds_rev" in split_names) != side_by_side, split_names
     if name == "bf16_b1_t2048_h16_k128":
         print(name, compare_full(inp, {k: (None if v is None else v.cpu()) for k, v in got.items()},
                                  oracle.run_inputs(inp)))
