@@ -26,6 +26,9 @@
 //                 dDelta = Aqk^T dO + K^ dS,
 //                 dS <- e^(Gamma_C) dS + Q~s^T dO - w^T dDelta; writes dS_out,
 //                 dDelta and dh0.
+//   tc_state_both the two sweeps above in one launch (they are independent: the
+//                 reverse pass reads neither S_in nor delta), used when each
+//                 pass has at most one (sequence, value head) sweep per SM.
 //   tc_seg_combine   chains segment start states (long sequences).
 //   tc_state_load the backward's state pass from the forward's saved states.
 //   tc_fwd_out    the forward: the state pass with o = (scale Q~) S + Aqk
