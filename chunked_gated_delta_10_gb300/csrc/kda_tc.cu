@@ -461,17 +461,23 @@ struct FwdSm {
 };
 constexpr int kFwdSmem = 1024 + FwdSm::END;
 
-// (sequence n, value head hv, grid z: the segment, or for kSegEnds segment and mode)
+// (sequence n, value head hv, grid z: the segment, or for kSegEnds segment and mode.) The state's columns
+// evolve independently (delta's column v takes only S's column v), so a sweep may be split by columns: NH
+// = 2 runs all 128 on this CTA (thread = row k, 64 columns); NH = 1 runs the 64 columns of half h (thread
+// = row k, 32 columns), with narrower MMAs, for batches whose sweeps leave SMs idle.
+template <int NH>
 __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __restrict__ h0, const TcWs& ws,
                                                const SegArg& sg, const CUtensorMap& tm_v, uint8_t* sm, int hv, int n,
-                                               int z) {
-    uint8_t* tS = sm + FwdSm::S;
+                                               int z, int h) {
+    constexpr int CW = 64 * NH, TW = CW / 2;  // state columns of this CTA and of each thread
+    uint8_t* tS = sm + FwdSm::S;              // bf16 copy of S (128 x CW)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FwdSm::BARS);  // u[2], w, K^, mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k = tid & 127, vh = tid >> 7;
+    const int k = tid & 127, vq = tid >> 7;
+    const int cbase = 64 * h + TW * vq;  // this thread's first state column
     const int HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
@@ -488,25 +494,24 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
         fence_mbar_init();
         *fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
-    float S[64];
-    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
+    if (warp == 0) tmem_alloc(tslot, 2 * CW);  // delta [0, CW), state [CW, 2 CW)
+    float S[TW];
+    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + cbase;
     {
         const float* src = nullptr;
-        if (mode == 0) src = (lo == 0) ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
+        if (mode == 0) src = (lo == 0) ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + cbase : nullptr)
                                        : ws.seg_s0 + seg_at;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : (mode == 2 && 64 * vh + j == k ? 1.f : 0.f);
+        for (int j = 0; j < TW; ++j) S[j] = src ? src[j] : (mode == 2 && cbase + j == k ? 1.f : 0.f);
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
-    auto issue_u = [&](int it) {  // V rows of chunk it (TMA) and e^Gamma_C
+    auto issue_u = [&](int it) {  // V rows of chunk it (TMA; this CTA's columns) and e^Gamma_C
         const int b = (it - lo) & 1;
         uint8_t* buf = sm + FwdSm::U + b * FwdSm::UBUF;
-        mbar_expect_tx(&bars[b], (with_u ? TCD : 0) + 512);
+        mbar_expect_tx(&bars[b], (with_u ? NH * (TCD / 2) : 0) + 512);
         if (with_u) {
             const int row = (int)(bos + (int64_t)it * kC);
-            tma_load_3d(buf, &tm_v, 0, hv, row, &bars[b]);
-            tma_load_3d(buf + TCD / 2, &tm_v, 64, hv, row, &bars[b]);
+            for (int x = 0; x < NH; ++x) tma_load_3d(buf + x * (TCD / 2), &tm_v, 64 * (h + x), hv, row, &bars[b]);
         }
         bulk_load(buf + TCD, ws.egc + chunk(it) * D, 512, &bars[b]);
     };
@@ -536,15 +541,15 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
         const int rel = it - lo;
         const uint32_t ph = (uint32_t)rel & 1;  // phase of the single-buffered w and K^ barriers
         uint8_t* tU = sm + FwdSm::U + (rel & 1) * FwdSm::UBUF;
-        // bf16 copy of S (row k, this thread's 64 columns) for the MMAs and the S_in checkpoint
+        // bf16 copy of S (row k, this thread's columns) for the MMAs and the S_in checkpoint
 #pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
+        for (int c8 = 0; c8 < TW; c8 += 8) st_tile_row8(tS, k, TW * vq + c8, D, S + c8);
         fence_async_smem();
         // w, INVb and V (both prefetched) in one wait
         if (!wait_all2(&bars[2], ph, 21, &bars[rel & 1], (rel >> 1) & 1, 24, ws.status, fail)) break;
         const float e = reinterpret_cast<const float*>(tU + TCD)[k];  // e^Gamma_C of this thread's state row
-        // delta accumulator = -w S + INVb V (chunk rows on TMEM lanes, M = 64, N = 128)
-        const uint32_t idd = idesc_bf16(64, 128, false, true);
+        // delta accumulator = -w S + INVb V (chunk rows on TMEM lanes, M = 64, N = CW)
+        const uint32_t idd = idesc_bf16(64, CW, false, true);
         if (tid == 0) {
             tc_fence_after();
             for (int ks = 0; ks < D / 16; ++ks)
@@ -555,8 +560,8 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
                     mma_bf16(tmem, desc_kmajor(smem_u32(sm + FwdSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                              idd, 1);
             mma_commit(&bars[4]);
-            if (ckpt) {
-                bulk_store(ws.sin + ch * TDD, tS, TDD);
+            if (ckpt) {  // (column block h of the 128-row tile)
+                bulk_store(ws.sin + ch * TDD + h * (D * 128), tS, D * CW * 2);
                 bulk_commit();
             }
         }
@@ -565,31 +570,31 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
         mph ^= 1;
         if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w and INVb are consumed
         tc_fence_after();
-        {  // delta (bf16) in place of V: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
-            const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
+        {  // delta (bf16) in place of V: row r = 16 (warp % 4) + lane (lane < 16), CW / 2 columns per warp half
+            const int r = 16 * (warp & 3) + lane, cb = (CW / 2) * (warp >> 2);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int x = 0; x < CW / 64; ++x) {
                 float acc[32];
-                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld32(tmem + lq + cb + 32 * x, acc);
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * h + c8, kC, acc + c8);
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * x + c8, kC, acc + c8);
                 }
             }
         }
         tc_fence_before();
         fence_async_smem();
         if (!wait_all(&bars[3], ph, ws.status, 25, fail)) break;
-        if (tid == 0) {  // S accumulator = K^^T delta (M = 128, N = 128)
+        if (tid == 0) {  // S accumulator = K^^T delta (M = 128, N = CW)
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 128, true, true);
+            const uint32_t id = idesc_bf16(128, CW, true, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + FwdSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
+                mma_bf16(tmem + CW, desc_mnmajor(smem_u32(sm + FwdSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          id, ks > 0);
             mma_commit(&bars[4]);
-            if (ckpt) {
-                bulk_store(ws.vn + ch * TCD, tU, TCD);
+            if (ckpt) {  // (column block h of the 64-row tile)
+                bulk_store(ws.vn + ch * TCD + h * (kC * 128), tU, kC * CW * 2);
                 bulk_commit();
             }
         }
@@ -603,14 +608,14 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
         }
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int x = 0; x < TW / 32; ++x) {
             float acc[32];
-            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+            tmem_ld32(tmem + lq + CW + TW * vq + 32 * x, acc);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float2 v = fma2(bc2(e), f2(S[32 * h + j], S[32 * h + j + 1]), f2(acc[j], acc[j + 1]));
-                S[32 * h + j] = v.x, S[32 * h + j + 1] = v.y;
+                const float2 v = fma2(bc2(e), f2(S[32 * x + j], S[32 * x + j + 1]), f2(acc[j], acc[j + 1]));
+                S[32 * x + j] = v.x, S[32 * x + j + 1] = v.y;
             }
         }
         tc_fence_before();
@@ -618,18 +623,18 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
     if (mode != 0 && *(volatile int*)fail == 0) {
         float* dst = (mode == 1 ? ws.seg_e : ws.seg_p) + seg_at;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[j] = S[j];
+        for (int j = 0; j < TW; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 2 * CW);
 }
 
 __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg,
                                                           const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
-    state_fwd_body(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z);
+    state_fwd_body<2>(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -747,17 +752,21 @@ struct RevSm {
 };
 constexpr int kRevSmem = 1024 + RevSm::END;
 
-// (sequence n, value head hv, grid z as in state_fwd_body)
+// (sequence n, value head hv, grid z as in state_fwd_body.) The columns of dS evolve independently as well
+// (dDelta's column v takes only dS's and dO's column v): NH as in state_fwd_body.
+template <int NH>
 __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restrict__ dht, float* __restrict__ dh0,
                                             const TcWs& ws, const CUtensorMap& tm_do, const SegArg& sg, uint8_t* sm,
-                                            int hv, int n, int z) {
-    uint8_t* tS = sm + RevSm::S;  // bf16 dS (128 x 128), later dDelta (64 x 128)
+                                            int hv, int n, int z, int h) {
+    constexpr int CW = 64 * NH, TW = CW / 2;  // dS columns of this CTA and of each thread
+    uint8_t* tS = sm + RevSm::S;              // bf16 dS (128 x CW), later dDelta (64 x CW)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + RevSm::BARS);  // group 1, group 2, mma
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 3);
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k = tid & 127, vh = tid >> 7;
+    const int k = tid & 127, vq = tid >> 7;
+    const int cbase = 64 * h + TW * vq;  // this thread's first dS column
     const int HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
@@ -774,27 +783,27 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
         fence_mbar_init();
         *fail = 0;
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
-    float S[64];
-    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
+    if (warp == 0) tmem_alloc(tslot, 2 * CW);  // dDelta [0, CW), dS [CW, 2 CW)
+    float S[TW];
+    const int64_t seg_at = (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + cbase;
     {
         const float* src = nullptr;
-        if (mode == 0) src = (hi == nts) ? (dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
+        if (mode == 0) src = (hi == nts) ? (dht ? dht + (((int64_t)n * HV + hv) * D + k) * D + cbase : nullptr)
                                          : ws.seg_s0 + seg_at;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : (mode == 2 && 64 * vh + j == k ? 1.f : 0.f);
+        for (int j = 0; j < TW; ++j) S[j] = src ? src[j] : (mode == 2 && cbase + j == k ? 1.f : 0.f);
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
     auto issue1 = [&](int it) {  // operands of the first MMA group
         const int64_t ch = chunk(it);
-        mbar_expect_tx(&bars[0], with_do ? 3 * TCD + TCC : TCD);
+        mbar_expect_tx(&bars[0], with_do ? 2 * TCD + TCC + NH * (TCD / 2) : TCD);
         bulk_load(sm + RevSm::KH, ws.kh + ch * TCD, TCD, &bars[0]);
         if (with_do) {
             bulk_load(sm + RevSm::QS, ws.qs + ch * TCD, TCD, &bars[0]);
             bulk_load(sm + RevSm::AQK, ws.aqk + ch * TCC, TCC, &bars[0]);
             const int row = (int)(bos + (int64_t)it * kC);
-            tma_load_3d(sm + RevSm::DO, &tm_do, 0, hv, row, &bars[0]);
-            tma_load_3d(sm + RevSm::DO + TCD / 2, &tm_do, 64, hv, row, &bars[0]);
+            for (int x = 0; x < NH; ++x)  // this CTA's columns of dO
+                tma_load_3d(sm + RevSm::DO + x * (TCD / 2), &tm_do, 64 * (h + x), hv, row, &bars[0]);
         }
     };
     auto issue2 = [&](int it) {  // w (second MMA group) and e^Gamma_C (state update)
@@ -816,15 +825,15 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
     for (int it = hi - 1; it >= lo; --it) {
         const int64_t ch = chunk(it);
         const uint32_t ph = (uint32_t)(hi - 1 - it) & 1;
-        // bf16 copy of dS (row k, this thread's 64 columns): MMA operand and the dS_out checkpoint
+        // bf16 copy of dS (row k, this thread's columns): MMA operand and the dS_out checkpoint
 #pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
+        for (int c8 = 0; c8 < TW; c8 += 8) st_tile_row8(tS, k, TW * vq + c8, D, S + c8);
         fence_async_smem();
         if (!wait_all(&bars[0], ph, ws.status, 31, fail)) break;
         if (tid == 0) {
             tc_fence_after();
-            // dDelta = Aqk^T dO + K^ dS (chunk rows on TMEM lanes, M = 64, N = 128)
-            const uint32_t ida = idesc_bf16(64, 128, true, true), idb = idesc_bf16(64, 128, false, true);
+            // dDelta = Aqk^T dO + K^ dS (chunk rows on TMEM lanes, M = 64, N = CW)
+            const uint32_t ida = idesc_bf16(64, CW, true, true), idb = idesc_bf16(64, CW, false, true);
             if (with_do)
                 for (int ks = 0; ks < kC / 16; ++ks)
                     mma_bf16(tmem, desc_mnmajor(smem_u32(sm + RevSm::AQK), kC, ks),
@@ -832,15 +841,15 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + RevSm::KH), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), idb,
                          with_do || ks > 0);
-            // dS accumulator = Q~s^T dO (M = 128, N = 128)
-            const uint32_t idc = idesc_bf16(128, 128, true, true);
+            // dS accumulator = Q~s^T dO (M = 128, N = CW)
+            const uint32_t idc = idesc_bf16(128, CW, true, true);
             if (with_do)
                 for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::QS), kC, ks),
+                    mma_bf16(tmem + CW, desc_mnmajor(smem_u32(sm + RevSm::QS), kC, ks),
                              desc_mnmajor(smem_u32(sm + RevSm::DO), kC, ks), idc, ks > 0);
             mma_commit(&bars[2]);
-            if (ckpt) {
-                bulk_store(ws.dso + ch * TDD, tS, TDD);
+            if (ckpt) {  // (column block h of the 128-row tile)
+                bulk_store(ws.dso + ch * TDD + h * (D * 128), tS, D * CW * 2);
                 bulk_commit();
             }
         }
@@ -849,16 +858,16 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
         mph ^= 1;
         if (tid == 0 && it > lo) issue1(it - 1);  // the first group's operands are consumed
         tc_fence_after();
-        {  // dDelta rows into tS: row r = 16 (warp % 4) + lane (lane < 16), 64 columns per warp half
-            const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);
+        {  // dDelta rows into tS: row r = 16 (warp % 4) + lane (lane < 16), CW / 2 columns per warp half
+            const int r = 16 * (warp & 3) + lane, cb = (CW / 2) * (warp >> 2);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int x = 0; x < CW / 64; ++x) {
                 float acc[32];
-                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld32(tmem + lq + cb + 32 * x, acc);
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tS, r, cb + 32 * h + c8, kC, acc + c8);
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tS, r, cb + 32 * x + c8, kC, acc + c8);
                 }
             }
         }
@@ -867,13 +876,13 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
         if (!wait_all(&bars[1], ph, ws.status, 34, fail)) break;
         if (tid == 0) {  // dS accumulator -= w^T dDelta
             tc_fence_after();
-            const uint32_t id = idesc_neg_a(idesc_bf16(128, 128, true, true));
+            const uint32_t id = idesc_neg_a(idesc_bf16(128, CW, true, true));
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + RevSm::W), kC, ks), desc_mnmajor(smem_u32(tS), kC, ks),
+                mma_bf16(tmem + CW, desc_mnmajor(smem_u32(sm + RevSm::W), kC, ks), desc_mnmajor(smem_u32(tS), kC, ks),
                          id, with_do || ks > 0);
             mma_commit(&bars[2]);
-            if (ckpt) {
-                bulk_store(ws.dvn + ch * TCD, tS, TCD);
+            if (ckpt) {  // (column block h of the 64-row tile)
+                bulk_store(ws.dvn + ch * TCD + h * (kC * 128), tS, kC * CW * 2);
                 bulk_commit();
             }
         }
@@ -884,14 +893,14 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
         if (tid == 0 && it > lo) issue2(it - 1);  // w and e^Gamma_C are consumed
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int x = 0; x < TW / 32; ++x) {
             float acc[32];
-            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+            tmem_ld32(tmem + lq + CW + TW * vq + 32 * x, acc);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float2 v = fma2(bc2(e), f2(S[32 * h + j], S[32 * h + j + 1]), f2(acc[j], acc[j + 1]));
-                S[32 * h + j] = v.x, S[32 * h + j + 1] = v.y;
+                const float2 v = fma2(bc2(e), f2(S[32 * x + j], S[32 * x + j + 1]), f2(acc[j], acc[j + 1]));
+                S[32 * x + j] = v.x, S[32 * x + j + 1] = v.y;
             }
         }
         tc_fence_before();
@@ -899,38 +908,41 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
     if (*(volatile int*)fail == 0) {
         float* dst = mode == 1 ? ws.seg_e + seg_at
                      : mode == 2 ? ws.seg_p + seg_at
-                     : (dh0 && lo == 0) ? dh0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh
+                     : (dh0 && lo == 0) ? dh0 + (((int64_t)n * HV + hv) * D + k) * D + cbase
                                         : nullptr;
         if (dst)
 #pragma unroll
-            for (int j = 0; j < 64; ++j) dst[j] = S[j];
+            for (int j = 0; j < TW; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 2 * CW);
 }
 
 __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
                                                        TcWs ws, const __grid_constant__ CUtensorMap tm_do, SegArg sg) {
     extern __shared__ uint8_t smraw[];
-    ds_rev_body(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z);
+    ds_rev_body<2>(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
 }
 
 // The forward state pass and the reverse state-gradient pass, whole sweeps, in one launch: grid z = 0 runs
 // tc_state_fwd's sweep of (sequence, value head), z = 1 tc_ds_rev's. The reverse pass reads only the
 // intra-chunk tiles and dO (not S_in nor delta), so the two sweeps are independent and, when all their
-// CTAs are resident at once, run side by side instead of one after the other.
+// CTAs are resident at once, run side by side instead of one after the other. NH = 1 splits each sweep
+// by columns over two CTAs (grid x = 2 HV: value head x / 2, column half x % 2).
 constexpr int kBothSmem = kFwdSmem > kRevSmem ? kFwdSmem : kRevSmem;
+template <int NH>
 __global__ void __launch_bounds__(256, 2)
     k_tc_state_both(Prob p, const float* __restrict__ h0, const float* __restrict__ dht, float* __restrict__ dh0,
                     TcWs ws, const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do) {
     extern __shared__ uint8_t smraw[];
     const SegArg whole{0, 1, kSegNone};
+    const int hv = NH == 2 ? (int)blockIdx.x : (int)blockIdx.x >> 1, h = NH == 2 ? 0 : (int)blockIdx.x & 1;
     if (blockIdx.z == 0)
-        state_fwd_body(p, h0, ws, whole, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, 0);
+        state_fwd_body<NH>(p, h0, ws, whole, tm_v, align1024(smraw), hv, blockIdx.y, 0, h);
     else
-        ds_rev_body(p, dht, dh0, ws, tm_do, whole, align1024(smraw), blockIdx.x, blockIdx.y, 0);
+        ds_rev_body<NH>(p, dht, dh0, ws, tm_do, whole, align1024(smraw), hv, blockIdx.y, 0, h);
 }
 
 // ---------------------------------------------------------------------------
@@ -1336,7 +1348,8 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_ds_rev, kRevSmem)) != cudaSuccess) return e;
-    if ((e = set_smem(k_tc_state_both, kBothSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_both<2>, kBothSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_both<1>, kBothSmem)) != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.B * p.T;
     CUtensorMap tm_do;
     memset(&tm_do, 0, sizeof(tm_do));
@@ -1348,14 +1361,22 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
     if (stages >= 1 && !from_saved && (e = launch_intra(p, io, ws, st)) != cudaSuccess) return e;
     const SegPlan sp = seg_plan(p);
     const SegArg ends{sp.len, sp.M, kSegEnds}, ckpt{sp.len, sp.M, kSegCkpt}, whole{0, 1, kSegNone};
-    // the two state passes side by side when each has at most one sweep per SM (both fit at two CTAs per SM)
+    // the two state passes side by side when each has at most one sweep per SM (both fit at two CTAs per SM),
+    // and with each sweep split by columns over two CTAs when that still fits
     int dev = 0, nsm = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    const bool both = stages >= 3 && !fused && !from_saved && !io.states_in && !sp.len && (int64_t)p.N * p.HV <= nsm;
+    const int64_t sweeps = (int64_t)p.N * p.HV;
+    const bool both = stages >= 3 && !fused && !from_saved && !io.states_in && !sp.len && sweeps <= nsm;
     if (both) {
-        k_tc_state_both<<<dim3(p.HV, p.N, 2), 256, kBothSmem, st>>>(p, io.h0, io.dht, io.dh0, ws, tm_v, tm_do);
-        note_launch("tc_state_both", st);
+        if (2 * sweeps <= nsm) {
+            k_tc_state_both<1><<<dim3(2 * p.HV, p.N, 2), 256, kBothSmem, st>>>(p, io.h0, io.dht, io.dh0, ws, tm_v,
+                                                                                tm_do);
+            note_launch("tc_state_both_vhalf", st);
+        } else {
+            k_tc_state_both<2><<<dim3(p.HV, p.N, 2), 256, kBothSmem, st>>>(p, io.h0, io.dht, io.dh0, ws, tm_v, tm_do);
+            note_launch("tc_state_both", st);
+        }
         if (stages >= 4) {
             if ((e = cudaGetLastError()) != cudaSuccess) return e;
             return tc_grads(p, io, ws, st);

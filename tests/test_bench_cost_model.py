@@ -47,4 +47,5 @@ def test_forward_and_state_load_bytes():
 
 
 def test_merged_state_passes_bytes():
-    assert _kb_per_chunk_head("tc_state_both") == _kb_per_chunk_head("tc_state_fwd") + _kb_per_chunk_head("tc_ds_rev")
+    both = _kb_per_chunk_head("tc_state_fwd") + _kb_per_chunk_head("tc_ds_rev")
+    assert _kb_per_chunk_head("tc_state_both") == _kb_per_chunk_head("tc_state_both_vhalf") == both

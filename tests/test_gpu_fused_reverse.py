@@ -51,7 +51,8 @@ def _workspace(kda, inp):
 def _check_bitwise(kda, inp, reps=2):
     """The fused path, twice on one workspace, equals the split path bit for bit; clean status word.
     (With at most one (sequence, head) sweep per SM the split path runs its two state passes as one launch,
-    tc_state_both; the fused path runs tc_state_fwd on its own.)"""
+    tc_state_both, and with at most one per two SMs splits each sweep by columns over two CTAs,
+    tc_state_both_vhalf; the fused path runs tc_state_fwd on its own.)"""
     split = gpu_bwd(kda, inp)
     split_names = _launches(kda)
     ws = _workspace(kda, inp)
@@ -75,13 +76,18 @@ FUSED = {
     "varlen": dict(B=1, T=0, H=2, HV=2, K=128, V=128, seq_lens=[130, 1, 0, 64, 77, 0]),
     "no_state": dict(B=1, T=150, H=1, HV=1, K=128, V=128, h0=False, dht=False),
     "many_sweeps": dict(B=3, T=64 * 3 + 40, H=64, HV=64, K=128, V=128),
+    "sweeps_100": dict(B=2, T=64 * 2 + 9, H=50, HV=50, K=128, V=128),
 }
 
 
 @pytest.mark.parametrize("name", list(FUSED))
 def test_fused_reverse_bitwise_and_oracle(kda, name):
     inp = kda_inputs.small(seed=47, dtype="bf16", **FUSED[name])
-    got, _ = _check_bitwise(kda, inp)
+    got, split_names = _check_bitwise(kda, inp)
+    # the split path's state passes: column-split side by side up to 76 sweeps, side by side up to 152
+    sweeps = len(inp.seq_bounds) * FUSED[name]["HV"]
+    want = b"tc_state_both_vhalf" if sweeps <= 76 else b"tc_state_both" if sweeps <= 152 else b"tc_state_fwd"
+    assert want in split_names, (sweeps, split_names)
     print(name, compare_full(inp, got, oracle.run_inputs(inp)))
 
 
@@ -118,8 +124,8 @@ def test_fused_reverse_workloads_bitwise(kda, name):
     bit for bit the split path's gradients (whose whole-tensor oracle parity the parity tests check)."""
     inp = _workload(name)
     got, split_names = _check_bitwise(kda, inp, reps=1)
-    side_by_side = name == "bf16_b1_t2048_h16_k128"  # 16 sweeps; the others have 256 and 512
-    assert (b"tc_state_both" in split_names) == side_by_side, split_names
+    side_by_side = name == "bf16_b1_t2048_h16_k128"  # 16 sweeps (each split by columns); the others 256, 512
+    assert (b"tc_state_both_vhalf" in split_names) == side_by_side, split_names
     assert (b"tc_ds_rev" in split_names) != side_by_side, split_names
     if name == "bf16_b1_t2048_h16_k128":
         print(name, compare_full(inp, {k: (None if v is None else v.cpu()) for k, v in got.items()},

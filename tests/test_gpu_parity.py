@@ -154,7 +154,8 @@ def test_backward_from_saved_states_is_bitwise_recompute(kda, name):
     rec = gpu_bwd(kda, inp)
     lib = kda.load()
     names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
-    assert b"tc_state_fwd" in names or b"tc_state_both" in names, names  # (both passes in one launch when small)
+    # (both state passes in one launch when the batch is small)
+    assert b"tc_state_fwd" in names or any(x.startswith(b"tc_state_both") for x in names), names
     sv = gpu_bwd(kda, inp, states=st)
     names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
     assert b"tc_state_load" in names and b"tc_state_fwd" not in names, names
@@ -190,7 +191,8 @@ def _check_saved_context(kda, inp, oracle_parity=True):
     for rep in range(2):
         sv = _bwd_from_saved(kda, inp, x, saved)
         names = _launches(kda)
-        assert b"tc_grads" in names and not {b"tc_intra", b"tc_state_fwd", b"tc_state_both"} & set(names), names
+        assert b"tc_grads" in names and not {b"tc_intra", b"tc_state_fwd", b"tc_state_both",
+                                             b"tc_state_both_vhalf"} & set(names), names
         for key in GRADS:
             if rec[key] is not None:
                 assert torch.equal(rec[key], sv[key]), (rep, key)
