@@ -28,7 +28,9 @@
 //                 dDelta and dh0.
 //   tc_state_both the two sweeps above in one launch (they are independent: the
 //                 reverse pass reads neither S_in nor delta), used when each
-//                 pass has at most one (sequence, value head) sweep per SM.
+//                 pass has at most one (sequence, value head) sweep per SM; with
+//                 at most one per two SMs each sweep also splits by state
+//                 columns over two CTAs (the columns evolve independently).
 //   tc_seg_combine   chains segment start states (long sequences).
 //   tc_state_load the backward's state pass from the forward's saved states.
 //   tc_fwd_out    the forward: the state pass with o = (scale Q~) S + Aqk
