@@ -112,7 +112,9 @@ def pass_cost(mode, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None, seq_states=0)
 
 
 def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
-    """(bound, algorithmic bytes, algorithmic flops) of one launch of kernel ``name``."""
+    """(bound, algorithmic bytes, algorithmic flops) of one launch of kernel ``name``. A ``_vhalf`` launch
+    (each sweep split by state columns over two CTAs) has the algorithmic cost of the whole one."""
+    name = name[: -len("_vhalf")] if name.endswith("_vhalf") else name
     s = step_cost(B, T, H, HV, K, V, in_bytes, C, nck)
     nck = s["nck"]
     th = B * T * HV
@@ -145,7 +147,7 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
         return "hbm", b, f
     if name == "tc_state_fwd":  # w, INV diag(beta), V, K^, e^Gamma_C in; S_in, delta out
         return "hbm", nck * (3 * tcd + tcc + K * 4 + tdd + tcd), nck * 4 * C * K * V
-    if name in ("tc_state_both", "tc_state_both_vhalf"):  # tc_state_fwd and tc_ds_rev in one launch
+    if name == "tc_state_both":  # tc_state_fwd and tc_ds_rev in one launch
         sf, sr = kernel_cost("tc_state_fwd", B, T, H, HV, K, V, in_bytes, C, nck), kernel_cost(
             "tc_ds_rev", B, T, H, HV, K, V, in_bytes, C, nck)
         return "hbm", sf[1] + sr[1], sf[2] + sr[2]
@@ -176,7 +178,7 @@ MEASURED_TRAFFIC = {
                      "bytes_per_chunk_head": (875.185152e6 + 309.354240e6) / 4096},
     # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change host code (the segment plan, the
     # launch choices) and the two state passes' kernels, not tc_intra
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "636cf49bbfa4",
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "34c38cc10393",
                  "bytes_per_chunk_head": (269.066240e6 + 249.859328e6) / 4096},
 }
 

@@ -638,6 +638,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __
     extern __shared__ uint8_t smraw[];
     state_fwd_body<2>(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
 }
+// whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
+__global__ void __launch_bounds__(256, 2) k_tc_state_fwd_half(Prob p, const float* __restrict__ h0, TcWs ws,
+                                                               const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ uint8_t smraw[];
+    state_fwd_body<1>(p, h0, ws, SegArg{0, 1, kSegNone}, tm_v, align1024(smraw), blockIdx.x >> 1, blockIdx.y, 0,
+                      blockIdx.x & 1);
+}
 
 // ---------------------------------------------------------------------------
 // tc_seg_combine: start states of the segments of one (sequence, value head),
@@ -927,6 +934,14 @@ __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __res
     extern __shared__ uint8_t smraw[];
     ds_rev_body<2>(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
 }
+// whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
+__global__ void __launch_bounds__(256, 2) k_tc_ds_rev_half(Prob p, const float* __restrict__ dht,
+                                                            float* __restrict__ dh0, TcWs ws,
+                                                            const __grid_constant__ CUtensorMap tm_do) {
+    extern __shared__ uint8_t smraw[];
+    ds_rev_body<1>(p, dht, dh0, ws, tm_do, SegArg{0, 1, kSegNone}, align1024(smraw), blockIdx.x >> 1, blockIdx.y, 0,
+                   blockIdx.x & 1);
+}
 
 // The forward state pass and the reverse state-gradient pass, whole sweeps, in one launch: grid z = 0 runs
 // tc_state_fwd's sweep of (sequence, value head), z = 1 tc_ds_rev's. The reverse pass reads only the
@@ -1068,10 +1083,14 @@ struct FoSm {
 };
 constexpr int kFoSmem = FoSm::END;
 
-__global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
-                                                        float* __restrict__ states, bf16* __restrict__ o, TcWs ws,
-                                                        SegArg sg, const __grid_constant__ CUtensorMap tm_v) {
-    extern __shared__ __align__(1024) uint8_t sm[];
+// (sequence n, value head hv, segment z; NH and the column half h as in state_fwd_body: o's column v takes
+// only S's and delta's column v)
+template <int NH>
+__device__ __forceinline__ void fwd_out_body(const Prob& p, const float* __restrict__ h0, float* __restrict__ ht,
+                                             float* __restrict__ states, bf16* __restrict__ o, const TcWs& ws,
+                                             const SegArg& sg, const CUtensorMap& tm_v, uint8_t* sm, int hv, int n,
+                                             int z, int h) {
+    constexpr int CW = 64 * NH, TW = CW / 2;  // state columns of this CTA and of each thread
     uint8_t* tS = sm + FoSm::S;
     uint8_t* tU = sm + FoSm::U;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FoSm::BARS);  // w, group 2, mma
@@ -1079,12 +1098,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     int* fail = reinterpret_cast<int*>(tslot + 1);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k = tid & 127, vh = tid >> 7;
-    const int HV = p.HV, hv = blockIdx.x, n = blockIdx.y;
+    const int k = tid & 127, vq = tid >> 7;
+    const int cbase = 64 * h + TW * vq;  // this thread's first state column
+    const int HV = p.HV;
     int64_t bos, eos, c0;
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
-    const int m = (int)blockIdx.z;  // segment (kSegCkpt) or the whole sequence (kSegNone)
+    const int m = z;  // segment (kSegCkpt) or the whole sequence (kSegNone)
     const int lo = sg.len ? m * sg.len : 0, hi = sg.len ? min(lo + sg.len, nts) : nts;
     if (sg.len && lo >= hi) return;
 
@@ -1094,13 +1114,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         *fail = (smem_u32(sm) & 1023u) ? 1 : 0;  // tiles need a 1024-byte aligned base
         if (*fail) *(volatile int*)ws.status = 70;
     }
-    if (warp == 0) tmem_alloc(tslot, 256);
-    float S[64];
+    if (warp == 0) tmem_alloc(tslot, 2 * CW);  // delta and then o [0, CW), state [CW, 2 CW)
+    float S[TW];
     {
-        const float* src = lo == 0 ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh : nullptr)
-                                   : ws.seg_s0 + (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + 64 * vh;
+        const float* src = lo == 0 ? (h0 ? h0 + (((int64_t)n * HV + hv) * D + k) * D + cbase : nullptr)
+                                   : ws.seg_s0 + (((int64_t)n * HV + hv) * sg.M + m) * D * D + (int64_t)k * D + cbase;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) S[j] = src ? src[j] : 0.f;
+        for (int j = 0; j < TW; ++j) S[j] = src ? src[j] : 0.f;
     }
     auto chunk = [&](int it) { return (c0 + it) * HV + hv; };
     auto issue_w = [&](int it) {  // w and INVb
@@ -1108,14 +1128,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         bulk_load(sm + FoSm::W, ws.w + chunk(it) * TCD, TCD, &bars[0]);
         bulk_load(sm + FoSm::IVB, ws.invb + chunk(it) * TCC, TCC, &bars[0]);
     };
-    auto issue_g2 = [&](int it) {  // K^, scale Q~, V (TMA), Aqk, e^Gamma_C
+    auto issue_g2 = [&](int it) {  // K^, scale Q~, V (TMA; this CTA's columns), Aqk, e^Gamma_C
         const int64_t ch = chunk(it);
         const int row = (int)(bos + (int64_t)it * kC);
-        mbar_expect_tx(&bars[1], 3 * TCD + TCC + 512);
+        mbar_expect_tx(&bars[1], 2 * TCD + NH * (TCD / 2) + TCC + 512);
         bulk_load(sm + FoSm::KH, ws.kh + ch * TCD, TCD, &bars[1]);
         bulk_load(sm + FoSm::QS, ws.qs + ch * TCD, TCD, &bars[1]);
-        tma_load_3d(tU, &tm_v, 0, hv, row, &bars[1]);
-        tma_load_3d(tU + TCD / 2, &tm_v, 64, hv, row, &bars[1]);
+        for (int x = 0; x < NH; ++x) tma_load_3d(tU + x * (TCD / 2), &tm_v, 64 * (h + x), hv, row, &bars[1]);
         bulk_load(sm + FoSm::AQK, ws.aqk + ch * TCC, TCC, &bars[1]);
         bulk_load(sm + FoSm::EGC, ws.egc + ch * D, 512, &bars[1]);
     };
@@ -1134,18 +1153,18 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
     for (int it = lo; it < hi && run; ++it) {
         const int64_t ch = chunk(it);
         const uint32_t ph = (uint32_t)(it - lo) & 1;
-        // bf16 copy of S (row k, this thread's 64 columns): operand of the delta and output MMAs
+        // bf16 copy of S (row k, this thread's columns): operand of the delta and output MMAs
 #pragma unroll
-        for (int c8 = 0; c8 < 64; c8 += 8) st_tile_row8(tS, k, 64 * vh + c8, D, S + c8);
+        for (int c8 = 0; c8 < TW; c8 += 8) st_tile_row8(tS, k, TW * vq + c8, D, S + c8);
         fence_async_smem();
         if (states) {  // the fp32 state entering this chunk, [chunk, HV, K, V]
-            float4* dst = reinterpret_cast<float4*>(states + (ch * D + k) * D + 64 * vh);
+            float4* dst = reinterpret_cast<float4*>(states + (ch * D + k) * D + cbase);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
+            for (int j = 0; j < TW / 4; ++j) dst[j] = make_float4(S[4 * j], S[4 * j + 1], S[4 * j + 2], S[4 * j + 3]);
         }
         if (!wait_all2(&bars[0], ph, 71, &bars[1], ph, 73, ws.status, fail)) break;
-        // delta accumulator = -w S + INVb V (M = 64, N = 128)
-        const uint32_t idd = idesc_bf16(64, 128, false, true);
+        // delta accumulator = -w S + INVb V (M = 64, N = CW)
+        const uint32_t idd = idesc_bf16(64, CW, false, true);
         if (tid == 0) {
             tc_fence_after();
             for (int ks = 0; ks < D / 16; ++ks)
@@ -1155,8 +1174,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::IVB), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          idd, 1);
             mma_commit(&bars[2]);
-            if (save) {
-                bulk_store(ws.sin + ch * TDD, tS, TDD);
+            if (save) {  // (column block h of the 128-row tile)
+                bulk_store(ws.sin + ch * TDD + h * (D * 128), tS, D * CW * 2);
                 bulk_commit();
             }
         }
@@ -1164,16 +1183,17 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         mph ^= 1;
         if (tid == 0 && it + 1 < hi) issue_w(it + 1);  // w and INVb are consumed
         tc_fence_after();
-        const int r = 16 * (warp & 3) + lane, cb = 64 * (warp >> 2);  // M = 64 row of this lane, column half
+        // M = 64 row of this lane, and this warp's half of the CTA's columns
+        const int r = 16 * (warp & 3) + lane, cb = (CW / 2) * (warp >> 2);
         {  // delta (bf16) in place of V
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int x = 0; x < CW / 64; ++x) {
                 float acc[32];
-                tmem_ld32(tmem + lq + cb + 32 * h, acc);
+                tmem_ld32(tmem + lq + cb + 32 * x, acc);
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * h + c8, kC, acc + c8);
+                    for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tU, r, cb + 32 * x + c8, kC, acc + c8);
                 }
             }
         }
@@ -1182,13 +1202,13 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            // S accumulator = K^^T delta (M = 128, N = 128)
-            const uint32_t is = idesc_bf16(128, 128, true, true);
+            // S accumulator = K^^T delta (M = 128, N = CW)
+            const uint32_t is = idesc_bf16(128, CW, true, true);
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_bf16(tmem + 128, desc_mnmajor(smem_u32(sm + FoSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
+                mma_bf16(tmem + CW, desc_mnmajor(smem_u32(sm + FoSm::KH), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks),
                          is, ks > 0);
-            // o accumulator (in the delta columns) = (scale Q~) S + Aqk delta (M = 64, N = 128)
-            const uint32_t io = idesc_bf16(64, 128, false, true);
+            // o accumulator (in the delta columns) = (scale Q~) S + Aqk delta (M = 64, N = CW)
+            const uint32_t io = idesc_bf16(64, CW, false, true);
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::QS), kC, ks), desc_mnmajor(smem_u32(tS), D, ks), io,
                          ks > 0);
@@ -1196,8 +1216,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                 mma_bf16(tmem, desc_kmajor(smem_u32(sm + FoSm::AQK), kC, ks), desc_mnmajor(smem_u32(tU), kC, ks), io,
                          1);
             mma_commit(&bars[2]);
-            if (save) {
-                bulk_store(ws.vn + ch * TCD, tU, TCD);
+            if (save) {  // (column block h of the 64-row tile)
+                bulk_store(ws.vn + ch * TCD + h * (kC * 128), tU, kC * CW * 2);
                 bulk_commit();
                 bulk_wait_read();  // the S_in and delta copies have read tS and tU (both rewritten next)
             }
@@ -1208,23 +1228,23 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         if (tid == 0 && it + 1 < hi) issue_g2(it + 1);  // K^, Q~s, u / delta, Aqk, e^Gamma_C are consumed
         tc_fence_after();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {  // state update
+        for (int x = 0; x < TW / 32; ++x) {  // state update
             float acc[32];
-            tmem_ld32(tmem + lq + 128 + 64 * vh + 32 * h, acc);
+            tmem_ld32(tmem + lq + CW + TW * vq + 32 * x, acc);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) S[32 * h + j] = fmaf(e, S[32 * h + j], acc[j]);
+            for (int j = 0; j < 32; ++j) S[32 * x + j] = fmaf(e, S[32 * x + j], acc[j]);
         }
         {  // o rows (bf16)
             const int64_t r0 = bos + (int64_t)it * kC;
             const int c = (int)((eos - r0) < kC ? (eos - r0) : kC);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {  // 16 columns at a time (the 64 state values stay in registers)
+            for (int y = 0; y < CW / 32; ++y) {  // 16 columns at a time (the state values stay in registers)
                 float x[16];
-                tmem_ld16(tmem + lq + cb + 16 * h, x);
+                tmem_ld16(tmem + lq + cb + 16 * y, x);
                 tmem_ld_wait();
                 if (lane < 16 && r < c) {
-                    bf16* dst = o + ((r0 + r) * HV + hv) * D + cb + 16 * h;
+                    bf16* dst = o + ((r0 + r) * HV + hv) * D + 64 * h + cb + 16 * y;
 #pragma unroll
                     for (int u = 0; u < 16; u += 8) {
                         uint4 vv;
@@ -1240,14 +1260,30 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
         tc_fence_before();
     }
     if (ht && hi == nts && *(volatile int*)fail == 0) {
-        float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + 64 * vh;
+        float* dst = ht + (((int64_t)n * HV + hv) * D + k) * D + cbase;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) dst[j] = S[j];
+        for (int j = 0; j < TW; ++j) dst[j] = S[j];
     }
     if (tid == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, 2 * CW);
+}
+
+__global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __restrict__ h0, float* __restrict__ ht,
+                                                        float* __restrict__ states, bf16* __restrict__ o, TcWs ws,
+                                                        SegArg sg, const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    fwd_out_body<2>(p, h0, ht, states, o, ws, sg, tm_v, sm, blockIdx.x, blockIdx.y, blockIdx.z, 0);
+}
+// whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
+__global__ void __launch_bounds__(256, 2) k_tc_fwd_out_half(Prob p, const float* __restrict__ h0,
+                                                             float* __restrict__ ht, float* __restrict__ states,
+                                                             bf16* __restrict__ o, TcWs ws,
+                                                             const __grid_constant__ CUtensorMap tm_v) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    fwd_out_body<1>(p, h0, ht, states, o, ws, SegArg{0, 1, kSegNone}, tm_v, sm, blockIdx.x >> 1, blockIdx.y, 0,
+                    blockIdx.x & 1);
 }
 
 template <typename F>
@@ -1326,6 +1362,7 @@ static bool make_tmap_v(CUtensorMap* m, const Prob& p, const void* v) {
 cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
     if ((e = set_smem(k_tc_fwd_out, kFoSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_fwd_out_half, kFoSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     CUtensorMap tm_v;
     if (!make_tmap_v(&tm_v, p, io.v)) return cudaErrorInvalidValue;
@@ -1338,9 +1375,19 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
         k_tc_seg_combine<<<dim3(p.HV, p.N, D / kCombCols), 256, 0, st>>>(p, ends, 0, io.h0, ws);
         note_launch("tc_seg_combine", st);
     }
-    k_tc_fwd_out<<<dim3(p.HV, p.N, sp.M), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
-                                                              SegArg{sp.len, sp.M, sp.len ? kSegCkpt : kSegNone}, tm_v);
-    note_launch("tc_fwd_out", st);
+    int dev = 0, nsm = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (!sp.len && (int64_t)p.N * p.HV <= nsm) {  // few whole sweeps: each split by columns over two CTAs
+        k_tc_fwd_out_half<<<dim3(2 * p.HV, p.N), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
+                                                                     tm_v);
+        note_launch("tc_fwd_out_vhalf", st);
+    } else {
+        k_tc_fwd_out<<<dim3(p.HV, p.N, sp.M), 256, kFoSmem, st>>>(p, io.h0, io.ht, io.states_out, (bf16*)io.o, ws,
+                                                                  SegArg{sp.len, sp.M, sp.len ? kSegCkpt : kSegNone},
+                                                                  tm_v);
+        note_launch("tc_fwd_out", st);
+    }
     return cudaGetLastError();
 }
 
@@ -1348,8 +1395,10 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
                    bool fused) {
     cudaError_t e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_state_fwd_half, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_ds_rev, kRevSmem)) != cudaSuccess) return e;
+    if ((e = set_smem(k_tc_ds_rev_half, kRevSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_both<2>, kBothSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_both<1>, kBothSmem)) != cudaSuccess) return e;
     const int64_t rows = (int64_t)p.B * p.T;
@@ -1398,6 +1447,9 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
             note_launch("tc_seg_combine", st);
             k_tc_state_fwd<<<dim3(p.HV, p.N, sp.M), 256, kFwdSmem, st>>>(p, io.h0, ws, ckpt, tm_v);
             note_launch("tc_state_fwd", st);
+        } else if (sweeps <= nsm) {  // a pass alone, each sweep split by columns (two CTAs per SM at most)
+            k_tc_state_fwd_half<<<dim3(2 * p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, tm_v);
+            note_launch("tc_state_fwd_vhalf", st);
         } else {
             k_tc_state_fwd<<<dim3(p.HV, p.N), 256, kFwdSmem, st>>>(p, io.h0, ws, whole, tm_v);
             note_launch("tc_state_fwd", st);
@@ -1416,6 +1468,9 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
             note_launch("tc_seg_combine", st);
             k_tc_ds_rev<<<dim3(p.HV, p.N, sp.M), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, ckpt);
             note_launch("tc_ds_rev", st);
+        } else if (sweeps <= nsm) {
+            k_tc_ds_rev_half<<<dim3(2 * p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do);
+            note_launch("tc_ds_rev_vhalf", st);
         } else {
             k_tc_ds_rev<<<dim3(p.HV, p.N), 256, kRevSmem, st>>>(p, io.dht, io.dh0, ws, tm_do, whole);
             note_launch("tc_ds_rev", st);

@@ -49,3 +49,6 @@ def test_forward_and_state_load_bytes():
 def test_merged_state_passes_bytes():
     both = _kb_per_chunk_head("tc_state_fwd") + _kb_per_chunk_head("tc_ds_rev")
     assert _kb_per_chunk_head("tc_state_both") == _kb_per_chunk_head("tc_state_both_vhalf") == both
+
+    for name in ("tc_state_fwd", "tc_ds_rev"):
+        assert _kb_per_chunk_head(name + "_vhalf") == _kb_per_chunk_head(name)

@@ -84,9 +84,11 @@ FUSED = {
 def test_fused_reverse_bitwise_and_oracle(kda, name):
     inp = kda_inputs.small(seed=47, dtype="bf16", **FUSED[name])
     got, split_names = _check_bitwise(kda, inp)
-    # the split path's state passes: column-split side by side up to 76 sweeps, side by side up to 152
-    sweeps = len(inp.seq_bounds) * FUSED[name]["HV"]
-    want = b"tc_state_both_vhalf" if sweeps <= 76 else b"tc_state_both" if sweeps <= 152 else b"tc_state_fwd"
+    # the split path's state passes: side by side with each sweep split by columns up to one sweep per two SMs,
+    # side by side up to one per SM, else one after the other
+    sweeps, nsm = len(inp.seq_bounds) * FUSED[name]["HV"], torch.cuda.get_device_properties(0).multi_processor_count
+    want = (b"tc_state_both_vhalf" if 2 * sweeps <= nsm else b"tc_state_both" if sweeps <= nsm
+            else b"tc_state_fwd")
     assert want in split_names, (sweeps, split_names)
     print(name, compare_full(inp, got, oracle.run_inputs(inp)))
 
