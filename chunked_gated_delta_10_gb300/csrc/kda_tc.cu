@@ -36,6 +36,13 @@
 //   tc_fwd_out    the forward: the state pass with o = (scale Q~) S + Aqk
 //                 delta formed in the same MMA group.
 //
+// The columns of S and dS evolve independently (delta, dDelta and o take, per
+// column, only that column of S or dS and of V or dO), so when a batch has at
+// most one (sequence, value head) sweep per SM each whole sweep of the state,
+// reverse and output passes runs as two CTAs of 64 columns (the _half kernels
+// and the NH = 1 bodies): narrower MMAs and half the epilogue work per chunk
+// step on a chain that is latency-bound there.
+//
 // Intermediates live in the workspace as bf16 tiles in exactly the
 // shared-memory operand layout of tc_util.cuh (row-major, 64-column blocks,
 // 128-byte swizzle), so each consumer fetches a tile with one bulk copy.
