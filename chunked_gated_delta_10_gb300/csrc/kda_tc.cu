@@ -247,7 +247,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
         for (int i = 0; w < total; ++i, w += gridDim.x) {
             const int slot = i & 1;
             const int64_t ch = w;
-            chunk_rows(p, w / HV, r0, c);
+            // (r0, c: this item's rows, found while the previous item ran; with packed sequences a look-up in
+            // the chunk table, two dependent global loads, that would otherwise stall the item's start)
             const int64_t wn = w + gridDim.x;
             const bool has_next = wn < total;
             const int hvn = (int)(wn % HV);
@@ -429,6 +430,8 @@ __global__ void __launch_bounds__(256, 2) k_tc_intra(Prob p, const float* __rest
                 bulk_commit();
                 bulk_wait_read();  // the w, INV and INV diag(beta) tiles are rewritten by the next item's factor pass
             }
+            r0 = r0n;
+            c = cn;
             // (no barrier here: before its first barrier the next item writes only the item-start scratch, in the
             // dead K~ tile, and thread 0 reaches that barrier only once the copies above have read their tiles)
         }

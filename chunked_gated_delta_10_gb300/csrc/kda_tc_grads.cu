@@ -91,6 +91,17 @@ struct Item {
     int64_t r0, ch;
     int hv, h, c, valid;
 };
+// An item whose rows were looked up earlier and left in shared memory (r0, c at xrows[0], xrows[1]).
+__device__ __forceinline__ Item handed_item(const Prob& p, int64_t w, const int64_t* xrows) {
+    Item it;
+    it.hv = (int)(w % p.HV);
+    it.h = it.hv / (p.HV / p.H);
+    it.ch = w;
+    it.valid = 1;
+    it.r0 = xrows[0];
+    it.c = (int)xrows[1];
+    return it;
+}
 __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) {
     Item it;
     it.hv = (int)(w % p.HV);
@@ -332,10 +343,14 @@ __device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict
             float* sb = reinterpret_cast<float*>(sm + GS::BETA);
             sb[tid] = tid < first.c ? __bfloat162float(beta[(first.r0 + tid) * HV + first.hv]) : 0.f;
         }
+        // the next item's first row and row count, left by thread 0 while the current item runs (with packed
+        // sequences a chunk-table look-up, two dependent global loads, that would otherwise stall the item start)
+        int64_t* xrows = reinterpret_cast<int64_t*>(sm + GS::BARS + 96);
         for (int i = 0; live(w); ++i, w = next_w(w)) {
             const int slot = i & 1;
             const uint32_t par = (uint32_t)i & 1;
-            const Item cur = make_item(p, w, true);
+            // (the grouped instantiation looks up its own rows: the hand-off costs it registers)
+            const Item cur = (GROUPED || i == 0) ? make_item(p, w, true) : handed_item(p, w, xrows);
             const int64_t wn = next_w(w);
             const float* sbeta = reinterpret_cast<const float*>(sm + GS::BETA + 256 * slot);
             const float* segc = reinterpret_cast<const float*>(sm + GS::EGC + 512 * slot);
@@ -479,6 +494,10 @@ __device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict
                 if (live(wn)) {
                     const Item nx = make_item(p, wn, true);
                     if (tid < nx.c) nb = __bfloat162float(beta[(nx.r0 + tid) * HV + nx.hv]);
+                    if (!GROUPED && tid == 0) {  // (read after this item's last group barrier)
+                        xrows[0] = nx.r0;
+                        xrows[1] = nx.c;
+                    }
                 }
                 reinterpret_cast<float*>(sm + GS::BETA + 256 * (slot ^ 1))[tid] = nb;
             }
