@@ -44,7 +44,7 @@ struct Layout {
     size_t status, gam, w, u, vn, inv, aqk, sin, dso, dvn, dqt, dkh, dw, dgc, dqp, dkp, total;
     // tensor-core path regions
     bool tc;
-    size_t t_w, t_invb, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc, t_seg_e, t_seg_p, t_seg_s0;
+    size_t t_w, t_invb, t_kh, t_qs, t_vn, t_dvn, t_aqk, t_inv, t_sin, t_dso, t_egc, t_seg_e, t_seg_p, t_seg_s0, t_order;
 };
 
 // bf16 inputs with K = V = 128 run on the tensor-core path (forward and backward).
@@ -75,6 +75,7 @@ Layout layout(const Prob& p, int pass, bool tc) {
         L.t_inv = take(CH * TCC);
         L.t_invb = take(CH * TCC);
         L.t_egc = take(CH * 128 * f);
+        L.t_order = take((size_t)p.N * sizeof(int));  // the sweep order of packed sequences
         const SegPlan sp = seg_plan(p);
         if (sp.len) {  // segmented state passes: three fp32 K x V matrices per (sequence, head, segment)
             const size_t segs = (size_t)p.N * HV * sp.M * 128 * 128 * f;
@@ -169,6 +170,7 @@ TcWs carve_tc(void* base, const Layout& L) {
     w.seg_e = (float*)at(L.t_seg_e);
     w.seg_p = (float*)at(L.t_seg_p);
     w.seg_s0 = (float*)at(L.t_seg_s0);
+    w.seq_order = (int*)at(L.t_order);
     if (L.dqp) {
         w.dqp = (float*)at(L.dqp);
         w.dkp = (float*)at(L.dkp);

@@ -53,8 +53,16 @@ struct TcWs {
     // segmented state passes (long sequences, few sweeps): per (sequence, value head, segment) fp32
     // K x V end states from a zero start, K x K transitions and start states
     float *seg_e, *seg_p, *seg_s0;
+    // packed sequences: the sequence indices by decreasing chunk count (the order in which the sweeps of the
+    // state passes are launched, longest first), or null for the natural order
+    int* seq_order;
     int* status;
 };
+
+#ifdef __CUDACC__
+// The sequence of the y-th sweep row of a state-pass launch (grid y = sequence).
+__device__ __forceinline__ int sweep_seq(const TcWs& ws, int y) { return ws.seq_order ? ws.seq_order[y] : y; }
+#endif
 
 // Segmented sweeps of the state passes: segment m of a sequence covers chunks
 // [m * len, min((m + 1) * len, chunks)); len = 0 means no segmentation.

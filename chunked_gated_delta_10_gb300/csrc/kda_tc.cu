@@ -646,14 +646,14 @@ __device__ __forceinline__ void state_fwd_body(const Prob& p, const float* __res
 __global__ void __launch_bounds__(256, 2) k_tc_state_fwd(Prob p, const float* __restrict__ h0, TcWs ws, SegArg sg,
                                                           const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
-    state_fwd_body<2>(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
+    state_fwd_body<2>(p, h0, ws, sg, tm_v, align1024(smraw), blockIdx.x, sweep_seq(ws, blockIdx.y), blockIdx.z, 0);
 }
 // whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
 __global__ void __launch_bounds__(256, 2) k_tc_state_fwd_half(Prob p, const float* __restrict__ h0, TcWs ws,
                                                                const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ uint8_t smraw[];
-    state_fwd_body<1>(p, h0, ws, SegArg{0, 1, kSegNone}, tm_v, align1024(smraw), blockIdx.x >> 1, blockIdx.y, 0,
-                      blockIdx.x & 1);
+    state_fwd_body<1>(p, h0, ws, SegArg{0, 1, kSegNone}, tm_v, align1024(smraw), blockIdx.x >> 1,
+                      sweep_seq(ws, blockIdx.y), 0, blockIdx.x & 1);
 }
 
 // ---------------------------------------------------------------------------
@@ -942,15 +942,16 @@ __device__ __forceinline__ void ds_rev_body(const Prob& p, const float* __restri
 __global__ void __launch_bounds__(256, 2) k_tc_ds_rev(Prob p, const float* __restrict__ dht, float* __restrict__ dh0,
                                                        TcWs ws, const __grid_constant__ CUtensorMap tm_do, SegArg sg) {
     extern __shared__ uint8_t smraw[];
-    ds_rev_body<2>(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, blockIdx.y, blockIdx.z, 0);
+    ds_rev_body<2>(p, dht, dh0, ws, tm_do, sg, align1024(smraw), blockIdx.x, sweep_seq(ws, blockIdx.y), blockIdx.z,
+                   0);
 }
 // whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
 __global__ void __launch_bounds__(256, 2) k_tc_ds_rev_half(Prob p, const float* __restrict__ dht,
                                                             float* __restrict__ dh0, TcWs ws,
                                                             const __grid_constant__ CUtensorMap tm_do) {
     extern __shared__ uint8_t smraw[];
-    ds_rev_body<1>(p, dht, dh0, ws, tm_do, SegArg{0, 1, kSegNone}, align1024(smraw), blockIdx.x >> 1, blockIdx.y, 0,
-                   blockIdx.x & 1);
+    ds_rev_body<1>(p, dht, dh0, ws, tm_do, SegArg{0, 1, kSegNone}, align1024(smraw), blockIdx.x >> 1,
+                   sweep_seq(ws, blockIdx.y), 0, blockIdx.x & 1);
 }
 
 // The forward state pass and the reverse state-gradient pass, whole sweeps, in one launch: grid z = 0 runs
@@ -966,10 +967,11 @@ __global__ void __launch_bounds__(256, 2)
     extern __shared__ uint8_t smraw[];
     const SegArg whole{0, 1, kSegNone};
     const int hv = NH == 2 ? (int)blockIdx.x : (int)blockIdx.x >> 1, h = NH == 2 ? 0 : (int)blockIdx.x & 1;
+    const int n = sweep_seq(ws, blockIdx.y);
     if (blockIdx.z == 0)
-        state_fwd_body<NH>(p, h0, ws, whole, tm_v, align1024(smraw), hv, blockIdx.y, 0, h);
+        state_fwd_body<NH>(p, h0, ws, whole, tm_v, align1024(smraw), hv, n, 0, h);
     else
-        ds_rev_body<NH>(p, dht, dh0, ws, tm_do, whole, align1024(smraw), hv, blockIdx.y, 0, h);
+        ds_rev_body<NH>(p, dht, dh0, ws, tm_do, whole, align1024(smraw), hv, n, 0, h);
 }
 
 // ---------------------------------------------------------------------------
@@ -1284,7 +1286,7 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out(Prob p, const float* __re
                                                         float* __restrict__ states, bf16* __restrict__ o, TcWs ws,
                                                         SegArg sg, const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    fwd_out_body<2>(p, h0, ht, states, o, ws, sg, tm_v, sm, blockIdx.x, blockIdx.y, blockIdx.z, 0);
+    fwd_out_body<2>(p, h0, ht, states, o, ws, sg, tm_v, sm, blockIdx.x, sweep_seq(ws, blockIdx.y), blockIdx.z, 0);
 }
 // whole sweeps split by columns: grid x = 2 HV (value head x / 2, column half x % 2)
 __global__ void __launch_bounds__(256, 2) k_tc_fwd_out_half(Prob p, const float* __restrict__ h0,
@@ -1292,8 +1294,31 @@ __global__ void __launch_bounds__(256, 2) k_tc_fwd_out_half(Prob p, const float*
                                                              bf16* __restrict__ o, TcWs ws,
                                                              const __grid_constant__ CUtensorMap tm_v) {
     extern __shared__ __align__(1024) uint8_t sm[];
-    fwd_out_body<1>(p, h0, ht, states, o, ws, SegArg{0, 1, kSegNone}, tm_v, sm, blockIdx.x >> 1, blockIdx.y, 0,
-                    blockIdx.x & 1);
+    fwd_out_body<1>(p, h0, ht, states, o, ws, SegArg{0, 1, kSegNone}, tm_v, sm, blockIdx.x >> 1,
+                    sweep_seq(ws, blockIdx.y), 0, blockIdx.x & 1);
+}
+
+// Packed sequences: order[rank] = sequence, by decreasing chunk count (ties by index), so that the state
+// passes launch the sweeps of the longest sequences first and the short ones fill in behind them. Thread i
+// ranks sequence i against all others, N in tiles of 256 through shared memory.
+__global__ void __launch_bounds__(256) k_seq_order(const int64_t* __restrict__ cu, int N, int* __restrict__ order) {
+    __shared__ int tile[256];
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    auto chunks = [&](int j) { return (int)((cu[j + 1] - cu[j] + kC - 1) / kC); };
+    const int ci = i < N ? chunks(i) : 0;
+    int rank = 0;
+    for (int j0 = 0; j0 < N; j0 += 256) {
+        const int j = j0 + (int)threadIdx.x;
+        tile[threadIdx.x] = j < N ? chunks(j) : -1;
+        __syncthreads();
+        const int m = N - j0 < 256 ? N - j0 : 256;
+        for (int t = 0; t < m; ++t) {
+            const int cj = tile[t];
+            rank += (cj > ci || (cj == ci && j0 + t < i)) ? 1 : 0;
+        }
+        __syncthreads();
+    }
+    if (i < N) order[rank] = i;
 }
 
 template <typename F>
@@ -1338,6 +1363,19 @@ SegPlan seg_plan(const Prob& p) {
 
 namespace {
 
+// Packed batches of up to kOrderMaxSeqs sequences get the longest-first sweep order (k_seq_order, one
+// launch of a few microseconds); other batches keep the natural order (seq_order null).
+constexpr int kOrderMaxSeqs = 4096;
+TcWs order_sweeps(const Prob& p, TcWs ws, cudaStream_t st) {
+    if (!p.cu || p.N < 2 || p.N > kOrderMaxSeqs || !ws.seq_order) {
+        ws.seq_order = nullptr;
+        return ws;
+    }
+    k_seq_order<<<(p.N + 255) / 256, 256, 0, st>>>(p.cu, p.N, ws.seq_order);
+    note_launch("tc_seq_order", st);
+    return ws;
+}
+
 cudaError_t launch_intra(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
     cudaError_t e;
     if ((e = set_smem(k_tc_intra, kIntraSmem)) != cudaSuccess) return e;
@@ -1369,8 +1407,9 @@ static bool make_tmap_v(CUtensorMap* m, const Prob& p, const void* v) {
                                           (uint64_t)p.HV * D * 2, 64, 1, kC);
 }
 
-cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
+cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws_in, cudaStream_t st) {
     cudaError_t e;
+    const TcWs ws = order_sweeps(p, ws_in, st);
     if ((e = set_smem(k_tc_fwd_out, kFoSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_fwd_out_half, kFoSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
@@ -1401,9 +1440,10 @@ cudaError_t tc_fwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st, int stages, bool from_saved,
+cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws_in, cudaStream_t st, int stages, bool from_saved,
                    bool fused) {
     cudaError_t e;
+    const TcWs ws = stages >= 2 ? order_sweeps(p, ws_in, st) : ws_in;
     if ((e = set_smem(k_tc_state_fwd, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_fwd_half, kFwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(k_tc_state_load, kLoadSmem)) != cudaSuccess) return e;

@@ -873,7 +873,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGradsThreads, 1)
     extern __shared__ uint8_t smraw[];
     uint8_t* sm = align1024(smraw);
     const int sweep = (int)cluster_index();
-    const int hv = sweep % p.HV, n = sweep / p.HV;
+    const int hv = sweep % p.HV, n = sweep_seq(ws, sweep / p.HV);
     if (cluster_rank() == 0) {
         if (threadIdx.x < kSimt)
             rev_role(p, dht, dh0, ws, &maps.d_o, n, hv, sm);

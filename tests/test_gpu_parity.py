@@ -129,7 +129,11 @@ def test_tensor_core_forward(kda, name):
     o, ht, st = gpu_fwd(kda, inp)
     # the tensor-core path ran; with at most one (sequence, head) sweep per SM each sweep is split by columns
     sweeps, nsm = len(inp.seq_bounds) * FWD_TC[name]["HV"], torch.cuda.get_device_properties(0).multi_processor_count
-    assert kda.load().kda_launch_name(1) == (b"tc_fwd_out_vhalf" if sweeps <= nsm else b"tc_fwd_out")
+    lib = kda.load()
+    names = [lib.kda_launch_name(i) for i in range(lib.kda_last_launch_count())]
+    assert (b"tc_fwd_out_vhalf" if sweeps <= nsm else b"tc_fwd_out") in names, names
+    # packed sequences: the sweeps are launched longest first (a ranking launch before them)
+    assert (b"tc_seq_order" in names) == (inp.cu_seqlens is not None and len(inp.seq_bounds) > 1), names
     ref = oracle.run_inputs(inp, backward=False, chunk_states=True)
     tol = _tol(inp)
     errs = dict(o=rel_l2(to64(o), round_like(ref["o"], inp.torch_dtype)), ht=rel_l2(to64(ht), ref["ht"]),
