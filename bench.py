@@ -178,7 +178,7 @@ MEASURED_TRAFFIC = {
                      "bytes_per_chunk_head": (875.185152e6 + 309.354240e6) / 4096},
     # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change host code (the segment plan, the
     # launch choices) and the two state passes' kernels, not tc_intra
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "196772571a49",
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "5d4485ab5f02",
                  "bytes_per_chunk_head": (269.066240e6 + 249.859328e6) / 4096},
 }
 

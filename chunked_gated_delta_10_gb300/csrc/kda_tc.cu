@@ -41,7 +41,8 @@
 // most one (sequence, value head) sweep per SM each whole sweep of the state,
 // reverse and output passes runs as two CTAs of 64 columns (the _half kernels
 // and the NH = 1 bodies): narrower MMAs and half the epilogue work per chunk
-// step on a chain that is latency-bound there.
+// step on a chain that is latency-bound there. With packed sequences the
+// sweeps start longest first (k_seq_order; a sweep is as long as its sequence).
 //
 // Intermediates live in the workspace as bf16 tiles in exactly the
 // shared-memory operand layout of tc_util.cuh (row-major, 64-column blocks,
