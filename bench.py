@@ -172,14 +172,12 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 # source file is the revision named (sha1 prefix): the captured one, or a later one that leaves
 # that kernel's code as it was (the entry says so).
 MEASURED_TRAFFIC = {
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
-                 "bytes_per_chunk_head": (841.637632e6 + 303.195904e6) / 4096},
-    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "250bc1ece9e4",
-                     "bytes_per_chunk_head": (875.185152e6 + 309.354240e6) / 4096},
-    # captured at kda_tc.cu cef808f4f3f1; the file's later revisions change host code (the segment plan, the
-    # launch choices) and the two state passes' kernels, not tc_intra
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "a9d9606082da",
+                 "bytes_per_chunk_head": (841.621504e6 + 302.663936e6) / 4096},
+    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "a9d9606082da",
+                     "bytes_per_chunk_head": (875.249152e6 + 309.498368e6) / 4096},
     "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "5d4485ab5f02",
-                 "bytes_per_chunk_head": (269.066240e6 + 249.859328e6) / 4096},
+                 "bytes_per_chunk_head": (269.103104e6 + 249.853440e6) / 4096},
 }
 
 
