@@ -176,7 +176,8 @@ MEASURED_TRAFFIC = {
                  "bytes_per_chunk_head": (841.621504e6 + 302.663936e6) / 4096},
     "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "a9d9606082da",
                      "bytes_per_chunk_head": (875.249152e6 + 309.498368e6) / 4096},
-    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "5d4485ab5f02",
+    # captured at kda_tc.cu 5d4485ab5f02; the later revision changes only comments
+    "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "126e2613ba82",
                  "bytes_per_chunk_head": (269.103104e6 + 249.853440e6) / 4096},
 }
 

@@ -461,7 +461,8 @@ struct SegArg {
 // ---------------------------------------------------------------------------
 // tc_state_fwd: one CTA per (value head, sequence[, segment]), 256 threads;
 // thread t owns state row k = t % 128, columns 64 (t / 128) .. +63 in fp32
-// registers. A bf16 copy of S in shared memory feeds the MMAs and is the S_in
+// registers (split by columns, tc_state_fwd_half: 64 columns per CTA, 32 per
+// thread). A bf16 copy of S in shared memory feeds the MMAs and is the S_in
 // checkpoint. Chunk inputs: V (TMA) and e^Gamma_C double-buffered; w with INVb,
 // and K^, single-buffered, each refetched as soon as its MMA has consumed it.
 // delta = INVb V - w S accumulates in one TMEM accumulator and overwrites V in
@@ -760,7 +761,8 @@ __global__ void __launch_bounds__(256, 1) k_tc_seg_combine(Prob p, SegArg sg, in
 
 // ---------------------------------------------------------------------------
 // tc_ds_rev: one CTA per (value head, sequence), chunks in reverse; 256
-// threads, thread t owns dS row k = t % 128, columns 64 (t / 128) .. +63.
+// threads, thread t owns dS row k = t % 128, columns 64 (t / 128) .. +63
+// (tc_ds_rev_half: 64 columns per CTA, 32 per thread).
 // Chunk inputs are single-buffered in two groups, each refetched for the next
 // chunk as soon as its MMAs have consumed it: K^, Q~s, Aqk and dO after the
 // first MMA group, w and e^Gamma_C after the second. dDelta is staged in the
