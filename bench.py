@@ -569,8 +569,9 @@ def gpu_arm(args):
     hout = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in out.items()}
     h2d = sum(t.numel() * t.element_size() for t in hin.values())
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
-    e2e_steps = max(1, min(args.steps, 20))  # as many steps as the timed run: the pipeline's fill and drain
-                                             # (the first inputs in, the last results out) are amortised
+    # at least 20 steps (more when the timed run has more), so that the pipeline's fill and drain (the first
+    # inputs in, the last results out, not overlapped) are amortised as in a long training run
+    e2e_steps = max(20, args.steps)
     xs = [x, {n: torch.empty_like(t) for n, t in x.items()}]
     outs = [out, {n: torch.empty_like(t) for n, t in out.items()}]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
