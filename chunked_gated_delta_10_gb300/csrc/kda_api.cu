@@ -461,7 +461,8 @@ extern "C" kda_status kda_debug_ws_region(const kda_dims* dims, int32_t pass, co
         const char* n;
         size_t off;
     } tab[] = {{"w", L.t_w}, {"invb", L.t_invb}, {"kh", L.t_kh}, {"qs", L.t_qs}, {"vn", L.t_vn}, {"dvn", L.t_dvn},
-               {"aqk", L.t_aqk}, {"inv", L.t_inv}, {"sin", L.t_sin}, {"dso", L.t_dso}, {"egc", L.t_egc}};
+               {"aqk", L.t_aqk}, {"inv", L.t_inv}, {"sin", L.t_sin}, {"dso", L.t_dso}, {"egc", L.t_egc},
+               {"order", L.t_order}};
     if (!L.tc) return KDA_ERR_UNSUPPORTED;
     for (size_t i = 0; i < sizeof(tab) / sizeof(tab[0]); ++i)
         if (strcmp(tab[i].n, name) == 0) {

@@ -126,3 +126,32 @@ def test_stage_qs_and_egc(setup):
 
 def test_stage_dh0(setup):
     assert rel_l2(setup["dh0"], setup["ref"]["dh0"]) < 1e-2
+
+
+def test_sweep_order_longest_first(setup):
+    """Packed sequences: the workspace's sweep order lists the sequences by decreasing chunk count, ties by
+    index (empty and one-token sequences included), after a call that runs the state pass."""
+    import chunked_gated_delta_10_gb300 as kda
+
+    lib = kda.load()
+    lens = [10, 200, 64, 65, 0, 200, 1, 130]
+    inp = kda_inputs.small(seed=52, B=1, T=0, H=1, HV=1, K=128, V=128, dtype="bf16", seq_lens=lens)
+    c = lambda t: None if t is None else t.cuda().contiguous()
+    x = dict(q=c(inp.q), k=c(inp.k), v=c(inp.v), g=c(inp.g), beta=c(inp.beta), h0=c(inp.h0), do=c(inp.do),
+             dht=c(inp.dht))
+    dims = kda.make_dims(x["q"], x["v"], inp.scale, inp.cu_seqlens)
+    vl = kda._Varlen(inp.cu_seqlens, "cuda")
+    wsb = kda.workspace_bytes(dims, kda.PASS_BWD)
+    ws = torch.full((wsb,), 255, dtype=torch.uint8, device="cuda")
+    p = kda._ptr
+    rc = lib.kda_debug_bwd_stages(ctypes.byref(dims), p(x["q"]), p(x["k"]), p(x["v"]), p(x["g"]), p(x["beta"]),
+                                  p(x["h0"]), p(vl.cu), p(vl.idx), p(vl.off), p(x["do"]), p(x["dht"]), None, 2,
+                                  p(ws), wsb, kda._stream())
+    assert rc == 0, kda.STATUS.get(rc)
+    torch.cuda.synchronize()
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.kda_debug_ws_region(ctypes.byref(dims), kda.PASS_BWD, b"order", ctypes.byref(off),
+                                   ctypes.byref(nb)) == 0
+    got = ws[off.value:off.value + 4 * len(lens)].cpu().view(torch.int32).tolist()
+    chunks = [-(-n // 64) for n in lens]
+    assert got == sorted(range(len(lens)), key=lambda i: (-chunks[i], i)), (got, chunks)
