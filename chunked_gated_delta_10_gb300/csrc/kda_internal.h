@@ -87,9 +87,9 @@ cudaError_t tc_bwd(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st,
                    bool fused = false);
 // The per-chunk gradient stage (dq, dk summed over the value heads of a group in the same kernel).
 cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
-// The fused reverse: per (sequence, value head) a cluster of two CTAs, one running the reverse
-// state-gradient sweep and one the per-chunk gradients of its chunks, dS_out and d_delta passed
-// between them in shared memory (H == HV).
+// The fused reverse: per (sequence, value head) a cluster of three CTAs, one running the reverse
+// state-gradient sweep and two the per-chunk gradients of its chunks (alternate chunks each), dS_out
+// and d_delta passed to them in shared memory (H == HV).
 cudaError_t tc_rev_fused(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st);
 
 }  // namespace kda

@@ -70,14 +70,16 @@ struct GS {
 };
 constexpr int kGradsSmem = 1024 + GS::END;
 
-// Shared-memory map of the sweep CTA of a fused reverse pair: the chunk inputs K^, scale Q~, Aqk, dO, w,
-// e^Gamma_C, then two bf16 dS_out tiles and two d_delta tiles (by item parity: one is pushed to the
-// gradient CTA while the next is written). Barriers: [0] K^, Q~, Aqk, dO landed; [1] w, e^Gamma_C
-// landed; [2] MMA; [kFree] a gradient item finished (remote arrivals).
+// Shared-memory map of the sweep CTA of a fused reverse cluster: the chunk inputs K^, scale Q~, Aqk, dO, w,
+// e^Gamma_C, then up to three bf16 dS_out tiles and three d_delta tiles (item i in buffer i % (NG + 1) with
+// NG gradient CTAs: tiles in flight to the gradient CTAs while the next is written). Barriers: [0] K^, Q~,
+// Aqk, dO landed; [1] w, e^Gamma_C landed; [2] MMA; [kFree + g] an item of gradient CTA g finished (remote
+// arrivals).
 struct RevF {
     static constexpr int KH = 0, QS = TCD, AQK = 2 * TCD, DO = 2 * TCD + TCC, W = 3 * TCD + TCC, EGC = 4 * TCD + TCC;
-    static constexpr int S0 = EGC + 1024, DD0 = S0 + 2 * TDD, BARS = DD0 + 2 * TCD, END = BARS + 64;
-    static constexpr int kFree = 3;
+    static constexpr int kBufs = 3;
+    static constexpr int S0 = EGC + 1024, DD0 = S0 + kBufs * TDD, BARS = DD0 + kBufs * TCD, END = BARS + 64;
+    static constexpr int kFree = 3;  // [3], [4]
 };
 static_assert(RevF::END <= GS::END, "the sweep CTA fits the gradient CTA's shared memory");
 
@@ -133,15 +135,19 @@ __device__ __forceinline__ Item make_item(const Prob& p, int64_t w, bool valid) 
 // INV after epilogue B/D; S_in, dS_out, g and e^Gamma_C after phase E; q and k once the final
 // epilogue has read them.
 constexpr int kSimt = 512, kProducerWarp = kSimt / 32, kGradsThreads = kSimt + 32;
+// gradient CTAs per sweep CTA in the fused reverse kernel
+constexpr int kFusedGradCtas = 2;
 
 // GROUPED: HV = G H with G > 1 (the G value heads of a key head each add to its dq and dk).
-// FUSED: the gradient CTA of a fused reverse pair (below): items fw0, fw0 - HV, ..., wlo (the chunks of
-// one sweep, last first), with d_delta and dS_out pushed by the sweep CTA instead of loaded.
+// FUSED: a gradient CTA (cluster rank frank) of a fused reverse cluster (below): items fw0, fw0 - fstep, ...,
+// down to wlo (its share of the chunks of one sweep, last first), with d_delta and dS_out pushed by the sweep
+// CTA instead of loaded.
 template <bool GROUPED, bool FUSED>
 __device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict__ beta, bf16* __restrict__ dq_out,
                                            bf16* __restrict__ dk_out, bf16* __restrict__ dv_out,
                                            float* __restrict__ dg_out, bf16* __restrict__ db_out, const TcWs& ws,
-                                           const GradMaps& maps, uint8_t* sm, int64_t fw0, int64_t wlo) {
+                                           const GradMaps& maps, uint8_t* sm, int64_t fw0, int64_t wlo,
+                                           int64_t fstep = 0, int frank = 1) {
     // [0, 1] inputs (by item parity); [2] phase A, [3] phase B, [4] phase E complete; operands
     // written: [8] of phase B's first part, [5] of its second part, [6] of phase E; [7] accumulators read
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + GS::BARS);
@@ -155,7 +161,7 @@ __device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict
     // groups b, b + grid, ..., each group's G items back to back, so that this CTA keeps their running
     // dq / dk sum
     auto next_w = [&](int64_t w) -> int64_t {
-        if (FUSED) return w - HV;
+        if (FUSED) return w - fstep;
         return GROUPED ? ((w + 1) % G ? w + 1 : w + 1 + (int64_t)(gridDim.x - 1) * G) : w + gridDim.x;
     };
     const int64_t w0 = FUSED ? fw0 : GROUPED ? (int64_t)blockIdx.x * G : blockIdx.x;
@@ -211,7 +217,7 @@ __device__ __forceinline__ void grads_body(const Prob& p, const bf16* __restrict
             };
             int64_t w = w0;
             // (fused) the sweep CTA's barrier on which each finished item frees dS_out's and d_delta's regions
-            const uint32_t rev_free = FUSED ? peer_addr(S(RevF::BARS + 8 * RevF::kFree), 0) : 0u;
+            const uint32_t rev_free = FUSED ? peer_addr(S(RevF::BARS + 8 * (RevF::kFree + frank - 1)), 0) : 0u;
             if (!FUSED || live(w)) {
                 const Item first = make_item(p, w, true);
                 issue_a(first, &bars[0]);
@@ -702,21 +708,25 @@ __global__ void __launch_bounds__(kGradsThreads, 1)
     grads_body<GROUPED, false>(p, beta, dq_out, dk_out, dv_out, dg_out, db_out, ws, maps, align1024(smraw), 0, 0);
 }
 
-// The sweep CTA of a fused reverse pair: the reverse state-gradient pass of one (sequence, value head),
+// The sweep CTA of a fused reverse cluster: the reverse state-gradient pass of one (sequence, value head),
 // chunks last to first, on 512 threads: thread t owns dS row k = t % 128, columns 32 (t / 128) .. +31, in
 // fp32 registers. Per chunk, with dS the gradient of the state leaving it (dS_out):
 //   d_delta = Aqk^T dO + K^ dS,   dS <- e^Gamma_C dS + Q~s^T dO - w^T d_delta,
 // the arithmetic of the split reverse pass (tc_ds_rev) on the same operands, so the tiles are the same
-// bits. Instead of writing dS_out and d_delta to the workspace, it pushes their bf16 tiles into the
-// gradient CTA's input regions (the bytes count on that CTA's input barrier of the item). Item i's two
-// tiles are formed first; their pushes then wait until the gradient CTA has finished item i - 1 (its
-// arrival on barrier kFree), whose factor tiles fill the dS_out region until then. That wait also means the push of item i - 1 has landed, so its source tiles (the other
-// parity's) may be rewritten by item i + 1.
+// bits. Instead of writing dS_out and d_delta to the workspace, it pushes their bf16 tiles into the input
+// regions of gradient CTA g = i % NG (cluster rank 1 + g), whose j-th item item i = g + NG j is (the bytes
+// count on that CTA's input barrier of the item). Item i's two tiles are formed first; their pushes then
+// wait until CTA g has finished its item j - 1 (its arrival on barrier kFree + g), whose factor tiles fill
+// the dS_out region until then. Item i's tiles sit in buffer i % (NG + 1): they are rewritten by item
+// i + NG + 1, which is formed only after the push of item i + NG has waited for CTA g to finish item i, so
+// the push of item i has landed by then.
+template <int NG>
 __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict__ dht, float* __restrict__ dh0,
                                          const TcWs& ws, const CUtensorMap* tm_do, int n, int hv, uint8_t* sm) {
+    static_assert(NG + 1 <= RevF::kBufs && RevF::kFree + NG <= 5, "buffers and barriers of the sweep CTA");
     constexpr int NR = kSimt;  // threads of the sweep
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + RevF::BARS);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 4);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 5);
     int* fail = reinterpret_cast<int*>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int k = tid & 127, vq = tid >> 7;
@@ -725,7 +735,7 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
     seq_range(p, n, bos, eos, c0);
     const int nts = (int)((eos - bos + kC - 1) / kC);
     if (tid == 0) {
-        for (int x = 0; x < 4; ++x) mbar_init(&bars[x], 1);
+        for (int x = 0; x < 5; ++x) mbar_init(&bars[x], 1);
         fence_mbar_init();
         *fail = 0;
     }
@@ -753,9 +763,8 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
         bulk_load(sm + RevF::W, ws.w + ch * TCD, TCD, &bars[1]);
         bulk_load(sm + RevF::EGC, ws.egc + ch * D, 512, &bars[1]);
     };
-    // the gradient CTA (rank 1): its dS_out and d_delta regions and its input barriers
-    const uint32_t pdso = peer_addr(smem_u32(sm + GS::DSO), 1), pddl = peer_addr(smem_u32(sm + GS::DDL), 1);
-    const uint32_t pbar = peer_addr(smem_u32(sm + GS::BARS), 1);
+    // (the gradient CTAs' dS_out and d_delta regions and input barriers: rank 1 + g's copies of these addresses)
+    const uint32_t dso_at = smem_u32(sm + GS::DSO), ddl_at = smem_u32(sm + GS::DDL), bar_at = smem_u32(sm + GS::BARS);
     tc_fence_before();
     group_sync<NR>();
     tc_fence_after();
@@ -770,9 +779,9 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
     int i = 0;
     for (int it = nts - 1; it >= 0; --it, ++i) {
         const uint32_t ph = (uint32_t)i & 1;
-        uint8_t* tS = sm + RevF::S0 + (i & 1) * TDD;   // bf16 dS_out: MMA operand and the pushed tile
-        uint8_t* tD = sm + RevF::DD0 + (i & 1) * TCD;  // bf16 d_delta
-        const uint32_t ibar = pbar + 8u * (uint32_t)(i & 1);  // the gradient CTA's input barrier of item i
+        const int buf = i % (NG + 1), g = i % NG, j = i / NG;  // tile buffer, gradient CTA, its item index
+        uint8_t* tS = sm + RevF::S0 + buf * TDD;   // bf16 dS_out: MMA operand and the pushed tile
+        uint8_t* tD = sm + RevF::DD0 + buf * TCD;  // bf16 d_delta
 #pragma unroll
         for (int c8 = 0; c8 < 32; c8 += 8) st_tile_row8(tS, k, 32 * vq + c8, D, S + c8);
         fence_async_smem();
@@ -820,10 +829,13 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
             mma_commit(&bars[2]);
             // both tiles of item i, as soon as the gradient CTA has finished item i - 1; the gradient CTA
             // keeps d_delta's two 64-column halves TCD bytes apart
-            if (i > 0 && !mbar_wait_cluster(&bars[RevF::kFree], (uint32_t)(i - 1) & 1, ws.status, 62)) {
+            if (j > 0 && !mbar_wait_cluster(&bars[RevF::kFree + g], (uint32_t)(j - 1) & 1, ws.status, 62)) {
                 *(volatile int*)fail = 1;  // (read after the next group barrier)
             } else {
-                bulk_push(pdso, tS, TDD, ibar);
+                const uint32_t r = 1 + (uint32_t)g;
+                const uint32_t ibar = peer_addr(bar_at, r) + 8u * (uint32_t)(j & 1);  // CTA g's input barrier
+                const uint32_t pddl = peer_addr(ddl_at, r);
+                bulk_push(peer_addr(dso_at, r), tS, TDD, ibar);
                 bulk_push(pddl, tD, TCD / 2, ibar);
                 bulk_push(pddl + TCD, tD + TCD / 2, TCD / 2, ibar);
             }
@@ -851,7 +863,7 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
 #pragma unroll
             for (int j = 0; j < 32; ++j) dst[j] = S[j];
         }
-    } else if (tid == 0) {  // a wait gave up: let copies already issued land before the pair exits
+    } else if (tid == 0) {  // a wait gave up: let copies already issued land before the cluster exits
         const long long t0 = clock64();
         while (clock64() - t0 < 2000000) {
         }
@@ -862,11 +874,13 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
 }
 
 // Fused reverse (state-gradient sweep and per-chunk gradients in one launch, dS_out and d_delta kept on
-// chip): one cluster of two CTAs per (sequence, value head), on two SMs. CTA 0 runs the sweep (rev_role,
-// warps 0..15; warp 16 only meets the cluster barriers), CTA 1 the gradient work of the sweep's chunks in
-// the same order (grads_body), its dS_out and d_delta inputs pushed by CTA 0 into its shared memory.
-// Equal key and value heads only (the grouped sum of dq, dk runs across sweeps).
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGradsThreads, 1)
+// chip): one cluster of 1 + NG CTAs per (sequence, value head), on 1 + NG SMs. CTA 0 runs the sweep
+// (rev_role, warps 0..15; warp 16 only meets the cluster barriers); CTA 1 + g runs the gradient work of the
+// sweep's chunks i with i % NG == g, in the sweep's order (grads_body), its dS_out and d_delta inputs pushed
+// by CTA 0 into its shared memory. Equal key and value heads only (the grouped sum of dq, dk runs across
+// sweeps).
+template <int NG>
+__global__ void __cluster_dims__(NG + 1, 1, 1) __launch_bounds__(kGradsThreads, 1)
     k_tc_rev_fused(Prob p, const float* __restrict__ dht, float* __restrict__ dh0, const bf16* __restrict__ beta,
                    bf16* __restrict__ dq_out, bf16* __restrict__ dk_out, bf16* __restrict__ dv_out,
                    float* __restrict__ dg_out, bf16* __restrict__ db_out, TcWs ws, const __grid_constant__ GradMaps maps) {
@@ -874,19 +888,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGradsThreads, 1)
     uint8_t* sm = align1024(smraw);
     const int sweep = (int)cluster_index();
     const int hv = sweep % p.HV, n = sweep_seq(ws, sweep / p.HV);
-    if (cluster_rank() == 0) {
+    const int rank = (int)cluster_rank();
+    if (rank == 0) {
         if (threadIdx.x < kSimt)
-            rev_role(p, dht, dh0, ws, &maps.d_o, n, hv, sm);
+            rev_role<NG>(p, dht, dh0, ws, &maps.d_o, n, hv, sm);
         else
-            cluster_sync();  // (the pair's start barrier)
+            cluster_sync();  // (the cluster's start barrier)
     } else {
         int64_t bos, eos, c0;
         seq_range(p, n, bos, eos, c0);
         const int64_t nts = (eos - bos + kC - 1) / kC;
+        // this CTA's chunks of the sweep: it = nts - rank, nts - rank - NG, ... (none when nts < rank)
         grads_body<false, true>(p, beta, dq_out, dk_out, dv_out, dg_out, db_out, ws, maps, sm,
-                                (c0 + nts - 1) * p.HV + hv, c0 * p.HV + hv);
+                                (c0 + nts - rank) * p.HV + hv, c0 * p.HV + hv, (int64_t)NG * p.HV, rank);
     }
-    cluster_sync();  // neither CTA leaves while the other may still reach its shared memory
+    cluster_sync();  // no CTA leaves while another may still reach its shared memory
 }
 
 bool make_grad_maps(const Prob& p, const IO& io, GradMaps* m) {
@@ -928,14 +944,15 @@ cudaError_t tc_grads(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t s
 }
 
 cudaError_t tc_rev_fused(const Prob& p, const IO& io, const TcWs& ws, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(k_tc_rev_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
+    constexpr int NG = kFusedGradCtas;
+    cudaError_t e = cudaFuncSetAttribute(k_tc_rev_fused<NG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGradsSmem);
     if (e != cudaSuccess) return e;
     if (p.HV != p.H) return cudaErrorInvalidValue;
     const int64_t sweeps = (int64_t)p.N * p.HV;
     if (sweeps == 0) return cudaSuccess;
     GradMaps m;
     if (!make_grad_maps(p, io, &m)) return cudaErrorInvalidValue;
-    k_tc_rev_fused<<<(unsigned)(2 * sweeps), kGradsThreads, kGradsSmem, st>>>(
+    k_tc_rev_fused<NG><<<(unsigned)((NG + 1) * sweeps), kGradsThreads, kGradsSmem, st>>>(
         p, io.dht, io.dh0, (const bf16*)io.beta, (bf16*)io.dq, (bf16*)io.dk, (bf16*)io.dv, io.dg, (bf16*)io.dbeta,
         ws, m);
     note_launch("tc_rev_fused", st);

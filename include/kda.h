@@ -152,10 +152,11 @@ kda_status kda_chunk_bwd(const kda_dims* dims, const void* q, const void* k, con
  * structure of the FlashKDA backward (K2) page's kernel: one sweep per
  * (sequence, head) over the chunks from last to first with dS resident in
  * shared memory, the per-chunk gradient work inside the sweep).
- * Per (sequence, value head) a cluster of two CTAs on two SMs: one carries dS
- * in registers through the sweep, the other computes each chunk's dq, dk, dv,
- * dbeta and dg; each chunk's dS_out and d_delta tiles pass from the first to
- * the second through distributed shared memory instead of the workspace.
+ * Per (sequence, value head) a cluster of three CTAs on three SMs: one carries
+ * dS in registers through the sweep, the other two compute the chunks' dq, dk,
+ * dv, dbeta and dg (alternate chunks each); each chunk's dS_out and d_delta
+ * tiles pass from the first to the one that takes the chunk through
+ * distributed shared memory instead of the workspace.
  * Arguments, layouts, workspace and errors as kda_chunk_bwd, plus
  * KDA_ERR_UNSUPPORTED off the tensor-core path (bf16, K = V = 128) or when
  * HV != H. The split path (kda_chunk_bwd) is the faster one on the workloads

@@ -1,13 +1,13 @@
 """GPU: the fused reverse (kda_chunk_bwd_fused: the reverse state-gradient sweep and the per-chunk
-gradients in one launch, a cluster of two CTAs per (sequence, head) passing dS_out and d_delta through
-shared memory) against the split backward (kda_chunk_bwd) bit for bit, and against the fp64 oracle
-over whole tensors.
+gradients in one launch, a cluster of three CTAs per (sequence, head), the sweep CTA passing dS_out and
+d_delta to two gradient CTAs through shared memory) against the split backward (kda_chunk_bwd) bit for
+bit, and against the fp64 oracle over whole tensors.
 
 The two paths run the same arithmetic on the same operand values (the sweep CTA forms each chunk's
 dS_out and d_delta tiles exactly as the split reverse pass does), so every gradient must be equal, not
-merely close. Cases: a single token, one exact chunk, ragged tails, packed sequences with empty and
-length-1 members, no initial state and no dht, a long sequence whose forward state pass runs in
-segments, and the benchmark-sized workloads.
+merely close. Cases: a single token (one gradient CTA without chunks), one exact chunk, ragged tails,
+packed sequences with empty and length-1 members, no initial state and no dht, a long sequence whose
+forward state pass runs in segments, and the benchmark-sized workloads.
 """
 import functools
 
