@@ -172,10 +172,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 # source file is the revision named (sha1 prefix): the captured one, or a later one that leaves
 # that kernel's code as it was (the entry says so).
 MEASURED_TRAFFIC = {
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "a9d9606082da",
-                 "bytes_per_chunk_head": (841.621504e6 + 302.663936e6) / 4096},
-    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "a9d9606082da",
-                     "bytes_per_chunk_head": (875.249152e6 + 309.498368e6) / 4096},
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "145f696ca185",
+                 "bytes_per_chunk_head": (841.820928e6 + 302.801408e6) / 4096},
+    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "145f696ca185",
+                     "bytes_per_chunk_head": (875.679488e6 + 311.447296e6) / 4096},
     # captured at kda_tc.cu 5d4485ab5f02; the later revision changes only comments
     "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "126e2613ba82",
                  "bytes_per_chunk_head": (269.103104e6 + 249.853440e6) / 4096},
