@@ -172,9 +172,10 @@ def kernel_cost(name, B, T, H, HV, K, V, in_bytes=2, C=64, nck=None):
 # source file is the revision named (sha1 prefix): the captured one, or a later one that leaves
 # that kernel's code as it was (the entry says so).
 MEASURED_TRAFFIC = {
-    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "145f696ca185",
+    # tc_grads and tc_rev_fused captured at kda_tc_grads.cu 145f696ca185; the later revision changes only a comment
+    "tc_grads": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "519ea07f922c",
                  "bytes_per_chunk_head": (841.820928e6 + 302.801408e6) / 4096},
-    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "145f696ca185",
+    "tc_rev_fused": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc_grads.cu", "sha1": "519ea07f922c",
                      "bytes_per_chunk_head": (875.679488e6 + 311.447296e6) / 4096},
     # captured at kda_tc.cu 5d4485ab5f02; the later revision changes only comments
     "tc_intra": {"source": "chunked_gated_delta_10_gb300/csrc/kda_tc.cu", "sha1": "126e2613ba82",

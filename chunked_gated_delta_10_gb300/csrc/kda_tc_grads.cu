@@ -768,7 +768,7 @@ __device__ __forceinline__ void rev_role(const Prob& p, const float* __restrict_
     tc_fence_before();
     group_sync<NR>();
     tc_fence_after();
-    cluster_sync();  // both CTAs' barriers are initialised
+    cluster_sync();  // every CTA's barriers are initialised
     const uint32_t tmem = *tslot;
     const uint32_t lq = (uint32_t)(32 * (warp & 3)) << 16;
     if (tid == 0 && nts > 0) {
