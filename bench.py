@@ -387,8 +387,13 @@ def reference_arm(args):
         v, used, dt, sample = oracle_sample_any(inp)
         vals.append(v)
     value = statistics.median(vals)
+    tokens = int(inp.q.shape[0]) * int(inp.q.shape[1])
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tokens / value * 1e3 if value > 0 else None,
+            "timing": "each timed step runs the bounded sample (cpu_baseline.sample); value is the median rate over "
+                      "the steps and ms_per_step the whole workload's step at that rate",
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(inp, ws),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": used, "kind": "oracle", "sample": sample},
